@@ -1,0 +1,392 @@
+/*
+ * fp64 CPU oracle for padding-free packed bidirectional attention.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the independent definition that the CUDA
+ * library is checked against. Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg load it. It shares no code, header, table or helper
+ * with the CUDA library, and the CUDA library never calls it.
+ *
+ * Sources (all on the page "Source code for gigl.nn.packed_attention"):
+ *   - module docstring, "Data flow of a packed forward": pack_sequences turns
+ *     lengths into flat_index and cu_seqlens; the packed buffer is
+ *     grid.flatten()[flat_index]; every sequence attends only to itself.
+ *   - module docstring, "Constraints": cu_seqlens is int32, so the token count
+ *     must fit in int32.
+ *   - module docstring, "Example": lengths [3, 1, 2] with max_seq_len 3 give
+ *     flat_index [0, 1, 2, 3, 6, 7]; output shapes [6, 2, 8] and, with the
+ *     first-token query, [3, 2, 8].
+ *   - function _padded_packed_attention: the reference path. Tokens are laid out
+ *     on a zero-padded [num_sequences, max_seq_len] grid, padded keys are masked,
+ *     scaled-dot-product attention runs per sequence and head, outputs are
+ *     unpadded; in first-token mode each sequence's query sits in its first row
+ *     and only that row is kept.
+ *   - function packed_attention: every sequence must hold at least one token.
+ *   - custom op gigl::varlen_attention: returns the output and the log-sum-exp
+ *     of the scaled scores (natural log).
+ *
+ * Readings where the pages leave a step open:
+ *   - masking of padded keys: the pages add finfo.min/2 to their scores; since
+ *     every row has at least one real key that bias sends their weight to exactly
+ *     zero, so here padded keys are excluded from the softmax outright.
+ *   - lengths above max_seq_len would alias the next grid row: rejected like 0.
+ *   - scale is an explicit argument (the pages use SDPA's default 1/sqrt(d)).
+ *   - log-sum-exp layout: [H, Nq] fp64, natural log, no row padding.
+ *   - the backward is the analytic gradient of softmax attention (the pages
+ *     hand it to aten's backward kernel, which computes the same gradient).
+ *
+ * Everything is fp64, written as plain loops over the definition, with a
+ * pthread pool over (sequence, head) pairs and no blocking or fusion.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdatomic.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORC_OK 0
+#define ORC_BAD_LENGTH 2
+#define ORC_OVERFLOW 3
+#define ORC_NO_MEMORY 4
+#define ORC_INVALID 5
+
+/* ------------------------------------------------------------------------- */
+/* pack_sequences: "Data flow of a packed forward" and "Example".             */
+/*   cu_seqlens[0] = 0, cu_seqlens[i+1] = cu_seqlens[i] + L_i                 */
+/*   flat_index lists i*S + j for i ascending, then j ascending, j < L_i.     */
+/* ------------------------------------------------------------------------- */
+int orc_pack_sequences(const int32_t* lengths, int64_t B, int64_t S,
+                       int64_t* flat_index, int32_t* cu_seqlens, int64_t* num_tokens) {
+  if (B < 0 || S < 1) return ORC_INVALID;
+  int64_t total = 0;
+  for (int64_t i = 0; i < B; ++i) {
+    if (lengths[i] < 1 || lengths[i] > S) return ORC_BAD_LENGTH;
+    total += lengths[i];
+  }
+  if (total >= ((int64_t)1 << 31)) return ORC_OVERFLOW;
+  *num_tokens = total;
+  if (cu_seqlens) {
+    cu_seqlens[0] = 0;
+    for (int64_t i = 0; i < B; ++i) cu_seqlens[i + 1] = cu_seqlens[i] + lengths[i];
+  }
+  if (flat_index) {
+    int64_t t = 0;
+    for (int64_t i = 0; i < B; ++i)
+      for (int64_t j = 0; j < lengths[i]; ++j) flat_index[t++] = i * S + j;
+  }
+  return ORC_OK;
+}
+
+/* grid.flatten()[flat_index]: packed row t is padded row flat_index[t]. */
+void orc_gather_rows(const uint8_t* padded, const int64_t* flat_index, int64_t N,
+                     int64_t row_bytes, uint8_t* packed) {
+  for (int64_t t = 0; t < N; ++t)
+    memcpy(packed + t * row_bytes, padded + flat_index[t] * row_bytes, (size_t)row_bytes);
+}
+
+/* to_dense_batch with fill value 0: padded row i*S+j holds packed row
+ * cu_seqlens[i]+j when j < L_i, zeros otherwise. */
+void orc_scatter_rows(const uint8_t* packed, const int32_t* cu_seqlens, int64_t B, int64_t S,
+                      int64_t row_bytes, uint8_t* padded) {
+  for (int64_t i = 0; i < B; ++i) {
+    int64_t len = cu_seqlens[i + 1] - cu_seqlens[i];
+    for (int64_t j = 0; j < S; ++j) {
+      uint8_t* dst = padded + (i * S + j) * row_bytes;
+      if (j < len)
+        memcpy(dst, packed + ((int64_t)cu_seqlens[i] + j) * row_bytes, (size_t)row_bytes);
+      else
+        memset(dst, 0, (size_t)row_bytes);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* A small pthread pool over (sequence, head) pairs.                          */
+/* ------------------------------------------------------------------------- */
+typedef void (*orc_task_fn)(void* ctx, int64_t item, double* scratch);
+
+typedef struct {
+  orc_task_fn fn;
+  void* ctx;
+  int64_t num_items;
+  size_t scratch_doubles;
+  atomic_llong next;
+  atomic_int failed;
+} orc_pool;
+
+static void* orc_worker(void* arg) {
+  orc_pool* pool = (orc_pool*)arg;
+  double* scratch = (double*)malloc(pool->scratch_doubles * sizeof(double) + 64);
+  if (!scratch) {
+    atomic_store(&pool->failed, 1);
+    return NULL;
+  }
+  for (;;) {
+    int64_t item = atomic_fetch_add(&pool->next, 1);
+    if (item >= pool->num_items) break;
+    pool->fn(pool->ctx, item, scratch);
+  }
+  free(scratch);
+  return NULL;
+}
+
+static int orc_run(orc_task_fn fn, void* ctx, int64_t num_items, size_t scratch_doubles,
+                   int nthreads) {
+  orc_pool pool;
+  pool.fn = fn;
+  pool.ctx = ctx;
+  pool.num_items = num_items;
+  pool.scratch_doubles = scratch_doubles;
+  atomic_init(&pool.next, 0);
+  atomic_init(&pool.failed, 0);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t threads[256];
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&threads[started], NULL, orc_worker, &pool) != 0) break;
+    ++started;
+  }
+  orc_worker(&pool);
+  for (int t = 0; t < started; ++t) pthread_join(threads[t], NULL);
+  return atomic_load(&pool.failed) ? ORC_NO_MEMORY : ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Forward on the padded grid (_padded_packed_attention).                     */
+/* q: [Nq, H, D] with Nq = N (full) or B (first token). k, v: [N, H, D].      */
+/* o: shaped like q. lse: [H, Nq].                                            */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  const double *q, *k, *v;
+  const int32_t* cu;
+  int64_t B, S, H, D, Nq;
+  double scale;
+  int first_token;
+  double *o, *lse;
+} orc_fwd_ctx;
+
+/* One (sequence i, head h): lay the sequence out as a zero-padded S-row slab of
+ * this head (the padded grid of the reference path), then run masked softmax
+ * attention for every real query row and unpad the result. */
+static void orc_fwd_task(void* vctx, int64_t item, double* scratch) {
+  orc_fwd_ctx* c = (orc_fwd_ctx*)vctx;
+  const int64_t i = item / c->H, h = item % c->H;
+  const int64_t S = c->S, D = c->D, H = c->H;
+  const int64_t start = c->cu[i], len = (int64_t)c->cu[i + 1] - c->cu[i];
+  double* Qp = scratch;           /* [S][D] */
+  double* Kp = Qp + S * D;        /* [S][D] */
+  double* Vp = Kp + S * D;        /* [S][D] */
+  double* s = Vp + S * D;         /* [S] scores of one query row */
+  memset(Qp, 0, sizeof(double) * (size_t)(3 * S * D));
+  for (int64_t j = 0; j < len; ++j) {
+    for (int64_t c2 = 0; c2 < D; ++c2) {
+      Kp[j * D + c2] = c->k[((start + j) * H + h) * D + c2];
+      Vp[j * D + c2] = c->v[((start + j) * H + h) * D + c2];
+    }
+  }
+  /* First-token mode: the sequence's single query occupies its first row. */
+  const int64_t num_rows = c->first_token ? 1 : len;
+  for (int64_t r = 0; r < num_rows; ++r) {
+    const int64_t qrow = c->first_token ? i : start + r;
+    for (int64_t c2 = 0; c2 < D; ++c2) Qp[r * D + c2] = c->q[(qrow * H + h) * D + c2];
+  }
+  for (int64_t r = 0; r < num_rows; ++r) {
+    const int64_t orow = c->first_token ? i : start + r;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < S; ++j) {
+      if (j >= len) continue; /* padded key: excluded from the softmax */
+      double acc = 0.0;
+      for (int64_t c2 = 0; c2 < D; ++c2) acc += Qp[r * D + c2] * Kp[j * D + c2];
+      s[j] = c->scale * acc;
+      if (s[j] > m) m = s[j];
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < len; ++j) {
+      s[j] = exp(s[j] - m);
+      z += s[j];
+    }
+    double* out = c->o + (orow * H + h) * D;
+    for (int64_t c2 = 0; c2 < D; ++c2) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < len; ++j) acc += s[j] * Vp[j * D + c2];
+      out[c2] = acc / z;
+    }
+    if (c->lse) c->lse[h * c->Nq + orow] = m + log(z);
+  }
+}
+
+int orc_attention_fwd(const double* q, const double* k, const double* v, const int32_t* cu,
+                      int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                      int first_token, double* o, double* lse, int nthreads) {
+  if (B < 0 || S < 1 || H < 1 || D < 1) return ORC_INVALID;
+  for (int64_t i = 0; i < B; ++i) {
+    int64_t len = (int64_t)cu[i + 1] - cu[i];
+    if (len < 1 || len > S) return ORC_BAD_LENGTH;
+  }
+  orc_fwd_ctx ctx = {q, k, v, cu, B, S, H, D, first_token ? B : (B ? cu[B] : 0),
+                     scale, first_token, o, lse};
+  return orc_run(orc_fwd_task, &ctx, B * H, (size_t)(3 * S * D + S), nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Forward for chosen (row, head) pairs, read straight from the packed        */
+/* buffers: for large inputs, where the whole output is too costly.          */
+/* rows[r] is a packed token index (full mode) or a sequence index (first     */
+/* token mode). o: [R, D], lse: [R].                                          */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  const double *q, *k, *v;
+  const int32_t* cu;
+  int64_t B, H, D;
+  double scale;
+  int first_token;
+  const int64_t *rows, *heads;
+  double *o, *lse;
+} orc_rows_ctx;
+
+static int64_t orc_sequence_of(const int32_t* cu, int64_t B, int64_t t) {
+  int64_t lo = 0, hi = B; /* find i with cu[i] <= t < cu[i+1] */
+  while (hi - lo > 1) {
+    int64_t mid = (lo + hi) / 2;
+    if (cu[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+static void orc_rows_task(void* vctx, int64_t r, double* s) {
+  orc_rows_ctx* c = (orc_rows_ctx*)vctx;
+  const int64_t H = c->H, D = c->D, h = c->heads[r];
+  const int64_t i = c->first_token ? c->rows[r] : orc_sequence_of(c->cu, c->B, c->rows[r]);
+  const int64_t start = c->cu[i], len = (int64_t)c->cu[i + 1] - c->cu[i];
+  const double* qv = c->q + (c->rows[r] * H + h) * D;
+  double m = -INFINITY;
+  for (int64_t j = 0; j < len; ++j) {
+    const double* kv = c->k + ((start + j) * H + h) * D;
+    double acc = 0.0;
+    for (int64_t c2 = 0; c2 < D; ++c2) acc += qv[c2] * kv[c2];
+    s[j] = c->scale * acc;
+    if (s[j] > m) m = s[j];
+  }
+  double z = 0.0;
+  for (int64_t j = 0; j < len; ++j) {
+    s[j] = exp(s[j] - m);
+    z += s[j];
+  }
+  for (int64_t c2 = 0; c2 < D; ++c2) {
+    double acc = 0.0;
+    for (int64_t j = 0; j < len; ++j) acc += s[j] * c->v[((start + j) * H + h) * D + c2];
+    c->o[r * D + c2] = acc / z;
+  }
+  c->lse[r] = m + log(z);
+}
+
+int orc_attention_fwd_rows(const double* q, const double* k, const double* v,
+                           const int32_t* cu, int64_t B, int64_t H, int64_t D, double scale,
+                           int first_token, const int64_t* rows, const int64_t* heads,
+                           int64_t R, double* o, double* lse, int nthreads) {
+  int64_t max_len = 0;
+  for (int64_t i = 0; i < B; ++i) {
+    int64_t len = (int64_t)cu[i + 1] - cu[i];
+    if (len < 1) return ORC_BAD_LENGTH;
+    if (len > max_len) max_len = len;
+  }
+  orc_rows_ctx ctx = {q, k, v, cu, B, H, D, scale, first_token, rows, heads, o, lse};
+  return orc_run(orc_rows_task, &ctx, R, (size_t)max_len, nthreads);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Backward: analytic gradient of softmax attention, per (sequence, head).    */
+/* For each query row r, with P_r = softmax_j(scale * q_r . k_j):             */
+/*   O_r   = sum_j P_rj v_j                                                   */
+/*   Dlt_r = dO_r . O_r                                                       */
+/*   dS_rj = P_rj * (dO_r . v_j - Dlt_r)                                      */
+/*   dq_r  = scale * sum_j dS_rj k_j                                          */
+/*   dk_j += scale * dS_rj q_r                                                */
+/*   dv_j += P_rj dO_r                                                        */
+/* Every (sequence, head) writes a disjoint slice of dq, dk, dv.              */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  const double *q, *k, *v, *dout;
+  const int32_t* cu;
+  int64_t B, H, D;
+  double scale;
+  int first_token;
+  double *dq, *dk, *dv;
+} orc_bwd_ctx;
+
+static void orc_bwd_task(void* vctx, int64_t item, double* scratch) {
+  orc_bwd_ctx* c = (orc_bwd_ctx*)vctx;
+  const int64_t i = item / c->H, h = item % c->H;
+  const int64_t H = c->H, D = c->D;
+  const int64_t start = c->cu[i], len = (int64_t)c->cu[i + 1] - c->cu[i];
+  double* p = scratch;       /* [len] */
+  double* orow = p + len;    /* [D] */
+  for (int64_t j = 0; j < len; ++j)
+    for (int64_t c2 = 0; c2 < D; ++c2) {
+      c->dk[((start + j) * H + h) * D + c2] = 0.0;
+      c->dv[((start + j) * H + h) * D + c2] = 0.0;
+    }
+  const int64_t num_rows = c->first_token ? 1 : len;
+  for (int64_t r = 0; r < num_rows; ++r) {
+    const int64_t qrow = c->first_token ? i : start + r;
+    const double* qv = c->q + (qrow * H + h) * D;
+    const double* gv = c->dout + (qrow * H + h) * D;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < len; ++j) {
+      const double* kv = c->k + ((start + j) * H + h) * D;
+      double acc = 0.0;
+      for (int64_t c2 = 0; c2 < D; ++c2) acc += qv[c2] * kv[c2];
+      p[j] = c->scale * acc;
+      if (p[j] > m) m = p[j];
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < len; ++j) {
+      p[j] = exp(p[j] - m);
+      z += p[j];
+    }
+    for (int64_t j = 0; j < len; ++j) p[j] /= z;
+    for (int64_t c2 = 0; c2 < D; ++c2) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < len; ++j) acc += p[j] * c->v[((start + j) * H + h) * D + c2];
+      orow[c2] = acc;
+    }
+    double delta = 0.0;
+    for (int64_t c2 = 0; c2 < D; ++c2) delta += gv[c2] * orow[c2];
+    double* dqv = c->dq + (qrow * H + h) * D;
+    for (int64_t c2 = 0; c2 < D; ++c2) dqv[c2] = 0.0;
+    for (int64_t j = 0; j < len; ++j) {
+      const double* kv = c->k + ((start + j) * H + h) * D;
+      const double* vv = c->v + ((start + j) * H + h) * D;
+      double dp = 0.0;
+      for (int64_t c2 = 0; c2 < D; ++c2) dp += gv[c2] * vv[c2];
+      const double ds = p[j] * (dp - delta);
+      double* dkv = c->dk + ((start + j) * H + h) * D;
+      double* dvv = c->dv + ((start + j) * H + h) * D;
+      for (int64_t c2 = 0; c2 < D; ++c2) {
+        dqv[c2] += c->scale * ds * kv[c2];
+        dkv[c2] += c->scale * ds * qv[c2];
+        dvv[c2] += p[j] * gv[c2];
+      }
+    }
+  }
+}
+
+int orc_attention_bwd(const double* q, const double* k, const double* v, const double* dout,
+                      const int32_t* cu, int64_t B, int64_t H, int64_t D, double scale,
+                      int first_token, double* dq, double* dk, double* dv, int nthreads) {
+  int64_t max_len = 0;
+  for (int64_t i = 0; i < B; ++i) {
+    int64_t len = (int64_t)cu[i + 1] - cu[i];
+    if (len < 1) return ORC_BAD_LENGTH;
+    if (len > max_len) max_len = len;
+  }
+  orc_bwd_ctx ctx = {q, k, v, dout, cu, B, H, D, scale, first_token, dq, dk, dv};
+  return orc_run(orc_bwd_task, &ctx, B * H, (size_t)(max_len + D), nthreads);
+}
+
+int orc_hardware_threads(void) {
+  long n = sysconf(_SC_NPROCESSORS_ONLN);
+  return n > 0 ? (int)n : 1;
+}

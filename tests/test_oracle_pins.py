@@ -1,0 +1,338 @@
+"""Pins the fp64 oracle to facts fixed outside the oracle itself (CPU only).
+
+Each test checks the oracle against one of:
+  * values printed on the pages (tests/golden, each with its citation);
+  * closed forms of softmax attention;
+  * library routines on special cases (torch SDPA and autograd in fp64,
+    scipy's softmax, numpy boolean indexing);
+  * finite differences of the oracle's own forward (for the backward);
+  * invariants of the definition.
+A dropped term, a wrong sign or index, or a transposed operand anywhere in the
+oracle makes at least one of these fail.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+import oracle
+from oracle import OracleError
+from padding_free_packed_gb300 import workloads
+
+
+def _random_case(seed, b_max=7, s_max=13, h=3, d=8):
+    rng = np.random.default_rng(seed)
+    b = int(rng.integers(1, b_max + 1))
+    s = int(rng.integers(1, s_max + 1))
+    lengths = rng.integers(1, s + 1, b).astype(np.int32)
+    n = int(lengths.sum())
+    q = rng.standard_normal((n, h, d))
+    k = rng.standard_normal((n, h, d))
+    v = rng.standard_normal((n, h, d))
+    return lengths, s, q, k, v
+
+
+def _padded(x, lengths, s):
+    """Test-side padding with numpy boolean indexing: [B, S, ...], zeros at pads."""
+    b = len(lengths)
+    mask = np.arange(s)[None, :] < np.asarray(lengths)[:, None]
+    grid = np.zeros((b, s) + x.shape[1:], dtype=x.dtype)
+    grid[mask] = x
+    return grid, mask
+
+
+# --------------------------------------------------------------------------- pack
+
+def test_pack_worked_example(golden):
+    g = golden("pack_worked_example.txt")
+    flat, cu, n = oracle.pack_sequences(g["lengths"], g["max_seq_len"][0])
+    assert flat.tolist() == g["flat_index"]
+    assert cu.tolist() == g["cu_seqlens"]
+    assert n == g["num_tokens"][0]
+
+
+def test_pack_cu_seqlens_example(golden):
+    g = golden("pack_cu_seqlens_example.txt")
+    flat, cu, n = oracle.pack_sequences(g["lengths"], g["max_seq_len"][0])
+    assert cu.tolist() == g["cu_seqlens"]
+    assert n == g["num_tokens"][0]
+    assert cu.dtype == np.int32
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_pack_invariants(seed):
+    rng = np.random.default_rng(100 + seed)
+    b = int(rng.integers(1, 60))
+    s = int(rng.integers(1, 50))
+    lengths = rng.integers(1, s + 1, b).astype(np.int32)
+    flat, cu, n = oracle.pack_sequences(lengths, s)
+    assert n == int(lengths.sum())
+    assert cu.tolist() == [0] + np.cumsum(lengths).tolist()
+    assert np.all(np.diff(flat) > 0)
+    seq = flat // s
+    assert np.all(np.diff(seq) >= 0)
+    assert np.bincount(seq, minlength=b).tolist() == lengths.tolist()
+    assert np.all(flat % s < lengths[seq])
+    # flat_index lists exactly the real cells of the padded grid (numpy's own
+    # boolean-mask order is row-major, i.e. i ascending then j ascending).
+    mask = np.arange(s)[None, :] < lengths[:, None]
+    assert flat.tolist() == np.flatnonzero(mask.reshape(-1)).tolist()
+
+
+def test_pack_edge_cases():
+    flat, cu, n = oracle.pack_sequences(np.zeros(0, np.int32), 4)
+    assert n == 0 and cu.tolist() == [0] and flat.size == 0
+    flat, cu, n = oracle.pack_sequences([1] * 5, 4)
+    assert flat.tolist() == [0, 4, 8, 12, 16]
+    flat, cu, n = oracle.pack_sequences([4, 4], 4)
+    assert flat.tolist() == list(range(8))
+    with pytest.raises(OracleError) as e:
+        oracle.pack_sequences([3, 0, 2], 4)
+    assert e.value.code == 2
+    with pytest.raises(OracleError) as e:
+        oracle.pack_sequences([3, 5], 4)
+    assert e.value.code == 2
+    with pytest.raises(OracleError) as e:
+        oracle.pack_sequences([-1], 4)
+    assert e.value.code == 2
+    big = 1 << 30
+    _, cu, n = oracle.pack_sequences([big, big - 1], big, want_index=False)
+    assert n == (1 << 31) - 1
+    with pytest.raises(OracleError) as e:
+        oracle.pack_sequences([big, big], big, want_index=False)
+    assert e.value.code == 3
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_gather_scatter_round_trip(seed):
+    rng = np.random.default_rng(200 + seed)
+    b, s = int(rng.integers(1, 9)), int(rng.integers(1, 17))
+    lengths = rng.integers(1, s + 1, b).astype(np.int32)
+    grid = rng.standard_normal((b, s, 3, 5)).astype(np.float32)
+    flat, cu, n = oracle.pack_sequences(lengths, s)
+    packed = oracle.gather_rows(grid.reshape(b * s, 3, 5), flat)
+    mask = np.arange(s)[None, :] < lengths[:, None]
+    np.testing.assert_array_equal(packed, grid[mask])
+    back = oracle.scatter_rows(packed, cu, s)
+    np.testing.assert_array_equal(back[mask], grid[mask])
+    assert np.all(back[~mask] == 0)
+
+
+# --------------------------------------------------------------------------- forward
+
+def test_forward_shapes_worked_example(golden):
+    g = golden("pack_worked_example.txt")
+    _, cu, n = oracle.pack_sequences(g["lengths"], g["max_seq_len"][0])
+    h, d = g["heads"][0], g["head_dim"][0]
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((n, h, d))
+    o, lse = oracle.attention_fwd(x, x, x, cu, g["max_seq_len"][0], 1 / math.sqrt(d))
+    assert list(o.shape) == g["full_output_shape"]
+    assert lse.shape == (h, n)
+    o1, _ = oracle.attention_fwd(x[cu[:-1]], x, x, cu, g["max_seq_len"][0], 1 / math.sqrt(d),
+                                 first_token=True)
+    assert list(o1.shape) == g["first_token_output_shape"]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_forward_matches_sdpa_on_padded_grid(seed):
+    """The reference path itself: SDPA with padded keys masked, on a padded grid."""
+    lengths, s, q, k, v = _random_case(seed)
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    scale = 0.37 + 0.1 * seed
+    o, lse = oracle.attention_fwd(q, k, v, cu, s, scale)
+    qg, mask = _padded(q, lengths, s)
+    kg, _ = _padded(k, lengths, s)
+    vg, _ = _padded(v, lengths, s)
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (qg, kg, vg))
+    attn_mask = torch.from_numpy(mask)[:, None, None, :]
+    ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=attn_mask, scale=scale)
+    ref = ref.transpose(1, 2).numpy()[mask]
+    np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+    scores = torch.einsum("bhqd,bhkd->bhqk", tq, tk) * scale
+    scores = scores.masked_fill(~attn_mask, float("-inf"))
+    ref_lse = torch.logsumexp(scores, dim=-1).transpose(1, 2).numpy()[mask]  # [N, H]
+    np.testing.assert_allclose(lse.T, ref_lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_first_token_equals_rows_of_full_output(seed):
+    lengths, s, q, k, v = _random_case(10 + seed)
+    _, cu, _ = oracle.pack_sequences(lengths, s)
+    o, lse = oracle.attention_fwd(q, k, v, cu, s, 0.5)
+    first = cu[:-1].astype(np.int64)
+    o1, lse1 = oracle.attention_fwd(q[first], k, v, cu, s, 0.5, first_token=True)
+    np.testing.assert_array_equal(o1, o[first])
+    np.testing.assert_array_equal(lse1, lse[:, first])
+
+
+def test_closed_forms():
+    rng = np.random.default_rng(7)
+    h, d, scale = 2, 8, 0.3
+    # A length-1 sequence outputs its own v; its lse is scale * q.k.
+    lengths = np.array([1, 4, 1], np.int32)
+    _, cu, n = oracle.pack_sequences(lengths, 4)
+    q, k, v = (rng.standard_normal((n, h, d)) for _ in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, cu, 4, scale)
+    for t in (0, 5):
+        np.testing.assert_allclose(o[t], v[t], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[:, t], scale * np.sum(q[t] * k[t], axis=-1), atol=1e-14)
+    # q = 0 (or scale = 0) gives the mean of the sequence's values and lse = log L.
+    for zero_q in (True, False):
+        qq = np.zeros_like(q) if zero_q else q
+        o, lse = oracle.attention_fwd(qq, k, v, cu, 4, 0.0 if not zero_q else scale)
+        for i in range(len(lengths)):
+            rows = slice(cu[i], cu[i + 1])
+            np.testing.assert_allclose(o[rows], np.broadcast_to(v[rows].mean(0), o[rows].shape),
+                                       atol=1e-14)
+            np.testing.assert_allclose(lse[:, rows], math.log(lengths[i]), atol=1e-14)
+    # Constant values give that constant back.
+    const = rng.standard_normal((1, h, d))
+    o, _ = oracle.attention_fwd(q, k, np.broadcast_to(const, v.shape), cu, 4, scale)
+    np.testing.assert_allclose(o, np.broadcast_to(const, o.shape), atol=1e-14)
+
+
+def test_one_full_sequence_is_textbook_attention():
+    """B = 1, L = S: dense softmax(scale Q K^T) V, computed with scipy's softmax."""
+    rng = np.random.default_rng(8)
+    s, h, d, scale = 17, 2, 8, 0.41
+    q, k, v = (rng.standard_normal((s, h, d)) for _ in range(3))
+    _, cu, _ = oracle.pack_sequences([s], s)
+    o, _ = oracle.attention_fwd(q, k, v, cu, s, scale)
+    for hh in range(h):
+        w = scipy.special.softmax(scale * q[:, hh] @ k[:, hh].T, axis=1)
+        np.testing.assert_allclose(o[:, hh], w @ v[:, hh], atol=1e-13)
+
+
+def test_block_diagonal_brute_force_on_tiny_workload():
+    """Full token-by-token score matrix, keeping pairs in the same grid row."""
+    x = workloads.make_inputs("tiny_fp32")
+    s = x.workload.max_seq_len
+    flat, cu, n = oracle.pack_sequences(x.lengths, s)
+    q, k, v = (t.double().numpy() for t in (x.q, x.k, x.v))
+    o, _ = oracle.attention_fwd(q, k, v, cu, s, x.workload.scale)
+    same = (flat[:, None] // s) == (flat[None, :] // s)
+    for hh in range(x.workload.num_heads):
+        scores = x.workload.scale * q[:, hh] @ k[:, hh].T
+        scores = np.where(same, scores, -np.inf)
+        w = scipy.special.softmax(scores, axis=1)
+        np.testing.assert_allclose(o[:, hh], w @ v[:, hh], atol=1e-13)
+
+
+@pytest.mark.parametrize("first_token", [False, True])
+def test_sampled_rows_match_full_forward(first_token):
+    lengths, s, q, k, v = _random_case(31, b_max=9, s_max=40, h=4, d=16)
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    if first_token:
+        q = q[cu[:-1].astype(np.int64)]
+    o, lse = oracle.attention_fwd(q, k, v, cu, s, 0.25, first_token=first_token)
+    rng = np.random.default_rng(3)
+    rows = rng.integers(0, q.shape[0], 50)
+    heads = rng.integers(0, 4, 50)
+    o_r, lse_r = oracle.attention_fwd_rows(q, k, v, cu, 0.25, first_token, rows, heads)
+    np.testing.assert_allclose(o_r, o[rows, heads], atol=1e-14)
+    np.testing.assert_allclose(lse_r, lse[heads, rows], atol=1e-14)
+
+
+def test_cross_sequence_isolation():
+    lengths, s, q, k, v = _random_case(41, b_max=6)
+    if len(lengths) < 2:
+        lengths = np.array([3, 4], np.int32)
+        s = 4
+        rng = np.random.default_rng(0)
+        q, k, v = (rng.standard_normal((7, 3, 8)) for _ in range(3))
+    _, cu, _ = oracle.pack_sequences(lengths, s)
+    o, lse = oracle.attention_fwd(q, k, v, cu, s, 0.5)
+    k2, v2 = k.copy(), v.copy()
+    k2[cu[1]:cu[2]] += 3.0
+    v2[cu[1]:cu[2]] -= 5.0
+    o2, lse2 = oracle.attention_fwd(q, k2, v2, cu, s, 0.5)
+    keep = np.ones(q.shape[0], bool)
+    keep[cu[1]:cu[2]] = False
+    np.testing.assert_array_equal(o2[keep], o[keep])
+    np.testing.assert_array_equal(lse2[:, keep], lse[:, keep])
+    assert not np.array_equal(o2[~keep], o[~keep])
+
+
+# --------------------------------------------------------------------------- backward
+
+def _loss(q, k, v, dout, cu, s, scale, first_token):
+    o, _ = oracle.attention_fwd(q, k, v, cu, s, scale, first_token=first_token, threads=1)
+    return float(np.sum(o * dout))
+
+
+@pytest.mark.parametrize("first_token", [False, True])
+def test_backward_matches_finite_differences(first_token):
+    rng = np.random.default_rng(5)
+    lengths = np.array([3, 1, 4], np.int32)
+    s, h, d, scale = 4, 2, 4, 0.6
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    nq = len(lengths) if first_token else n
+    q = rng.standard_normal((nq, h, d))
+    k, v = rng.standard_normal((n, h, d)), rng.standard_normal((n, h, d))
+    dout = rng.standard_normal((nq, h, d))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, cu, scale, first_token=first_token)
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            fp = _loss(args["q"], args["k"], args["v"], dout, cu, s, scale, first_token)
+            args[name] = xm
+            fm = _loss(args["q"], args["k"], args["v"], dout, cu, s, scale, first_token)
+            fd[idx] = (fp - fm) / (2 * eps)
+        np.testing.assert_allclose(g, fd, rtol=0, atol=2e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_matches_torch_autograd_on_padded_grid(seed):
+    lengths, s, q, k, v = _random_case(50 + seed)
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    rng = np.random.default_rng(60 + seed)
+    dout = rng.standard_normal(q.shape)
+    scale = 0.45
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, cu, scale)
+    grids = [_padded(x, lengths, s)[0] for x in (q, k, v, dout)]
+    mask = _padded(q, lengths, s)[1]
+    tq, tk, tv = (torch.from_numpy(g).transpose(1, 2).requires_grad_(True) for g in grids[:3])
+    attn_mask = torch.from_numpy(mask)[:, None, None, :]
+    out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=attn_mask, scale=scale)
+    out.backward(torch.from_numpy(grids[3]).transpose(1, 2))
+    for g, t in ((dq, tq), (dk, tk), (dv, tv)):
+        ref = t.grad.transpose(1, 2).numpy()[mask]
+        np.testing.assert_allclose(g, ref, rtol=0, atol=1e-12)
+
+
+def test_backward_invariants():
+    """Rows of dS sum to zero, so dK sums to zero per (sequence, head); rows of P
+    sum to one, so dV sums to the sum of dO per (sequence, head)."""
+    lengths, s, q, k, v = _random_case(70, b_max=8, s_max=20)
+    _, cu, _ = oracle.pack_sequences(lengths, s)
+    dout = np.random.default_rng(71).standard_normal(q.shape)
+    _, dk, dv = oracle.attention_bwd(q, k, v, dout, cu, 0.35)
+    for i in range(len(lengths)):
+        rows = slice(cu[i], cu[i + 1])
+        np.testing.assert_allclose(dk[rows].sum(0), 0.0, atol=1e-12)
+        np.testing.assert_allclose(dv[rows].sum(0), dout[rows].sum(0), atol=1e-12)
+
+
+# --------------------------------------------------------------------------- input recipes
+
+def test_workload_recipes():
+    """Token counts of the seeded synthetic workloads (draw order: lengths first)."""
+    expect = {"tiny_fp32": (8, 91), "graph_fp32": (1024, 90487),
+              "contrastive_bf16": (320, 32299), "longdoc_bf16": (32, 169151)}
+    for name, (b, n) in expect.items():
+        lengths = workloads.draw_lengths(name, np.random.default_rng(0))
+        assert lengths.shape == (b,) and int(lengths.sum()) == n, name
+        assert lengths.min() >= 1 and lengths.max() <= workloads.WORKLOADS[name].max_seq_len
+    x = workloads.make_inputs("tiny_fp32")
+    assert x.q.dtype == torch.float32 and tuple(x.q.shape) == (91, 2, 8)
