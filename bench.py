@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of one padding-free packed attention step on GB300.
+
+A step is one pass of the hot path over one synthetic batch of the
+long-document indexing workload (32 documents of 2048..8192 tokens, 16 heads x
+64, bf16, forward only): pack the lengths (one host read), gather q, k and v
+from their padded grids into packed buffers, plan the tiles, run the packed
+attention forward, and scatter the output back to a zero-padded grid.
+
+The metric is real-token TFLOP/s, 4 * sum_i L_i^2 * H * d per step divided by
+the step time (tokens/s and the fraction of the tensor-core peak ride along).
+Inputs (three 0.5 GB padded grids) are larger than the 129 MB L2, so no L2
+flush runs between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (the only other place this file runs the oracle
+is the cpu_baseline leg).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed attention real-token TFLOP/s and tokens/s; % of GB300 tensor-core peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def real_flops(lengths, heads, head_dim, first_token=False):
+    lengths = np.asarray(lengths, dtype=np.int64)
+    if first_token:
+        return float(4 * lengths.sum() * heads * head_dim)
+    return float(4 * (lengths ** 2).sum() * heads * head_dim)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/pe_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- traffic
+
+def committed_traffic(kernel_name: str, source_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (its sha1 is recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_name}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            key, _, value = line.partition(":")
+            fields[key.strip()] = value.strip()
+    src = os.path.join(ROOT, "padding_free_packed_gb300", "csrc", source_file)
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest() if os.path.exists(src) else ""
+    if fields.get("source_sha1") != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+KERNEL_SOURCES = {"tcgen05_bf16_d64": "pe_fwd_sm103.cu", "simt_ffma": "pe_fwd_simt.cu",
+                  "first_token_gemv": "pe_fwd_simt.cu"}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import torch
+
+    import padding_free_packed_gb300 as pe
+    from padding_free_packed_gb300 import workloads
+
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pe.load_library()
+    wl = workloads.WORKLOADS[args.workload]
+    # Weak scaling: every rank draws its own batch of the same workload.
+    lengths, gq, gk, gv = workloads.make_padded_inputs(args.workload, seed=args.seed + rank)
+    s, h, d = wl.max_seq_len, wl.num_heads, wl.head_dim
+    n_tokens = int(lengths.astype(np.int64).sum())
+    flops = real_flops(lengths, h, d)
+    kernel = pe.pe_attention_kernel(wl.torch_dtype, d)
+
+    lengths_d = torch.from_numpy(lengths).to(dev)
+    qg, kg, vg = gq.to(dev), gk.to(dev), gv.to(dev)
+    og = torch.empty_like(qg)
+    stream = torch.cuda.current_stream(dev)
+    fwd_events = []
+
+    def step(lengths_t, q_grid, k_grid, v_grid, out_grid, record):
+        flat, cu, n = pe.pe_pack_sequences(lengths_t, s)
+        q = pe.pe_gather_packed(q_grid, flat, n)
+        k = pe.pe_gather_packed(k_grid, flat, n)
+        v = pe.pe_gather_packed(v_grid, flat, n)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        out, _ = pe.pe_packed_attention_fwd(q, k, v, cu, s, wl.scale)
+        if record:
+            e1.record(stream)
+            fwd_events.append((e0, e1))
+        pe.pe_scatter_padded(out, cu, s, out=out_grid)
+        return n
+
+    launches_per_step = 2 + 3 + 2 + 1  # pack scan+fill, 3 gathers, plan+attention, scatter
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(lengths_d, qg, kg, vg, og, False)
+    barrier()
+    with ClockSampler(local_rank) as clocks:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(args.steps):
+            step(lengths_d, qg, kg, vg, og, True)
+        end.record(stream)
+        barrier()
+    elapsed_ms = start.elapsed_time(end)
+    fwd_ms = sum(a.elapsed_time(b) for a, b in fwd_events) / len(fwd_events)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+
+    # End to end through the same public calls: pinned host grids in, padded
+    # output back to pinned host memory, copies inside the timed region.
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in (gq, gk, gv))
+        hlen = torch.from_numpy(lengths).pin_memory()
+        hout = torch.empty_like(gq).pin_memory()
+        dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+        dlen = torch.empty_like(lengths_d)
+
+        def e2e_step():
+            dlen.copy_(hlen, non_blocking=True)
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            step(dlen, dq, dk, dv, og, False)
+            hout.copy_(og, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        barrier()
+        e2e_steps = max(1, min(args.steps, 10))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        t1.record(stream)
+        barrier()
+        e2e_ms = t0.elapsed_time(t1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hlen, hq, hk, hv))
+        d2h = hout.numel() * hout.element_size()
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    peaks, peaks_src = load_peaks()
+    if kernel.startswith("tcgen05"):
+        bound, peak, unit = "tensor", float(peaks["bf16_tflops"]), "TFLOP/s"
+        peak_note = f"dense bf16 burst, {peaks_src}"
+    elif kernel == "first_token_gemv":
+        bound, peak, unit = "hbm", float(peaks["hbm_gbs"]), "GB/s"
+        peak_note = f"HBM copy, {peaks_src}"
+    else:
+        ffma = (torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2
+                * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12)
+        bound, peak, unit = "alu", ffma, "TFLOP/s"
+        peak_note = "FFMA: SMs x 128 lanes x 2 flop x max SM clock"
+    achieved = flops / (fwd_ms * 1e-3) / 1e12
+    traffic = committed_traffic(kernel, KERNEL_SOURCES.get(kernel, ""))
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "description": wl.description,
+                   "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
+                   "heads": h, "head_dim": d, "max_seq_len": s,
+                   "step": "pack + gather q,k,v + tile plan + attention forward + scatter",
+                   "l2": "inputs larger than L2 (three padded grids of "
+                         f"{gq.numel() * gq.element_size() / 1e9:.2f} GB); no flush",
+                   "parallelism": f"dp{world} (independent batches per GPU, no collective)"},
+        "tokens_per_s": world * n_tokens / (ms_per_step * 1e-3),
+        "pct_of_tensor_peak": 100.0 * value / world / float(peaks["bf16_tflops"]),
+        "attention_kernel": kernel,
+        "attention_ms": fwd_ms,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
+                     "frac_of_sustained": (achieved / float(peaks["bf16_tflops_sustained"])
+                                           if bound == "tensor" else None)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows, args.seed)
+    return line
+
+
+# --------------------------------------------------------------------------- oracle arms
+
+def _oracle_sample(workload: str, rows: int, seed: int):
+    """A bounded sample of the workload for the oracle: `rows` random (token,
+    head) query rows, each attending over its whole sequence."""
+    from padding_free_packed_gb300 import workloads
+    x = workloads.make_inputs(workload, seed=seed)
+    import oracle
+    _, cu, n = oracle.pack_sequences(x.lengths, x.workload.max_seq_len)
+    rng = np.random.default_rng(1234)
+    r = rng.integers(0, n, rows)
+    hs = rng.integers(0, x.workload.num_heads, rows)
+    seq = np.searchsorted(cu, r, side="right") - 1
+    lens = (cu[1:] - cu[:-1]).astype(np.int64)[seq]
+    flops = float(4 * lens.sum() * x.workload.head_dim)
+    # Widen to fp64 once, outside any timed region.
+    x.q, x.k, x.v = (t.double().numpy() for t in (x.q, x.k, x.v))
+    return x, cu, r, hs, flops
+
+
+def _time_oracle(x, cu, r, hs):
+    import oracle
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attention_fwd_rows(x.q, x.k, x.v, cu, x.workload.scale, False, r, hs, threads=threads)
+    return time.perf_counter() - t0, threads
+
+
+def cpu_baseline(workload: str, rows: int, seed: int):
+    x, cu, r, hs, flops = _oracle_sample(workload, rows, seed)
+    dt, threads = _time_oracle(x, cu, r, hs)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{rows} random (token, head) query rows of {workload} (seed {seed}), each "
+                      "over its whole sequence, fp64 oracle row path"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    from padding_free_packed_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    x, cu, r, hs, flops = _oracle_sample(args.workload, args.ref_rows, args.seed)
+    for _ in range(args.warmup):
+        _time_oracle(x, cu, r, hs)
+    times = []
+    threads = 1
+    for _ in range(args.steps):
+        dt, threads = _time_oracle(x, cu, r, hs)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = (f"{args.ref_rows} random (token, head) query rows of {args.workload} per step, "
+              "each over its whole sequence, fp64 oracle row path")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload,
+                                            "description": wl.description},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="longdoc_bf16")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=24576,
+                    help="query rows in the cpu_baseline sample (about 10-30 s of CPU work)")
+    ap.add_argument("--ref-rows", type=int, default=2048,
+                    help="query rows per reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

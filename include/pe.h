@@ -1,0 +1,184 @@
+/*
+ * pe.h - C ABI of the padding-free packed attention library (libpe).
+ *
+ * Variable-length sequences live in one flat token-major buffer
+ * [num_tokens, num_heads, head_dim] with no padding; int32 cu_seqlens marks
+ * where each sequence starts, and every sequence attends only to itself
+ * (page "Source code for gigl.nn.packed_attention", module docstring,
+ * "Data flow of a packed forward").
+ *
+ * Conventions shared by every call:
+ *   - Every buffer argument is DEVICE memory owned by the caller, except the
+ *     host out-parameter of pe_pack_sequences and pe_read_device_status.
+ *     The library allocates nothing and keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream), except pe_pack_sequences, which performs the one host read of
+ *     the token count, and pe_read_device_status.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns a status and launches nothing.
+ *   - Rows are row-major and tightly packed. bf16 is IEEE bfloat16; fp32 is
+ *     IEEE binary32. Accumulation is always fp32.
+ *   - Kernels run on the current CUDA device, which must be compute
+ *     capability 10.3 (sm_103a); any other device gives PE_ERR_UNSUPPORTED.
+ */
+#ifndef PE_H_
+#define PE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* pe_stream_t;
+
+typedef enum pe_status {
+  PE_OK = 0,
+  PE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad scale, ...        */
+  PE_ERR_BAD_LENGTH = 2,     /* a sequence length < 1 or > max_seq_len             */
+  PE_ERR_OVERFLOW = 3,       /* token count (or tile count) does not fit in int32  */
+  PE_ERR_UNSUPPORTED = 4,    /* head_dim, dtype, alignment or device not supported */
+  PE_ERR_WORKSPACE = 5,      /* workspace null or smaller than *_workspace_size     */
+  PE_ERR_CUDA = 6,           /* a CUDA runtime call failed                         */
+  PE_ERR_DEVICE_TIMEOUT = 7  /* a kernel gave up waiting on its own pipeline        */
+} pe_status;
+
+typedef enum pe_dtype { PE_BF16 = 0, PE_FP32 = 1 } pe_dtype;
+
+/* Text for a status code; never NULL. */
+const char* pe_status_string(int status);
+
+/* Version of this ABI (incremented on any signature change). */
+int pe_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * pack_sequences  (module docstring, "Data flow of a packed forward",
+ * "Constraints" and "Example": lengths [3,1,2], max_seq_len 3 give
+ * flat_index [0,1,2,3,6,7]; packing reads the token count back to the host
+ * once, and nothing else syncs).
+ *
+ *   cu_seqlens[0] = 0, cu_seqlens[i+1] = cu_seqlens[i] + lengths[i]
+ *   flat_index[cu_seqlens[i] + j] = i * max_seq_len + j   for 0 <= j < lengths[i]
+ *
+ * lengths:      int32 [num_sequences], device.
+ * flat_index:   int64, device, capacity >= num_sequences * max_seq_len entries
+ *               (a bound the host knows, so no allocation waits on the count);
+ *               the first *num_tokens entries are written.
+ * cu_seqlens:   int32 [num_sequences + 1], device.
+ * num_tokens:   HOST out: the token count N. This is the single device-to-host
+ *               read; the call synchronizes `stream` to perform it.
+ * workspace:    device, >= pe_pack_workspace_size() bytes.
+ * Errors: PE_ERR_BAD_LENGTH if some length is < 1 or > max_seq_len (detected
+ * on the device, reported through the same host read; flat_index is then not
+ * written), PE_ERR_OVERFLOW if N >= 2^31. num_sequences == 0 gives N = 0 and
+ * cu_seqlens = [0].
+ * ------------------------------------------------------------------------ */
+size_t pe_pack_workspace_size(int32_t num_sequences);
+pe_status pe_pack_sequences(const int32_t* lengths, int32_t num_sequences, int32_t max_seq_len,
+                            int64_t* flat_index, int32_t* cu_seqlens, int64_t* num_tokens,
+                            void* workspace, size_t workspace_bytes, pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Padded -> packed gather: packed[t, :] = padded[flat_index[t], :]
+ * (module docstring, "Data flow of a packed forward": grid.flatten()[flat_index]).
+ *
+ * padded:     device, rows of row_bytes bytes (any number of rows; every
+ *             flat_index value must name one of them).
+ * flat_index: int64 [num_tokens], device (from pe_pack_sequences).
+ * packed:     device, [num_tokens] rows of row_bytes bytes.
+ * 16-byte vector copies when row_bytes and both pointers are 16-byte aligned,
+ * 4-byte copies when 4-byte aligned, byte copies otherwise (all on the GPU).
+ * ------------------------------------------------------------------------ */
+pe_status pe_gather_packed(const void* padded, const int64_t* flat_index, int64_t num_tokens,
+                           int64_t row_bytes, void* packed, pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Packed -> padded scatter with zero fill (function _padded_packed_attention,
+ * which unpacks with to_dense_batch, fill value 0):
+ *   padded[i*max_seq_len + j, :] = j < L_i ? packed[cu_seqlens[i] + j, :] : 0
+ *
+ * packed:     device, [cu_seqlens[num_sequences]] rows of row_bytes bytes.
+ * cu_seqlens: int32 [num_sequences + 1], device (trusted output of pack).
+ * padded:     device, [num_sequences * max_seq_len] rows; every row is written.
+ * ------------------------------------------------------------------------ */
+pe_status pe_scatter_padded(const void* packed, const int32_t* cu_seqlens, int32_t num_sequences,
+                            int32_t max_seq_len, int64_t row_bytes, void* padded,
+                            pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Packed attention forward (function packed_attention and the custom op
+ * gigl::varlen_attention, which returns the output and the log-sum-exp).
+ *
+ * For every sequence i, head h and query row r:
+ *   O[r,h,:]  = sum_j softmax_j(scale * q[r,h,:] . k[j,h,:]) v[j,h,:]
+ *   lse[h,r]  = log sum_j exp(scale * q[r,h,:] . k[j,h,:])      (natural log)
+ * with j over the keys of sequence i only (cu_seqlens[i] <= j < cu_seqlens[i+1]).
+ *
+ * query_is_first_token = 0: q and out are [num_tokens, H, D]; row r of
+ *   sequence i is token cu_seqlens[i] + r.
+ * query_is_first_token = 1: q and out are [num_sequences, H, D]; q[i] is the
+ *   query of sequence i (its first token, as the caller sliced it), and out[i]
+ *   equals row cu_seqlens[i] of the full-mode output.
+ * k, v: [num_tokens, H, D]. dtype applies to q, k, v and out.
+ * lse: fp32 [H, Nq] (Nq = num_tokens or num_sequences), or NULL to skip it.
+ * cu_seqlens: int32 [num_sequences + 1], device, trusted output of
+ *   pe_pack_sequences (lengths >= 1 and <= max_seq_len).
+ * scale: finite and > 0 (1/sqrt(D) is the pages' default).
+ * head_dim: a multiple of 8 (the module docstring's "Constraints" require
+ *   it for the aligned kernels), at most 128; bf16 with head_dim 64 runs on the
+ *   tcgen05 tensor cores.
+ * All tensor pointers 16-byte aligned.
+ * workspace: device, >= pe_attention_workspace_size(...) bytes. Its first 4
+ *   bytes receive a device-side status (PE_OK or PE_ERR_DEVICE_TIMEOUT),
+ *   readable with pe_read_device_status after the call.
+ * ------------------------------------------------------------------------ */
+size_t pe_attention_workspace_size(pe_dtype dtype, int32_t num_sequences, int64_t num_tokens,
+                                   int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
+                                   int query_is_first_token, int backward);
+
+pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t num_sequences, int64_t num_tokens,
+                                  int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
+                                  const void* q, const void* k, const void* v,
+                                  const int32_t* cu_seqlens, float scale, int query_is_first_token,
+                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                  pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Packed attention backward (the custom op gigl::varlen_attention_backward,
+ * which takes the saved q, k, v, output and log-sum-exp and returns the
+ * gradients in q, k and v). With P = softmax(scale q k^T) per sequence/head:
+ *   Delta_r = dO_r . O_r,  dS = P o (dO v^T - Delta),
+ *   dq = scale dS k,  dk = scale dS^T q,  dv = P^T dO.
+ * Arguments as in the forward; out and lse are that forward's results for
+ * the same inputs; dout, dq are shaped like q; dk, dv like k. Every element
+ * of dq, dk, dv is written. The result is bitwise deterministic run to run
+ * (no floating-point atomics).
+ * ------------------------------------------------------------------------ */
+pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t num_sequences, int64_t num_tokens,
+                                  int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
+                                  const void* q, const void* k, const void* v,
+                                  const int32_t* cu_seqlens, float scale, int query_is_first_token,
+                                  const void* out, const float* lse, const void* dout,
+                                  void* dq, void* dk, void* dv,
+                                  void* workspace, size_t workspace_bytes, pe_stream_t stream);
+
+/* Name of the kernel family that pe_packed_attention_fwd (backward = 0) or
+ * pe_packed_attention_bwd (backward = 1) runs for these arguments on an sm_103a
+ * device: "tcgen05_bf16_d64", "simt_ffma", "first_token_gemv",
+ * "simt_ffma_bwd", "tcgen05_bf16_d64_bwd", or "unsupported". A static
+ * string; never NULL. */
+const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_first_token,
+                                int backward);
+
+/* Synchronizes `stream` and returns the device-side status that the last
+ * attention call on `workspace` left in its first 4 bytes (PE_OK when every
+ * pipeline wait completed). */
+pe_status pe_read_device_status(const void* workspace, pe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PE_H_ */

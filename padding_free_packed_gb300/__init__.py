@@ -1,0 +1,20 @@
+"""Padding-free packed bidirectional attention on GB300 (sm_103a).
+
+Sequences are packed into one flat [num_tokens, heads, head_dim] buffer; each
+sequence attends only to itself inside its cu_seqlens boundaries. The compute
+lives in libpe.so (CUDA kernels behind the C ABI in include/pe.h); this
+package is its thin Python binding plus the seeded synthetic workloads.
+"""
+
+from .binding import (  # noqa: F401
+    PackedAttentionError,
+    attention_workspace_bytes,
+    load_library,
+    pe_attention_kernel,
+    pe_gather_packed,
+    pe_pack_sequences,
+    pe_packed_attention_bwd,
+    pe_packed_attention_fwd,
+    pe_read_device_status,
+    pe_scatter_padded,
+)

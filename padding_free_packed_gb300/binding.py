@@ -1,0 +1,231 @@
+"""Thin Python binding over libpe's C ABI (include/pe.h).
+
+Argument marshalling only: every step of the packed-attention path runs in the
+library's CUDA kernels. PyTorch provides device memory (outputs and
+workspaces are torch tensors) and the current CUDA stream. There is no CPU
+fallback: if libpe.so is missing or the device is not sm_103a the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpe.so")
+
+PE_BF16 = 0
+PE_FP32 = 1
+
+EXPORTED = (
+    "pe_status_string", "pe_abi_version", "pe_pack_workspace_size", "pe_pack_sequences",
+    "pe_gather_packed", "pe_scatter_padded", "pe_attention_workspace_size",
+    "pe_packed_attention_fwd", "pe_packed_attention_bwd", "pe_read_device_status",
+    "pe_attention_kernel",
+)
+
+_lib = None
+
+
+class PackedAttentionError(RuntimeError):
+    def __init__(self, call: str, status: int, text: str):
+        super().__init__(f"{call} failed with status {status}: {text}")
+        self.status = status
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads libpe.so and declares its signatures. Raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"libpe.so not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    c = ctypes
+    i32, i64, vp, sz = c.c_int32, c.c_int64, c.c_void_p, c.c_size_t
+    lib.pe_status_string.argtypes = [c.c_int]
+    lib.pe_status_string.restype = c.c_char_p
+    lib.pe_abi_version.argtypes = []
+    lib.pe_abi_version.restype = c.c_int
+    lib.pe_pack_workspace_size.argtypes = [i32]
+    lib.pe_pack_workspace_size.restype = sz
+    lib.pe_pack_sequences.argtypes = [vp, i32, i32, vp, vp, c.POINTER(i64), vp, sz, vp]
+    lib.pe_pack_sequences.restype = c.c_int
+    lib.pe_gather_packed.argtypes = [vp, vp, i64, i64, vp, vp]
+    lib.pe_gather_packed.restype = c.c_int
+    lib.pe_scatter_padded.argtypes = [vp, vp, i32, i32, i64, vp, vp]
+    lib.pe_scatter_padded.restype = c.c_int
+    lib.pe_attention_workspace_size.argtypes = [c.c_int, i32, i64, i32, i32, i32, c.c_int, c.c_int]
+    lib.pe_attention_workspace_size.restype = sz
+    lib.pe_packed_attention_fwd.argtypes = [c.c_int, i32, i64, i32, i32, i32, vp, vp, vp, vp,
+                                            c.c_float, c.c_int, vp, vp, vp, sz, vp]
+    lib.pe_packed_attention_fwd.restype = c.c_int
+    lib.pe_packed_attention_bwd.argtypes = [c.c_int, i32, i64, i32, i32, i32, vp, vp, vp, vp,
+                                            c.c_float, c.c_int, vp, vp, vp, vp, vp, vp, vp, sz,
+                                            vp]
+    lib.pe_packed_attention_bwd.restype = c.c_int
+    lib.pe_attention_kernel.argtypes = [c.c_int, i32, c.c_int, c.c_int]
+    lib.pe_attention_kernel.restype = c.c_char_p
+    lib.pe_read_device_status.argtypes = [vp, vp]
+    lib.pe_read_device_status.restype = c.c_int
+    _lib = lib
+    return lib
+
+
+def _check(call: str, status: int):
+    if status != 0:
+        text = load_library().pe_status_string(status).decode()
+        raise PackedAttentionError(call, status, text)
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _dtype_code(dtype: torch.dtype) -> int:
+    if dtype == torch.bfloat16:
+        return PE_BF16
+    if dtype == torch.float32:
+        return PE_FP32
+    raise TypeError(f"unsupported dtype {dtype}: bfloat16 or float32 only")
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    return t.contiguous()
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def pe_pack_sequences(lengths: torch.Tensor, max_seq_len: int):
+    """Returns (flat_index int64 [N], cu_seqlens int32 [B+1], N) for device lengths."""
+    lib = load_library()
+    lengths = _cuda(lengths, "lengths").to(torch.int32)
+    b = int(lengths.numel())
+    dev = lengths.device
+    flat = torch.empty(max(b * int(max_seq_len), 1), dtype=torch.int64, device=dev)
+    cu = torch.empty(b + 1, dtype=torch.int32, device=dev)
+    ws = _workspace(lib.pe_pack_workspace_size(b), dev)
+    n = ctypes.c_int64(0)
+    _check("pe_pack_sequences",
+           lib.pe_pack_sequences(_ptr(lengths), b, int(max_seq_len), _ptr(flat), _ptr(cu),
+                                 ctypes.byref(n), _ptr(ws), ws.numel(), _stream(dev)))
+    return flat[: n.value], cu, int(n.value)
+
+
+def pe_gather_packed(padded: torch.Tensor, flat_index: torch.Tensor, num_tokens: int | None = None):
+    """packed[t] = padded.flatten(0, 1)[flat_index[t]] for a [B, S, ...] grid."""
+    lib = load_library()
+    padded = _cuda(padded, "padded")
+    flat_index = _cuda(flat_index, "flat_index")
+    n = int(flat_index.numel()) if num_tokens is None else int(num_tokens)
+    row_shape = tuple(padded.shape[2:])
+    packed = torch.empty((n,) + row_shape, dtype=padded.dtype, device=padded.device)
+    row_bytes = padded.element_size() * math.prod(row_shape)
+    _check("pe_gather_packed",
+           lib.pe_gather_packed(_ptr(padded), _ptr(flat_index), n, row_bytes, _ptr(packed),
+                                _stream(padded.device)))
+    return packed
+
+
+def pe_scatter_padded(packed: torch.Tensor, cu_seqlens: torch.Tensor, max_seq_len: int,
+                      out: torch.Tensor | None = None):
+    """Returns the zero-padded [B, S, ...] grid of a packed [N, ...] buffer."""
+    lib = load_library()
+    packed = _cuda(packed, "packed")
+    cu_seqlens = _cuda(cu_seqlens, "cu_seqlens")
+    b = int(cu_seqlens.numel()) - 1
+    row_shape = tuple(packed.shape[1:])
+    if out is None:
+        out = torch.empty((b, int(max_seq_len)) + row_shape, dtype=packed.dtype,
+                          device=packed.device)
+    row_bytes = packed.element_size() * math.prod(row_shape)
+    _check("pe_scatter_padded",
+           lib.pe_scatter_padded(_ptr(packed), _ptr(cu_seqlens), b, int(max_seq_len), row_bytes,
+                                 _ptr(out), _stream(packed.device)))
+    return out
+
+
+def attention_workspace_bytes(dtype, num_sequences, num_tokens, num_heads, head_dim,
+                              max_seq_len, query_is_first_token=False, backward=False) -> int:
+    return int(load_library().pe_attention_workspace_size(
+        _dtype_code(dtype), int(num_sequences), int(num_tokens), int(num_heads), int(head_dim),
+        int(max_seq_len), int(bool(query_is_first_token)), int(bool(backward))))
+
+
+def pe_packed_attention_fwd(q, k, v, cu_seqlens, max_seq_len: int, scale: float | None = None,
+                            query_is_first_token: bool = False, need_lse: bool = False,
+                            out=None, lse=None, workspace=None):
+    """Packed attention forward. Returns (out, lse or None)."""
+    lib = load_library()
+    q, k, v = _cuda(q, "q"), _cuda(k, "k"), _cuda(v, "v")
+    cu_seqlens = _cuda(cu_seqlens, "cu_seqlens")
+    n, h, d = k.shape
+    b = int(cu_seqlens.numel()) - 1
+    nq = b if query_is_first_token else n
+    if tuple(q.shape) != (nq, h, d) or v.shape != k.shape or q.dtype != k.dtype:
+        raise ValueError(f"shape/dtype mismatch: q {tuple(q.shape)} k {tuple(k.shape)}")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if need_lse and lse is None:
+        lse = torch.empty((h, nq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(attention_workspace_bytes(q.dtype, b, n, h, d, max_seq_len,
+                                                         query_is_first_token, False), q.device)
+    _check("pe_packed_attention_fwd",
+           lib.pe_packed_attention_fwd(_dtype_code(q.dtype), b, n, h, d, int(max_seq_len),
+                                       _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), scale,
+                                       int(bool(query_is_first_token)), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return out, lse
+
+
+def pe_packed_attention_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seq_len: int,
+                            scale: float | None = None, query_is_first_token: bool = False,
+                            workspace=None):
+    """Packed attention backward. Returns (dq, dk, dv)."""
+    lib = load_library()
+    q, k, v = _cuda(q, "q"), _cuda(k, "k"), _cuda(v, "v")
+    out, dout, lse = _cuda(out, "out"), _cuda(dout, "dout"), _cuda(lse, "lse")
+    cu_seqlens = _cuda(cu_seqlens, "cu_seqlens")
+    n, h, d = k.shape
+    b = int(cu_seqlens.numel()) - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = _workspace(attention_workspace_bytes(q.dtype, b, n, h, d, max_seq_len,
+                                                         query_is_first_token, True), q.device)
+    _check("pe_packed_attention_bwd",
+           lib.pe_packed_attention_bwd(_dtype_code(q.dtype), b, n, h, d, int(max_seq_len),
+                                       _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), scale,
+                                       int(bool(query_is_first_token)), _ptr(out), _ptr(lse),
+                                       _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                       _ptr(workspace), workspace.numel(), _stream(q.device)))
+    return dq, dk, dv
+
+
+def pe_attention_kernel(dtype: torch.dtype, head_dim: int, query_is_first_token: bool = False,
+                        backward: bool = False) -> str:
+    """Kernel family the forward (or backward) dispatches to for these arguments."""
+    return load_library().pe_attention_kernel(
+        _dtype_code(dtype), int(head_dim), int(bool(query_is_first_token)),
+        int(bool(backward))).decode()
+
+
+def pe_read_device_status(workspace: torch.Tensor) -> int:
+    """Device-side status left in an attention workspace (0 = every wait completed)."""
+    lib = load_library()
+    return int(lib.pe_read_device_status(_ptr(workspace), _stream(workspace.device)))

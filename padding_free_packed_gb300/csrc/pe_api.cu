@@ -1,0 +1,187 @@
+// C-ABI entry points of libpe: host-side argument checks, workspace layout and
+// dispatch to the kernel families. Every check runs before any launch.
+#include <math.h>
+
+#include "pe_kernels.cuh"
+
+namespace pe {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+int g_is_sm103[kMaxDevices];  // 0 unknown, 1 yes, 2 no
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sm_count[dev] = n > 0 ? n : 1;
+  }
+  return g_sm_count[dev];
+}
+
+bool device_is_sm103() {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  if (g_is_sm103[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_is_sm103[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_is_sm103[dev] == 1;
+}
+
+namespace {
+
+inline size_t round16(size_t x) { return (x + 15) / 16 * 16; }
+
+size_t attention_ws_bytes(int32_t B, int64_t N, int32_t H, int query_is_first_token,
+                          int backward) {
+  size_t bytes = plan_bytes(B);
+  if (backward) {
+    const int64_t nq = query_is_first_token ? B : N;
+    bytes += round16((size_t)H * (size_t)nq * sizeof(float));
+  }
+  return bytes;
+}
+
+pe_status check_common(pe_dtype dtype, int32_t B, int64_t N, int32_t H, int32_t D, int32_t S,
+                       float scale) {
+  if (dtype != PE_BF16 && dtype != PE_FP32) return PE_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || H < 1 || S < 1) return PE_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !isfinite(scale)) return PE_ERR_INVALID_ARG;
+  if (D < 8 || D % 8 != 0 || D > kMaxHeadDim) return PE_ERR_UNSUPPORTED;
+  if (N >= (1LL << 31)) return PE_ERR_OVERFLOW;
+  if ((N == 0) != (B == 0)) return PE_ERR_INVALID_ARG;  // every sequence holds >= 1 token
+  // Tile counts are int32 on the device: bound them on the host.
+  const int64_t tiles = (int64_t)H * (N / 64 + B + 1);
+  if (tiles >= (1LL << 31)) return PE_ERR_OVERFLOW;
+  return PE_OK;
+}
+
+pe_status check_tensor(const void* p, int64_t elems) {
+  if (elems == 0) return PE_OK;
+  if (!p) return PE_ERR_INVALID_ARG;
+  if (!aligned(p, 16)) return PE_ERR_UNSUPPORTED;
+  return PE_OK;
+}
+
+pe_status check_workspace(void* ws, size_t have, size_t need) {
+  if (!ws || have < need || !aligned(ws, 16)) return PE_ERR_WORKSPACE;
+  return PE_OK;
+}
+
+}  // namespace
+}  // namespace pe
+
+using namespace pe;
+
+extern "C" const char* pe_status_string(int status) {
+  switch (status) {
+    case PE_OK: return "ok";
+    case PE_ERR_INVALID_ARG: return "invalid argument";
+    case PE_ERR_BAD_LENGTH: return "sequence length < 1 or > max_seq_len";
+    case PE_ERR_OVERFLOW: return "token or tile count does not fit in int32";
+    case PE_ERR_UNSUPPORTED: return "unsupported head_dim, dtype, alignment or device";
+    case PE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PE_ERR_CUDA: return "CUDA runtime error";
+    case PE_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting on its pipeline";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int pe_abi_version(void) { return 1; }
+
+extern "C" size_t pe_attention_workspace_size(pe_dtype /*dtype*/, int32_t B, int64_t N,
+                                              int32_t H, int32_t /*D*/, int32_t /*S*/,
+                                              int query_is_first_token, int backward) {
+  if (B < 0 || N < 0 || H < 1) return 0;
+  return attention_ws_bytes(B, N, H, query_is_first_token, backward);
+}
+
+extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
+                                             int32_t D, int32_t S, const void* q, const void* k,
+                                             const void* v, const int32_t* cu_seqlens,
+                                             float scale, int query_is_first_token, void* out,
+                                             float* lse, void* workspace, size_t workspace_bytes,
+                                             pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  PE_TRY(check_common(dtype, B, N, H, D, S, scale));
+  const int64_t nq = query_is_first_token ? B : N;
+  PE_TRY(check_tensor(q, nq));
+  PE_TRY(check_tensor(k, N));
+  PE_TRY(check_tensor(v, N));
+  PE_TRY(check_tensor(out, nq));
+  if (B > 0 && !cu_seqlens) return PE_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return PE_ERR_UNSUPPORTED;
+  PE_TRY(check_workspace(workspace, workspace_bytes,
+                         attention_ws_bytes(B, N, H, query_is_first_token, 0)));
+  if (query_is_first_token && !first_token_supported(D)) return PE_ERR_UNSUPPORTED;
+  if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
+  if (B == 0) return PE_OK;
+  if (query_is_first_token)
+    return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, scale, out, lse, stream);
+  TilePlan plan = plan_view(workspace, B);
+  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_tile(), S, plan, nullptr, stream));
+  return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, out, lse, N, plan, stream);
+}
+
+extern "C" pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
+                                             int32_t D, int32_t S, const void* q, const void* k,
+                                             const void* v, const int32_t* cu_seqlens,
+                                             float scale, int query_is_first_token,
+                                             const void* out, const float* lse, const void* dout,
+                                             void* dq, void* dk, void* dv, void* workspace,
+                                             size_t workspace_bytes, pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  PE_TRY(check_common(dtype, B, N, H, D, S, scale));
+  const int64_t nq = query_is_first_token ? B : N;
+  PE_TRY(check_tensor(q, nq));
+  PE_TRY(check_tensor(k, N));
+  PE_TRY(check_tensor(v, N));
+  PE_TRY(check_tensor(out, nq));
+  PE_TRY(check_tensor(dout, nq));
+  PE_TRY(check_tensor(dq, nq));
+  PE_TRY(check_tensor(dk, N));
+  PE_TRY(check_tensor(dv, N));
+  if (B > 0 && (!cu_seqlens || !lse)) return PE_ERR_INVALID_ARG;
+  if (lse && !aligned(lse, 4)) return PE_ERR_UNSUPPORTED;
+  PE_TRY(check_workspace(workspace, workspace_bytes,
+                         attention_ws_bytes(B, N, H, query_is_first_token, 1)));
+  if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
+  if (B == 0) return PE_OK;
+  TilePlan plan = plan_view(workspace, B);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
+  return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, out, lse,
+                  dout, dq, dk, dv, delta, plan, stream);
+}
+
+extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_is_first_token,
+                                          int backward) {
+  if ((dtype != PE_BF16 && dtype != PE_FP32) || D < 8 || D % 8 != 0 || D > kMaxHeadDim)
+    return "unsupported";
+  if (backward) return "simt_ffma_bwd";
+  if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
+  return "simt_ffma";
+}
+
+extern "C" pe_status pe_read_device_status(const void* workspace, pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!workspace) return PE_ERR_INVALID_ARG;
+  DeviceStatus host;
+  PE_CUDA_TRY(cudaMemcpyAsync(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost, stream));
+  PE_CUDA_TRY(cudaStreamSynchronize(stream));
+  return (pe_status)host.code;
+}

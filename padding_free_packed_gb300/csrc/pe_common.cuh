@@ -1,0 +1,123 @@
+// Shared device/host helpers of libpe (internal header).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pe.h"
+
+namespace pe {
+
+constexpr int kMaxHeadDim = 128;
+
+// Host-side check of a CUDA runtime call; returns PE_ERR_CUDA from the caller.
+#define PE_CUDA_TRY(expr)                                   \
+  do {                                                      \
+    cudaError_t pe_err_ = (expr);                           \
+    if (pe_err_ != cudaSuccess) return PE_ERR_CUDA;         \
+  } while (0)
+
+#define PE_TRY(expr)                                        \
+  do {                                                      \
+    pe_status pe_st_ = (expr);                              \
+    if (pe_st_ != PE_OK) return pe_st_;                     \
+  } while (0)
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Element conversions to and from the fp32 compute type.
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// log2(e): scores are kept in the base-2 domain so that exp(x) = 2^(x log2 e)
+// maps onto the hardware ex2 instruction.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Device-side status word at the head of every attention workspace.
+struct DeviceStatus {
+  int32_t code;       // pe_status
+  int32_t detail;     // where the wait gave up (role id), for diagnostics
+  int32_t pad[2];
+};
+
+__device__ __forceinline__ void report_timeout(DeviceStatus* st, int detail) {
+  if (st) {
+    atomicCAS(&st->code, (int)PE_OK, (int)PE_ERR_DEVICE_TIMEOUT);
+    st->detail = detail;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tile plan: longest-processing-time-first order of sequences and the
+// cumulative tile count in that order (built on the device, no host read).
+// ---------------------------------------------------------------------------
+struct TilePlan {
+  int32_t* counter;        // work counter claimed with atomicAdd (reset by the plan)
+  int32_t* total_tiles;    // number of tiles
+  int32_t* order;          // [B] sequence index at each position (longest first)
+  int32_t* tile_end;       // [B] inclusive prefix of tiles over positions
+};
+
+// Workspace layout shared by the attention entry points:
+//   [0, 16)        DeviceStatus
+//   [16, 32)       counter, total_tiles
+//   [32, ...)      order[B], tile_end[B] (each rounded to 16 bytes)
+//   [...]          kernel-specific scratch (16-byte aligned)
+inline size_t plan_bytes(int32_t B) {
+  size_t per = ((size_t)B * 4 + 15) / 16 * 16;
+  return 32 + 2 * per;
+}
+
+inline TilePlan plan_view(void* ws, int32_t B) {
+  char* base = static_cast<char*>(ws);
+  size_t per = ((size_t)B * 4 + 15) / 16 * 16;
+  TilePlan p;
+  p.counter = reinterpret_cast<int32_t*>(base + 16);
+  p.total_tiles = reinterpret_cast<int32_t*>(base + 20);
+  p.order = reinterpret_cast<int32_t*>(base + 32);
+  p.tile_end = reinterpret_cast<int32_t*>(base + 32 + per);
+  return p;
+}
+
+// Decodes tile t of a plan into (sequence, local tile index) by binary search
+// over the inclusive prefix; local < tiles of that sequence.
+__device__ __forceinline__ void plan_decode(const int32_t* __restrict__ order,
+                                            const int32_t* __restrict__ tile_end, int32_t B,
+                                            int32_t t, int32_t& seq, int32_t& local) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(tile_end + mid) > t) hi = mid; else lo = mid + 1;
+  }
+  seq = __ldg(order + lo);
+  local = t - (lo > 0 ? __ldg(tile_end + lo - 1) : 0);
+}
+
+// Launches the plan kernel: tiles of sequence i = heads * ceil(L_i / rows_per_tile).
+pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
+                           int32_t rows_per_tile, int32_t max_seq_len, TilePlan plan,
+                           DeviceStatus* status, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+// True if the current device is compute capability 10.3.
+bool device_is_sm103();
+
+}  // namespace pe

@@ -1,0 +1,27 @@
+// Internal launchers behind the C ABI (one per kernel family).
+#pragma once
+
+#include "pe_common.cuh"
+
+namespace pe {
+
+// CUDA-core forward (fp32 any head_dim; bf16 head_dims without a tensor-core kernel).
+int simt_rows_per_tile();
+pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
+                   const int32_t* cu, int32_t B, int32_t H, float scale, void* out, float* lse,
+                   int64_t N, TilePlan plan, cudaStream_t stream);
+
+// First-token query (one query row per sequence).
+bool first_token_supported(int D);
+pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
+                          const int32_t* cu, int32_t B, int32_t H, float scale, void* out,
+                          float* lse, cudaStream_t stream);
+
+// CUDA-core backward; delta is [H, Nq] fp32 scratch.
+pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
+                   const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,
+                   int first_token, const void* out, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, float* delta, TilePlan plan,
+                   cudaStream_t stream);
+
+}  // namespace pe

@@ -1,0 +1,96 @@
+"""The C ABI library loads and exports every symbol include/pe.h declares;
+host-side argument checks answer without a GPU (no compute is launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pe_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from padding_free_packed_gb300 import binding
+    from padding_free_packed_gb300 import build
+    if build.is_stale():
+        build.build()
+    return binding.load_library()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("pe_pack_sequences", "pe_gather_packed", "pe_scatter_padded",
+                 "pe_packed_attention_fwd", "pe_packed_attention_bwd"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from padding_free_packed_gb300 import binding
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(binding.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.pe_abi_version() == 1
+    for code in range(8):
+        assert lib.pe_status_string(code)
+    assert lib.pe_status_string(0) == b"ok"
+
+
+def test_workspace_sizes(lib):
+    fwd = lib.pe_attention_workspace_size(0, 320, 32299, 12, 64, 8192, 0, 0)
+    bwd = lib.pe_attention_workspace_size(0, 320, 32299, 12, 64, 8192, 0, 1)
+    assert fwd >= 16 and bwd >= fwd + 12 * 32299 * 4
+    assert lib.pe_attention_workspace_size(0, -1, 0, 1, 64, 1, 0, 0) == 0
+    assert lib.pe_pack_workspace_size(10) >= 16
+
+
+def _fwd(lib, **kw):
+    args = dict(dtype=0, B=2, N=10, H=2, D=64, S=8, q=16, k=16, v=16, cu=16, scale=0.125,
+                first=0, out=16, lse=None, ws=16, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.pe_packed_attention_fwd(args["dtype"], args["B"], args["N"], args["H"], args["D"],
+                                       args["S"], args["q"], args["k"], args["v"], args["cu"],
+                                       args["scale"], args["first"], args["out"], args["lse"],
+                                       args["ws"], args["ws_bytes"], args["stream"])
+
+
+def test_host_checks_reject_bad_arguments(lib):
+    # Fake, never-dereferenced addresses: every case fails in the host checks.
+    assert _fwd(lib, scale=-1.0) == 1
+    assert _fwd(lib, scale=float("nan")) == 1
+    assert _fwd(lib, scale=float("inf")) == 1
+    assert _fwd(lib, D=12) == 4
+    assert _fwd(lib, D=136) == 4
+    assert _fwd(lib, dtype=7) == 1
+    assert _fwd(lib, N=1 << 31) == 3
+    assert _fwd(lib, q=None) == 1
+    assert _fwd(lib, q=24) == 4       # not 16-byte aligned
+    assert _fwd(lib, ws_bytes=8) == 5
+    assert _fwd(lib, ws=None) == 5
+    assert _fwd(lib, H=0) == 1
+    assert _fwd(lib, B=0, N=5) == 1   # tokens without sequences
+    n = ctypes.c_int64(0)
+    assert lib.pe_pack_sequences(16, -1, 4, 16, 16, ctypes.byref(n), 16, 64, None) == 1
+    assert lib.pe_pack_sequences(16, 3, 0, 16, 16, ctypes.byref(n), 16, 64, None) == 1
+    assert lib.pe_pack_sequences(16, 3, 4, 16, 16, ctypes.byref(n), None, 64, None) == 5
+    assert lib.pe_gather_packed(16, 16, 0, 16, 16, None) == 0   # nothing to move
+    assert lib.pe_gather_packed(16, 16, -1, 16, 16, None) == 1
+    assert lib.pe_scatter_padded(16, 16, 0, 4, 16, 16, None) == 0
+
+
+def test_no_gpu_means_unsupported(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(lib) == 4
