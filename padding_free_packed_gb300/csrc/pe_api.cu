@@ -133,6 +133,12 @@ extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t 
   if (query_is_first_token)
     return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, scale, out, lse, stream);
   TilePlan plan = plan_view(workspace, B);
+  if (dtype == PE_BF16 && D == 64) {
+    PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(), S, plan, nullptr,
+                            stream));
+    return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, out, lse, plan,
+                     static_cast<DeviceStatus*>(workspace), stream);
+  }
   PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_tile(), S, plan, nullptr, stream));
   return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, out, lse, N, plan, stream);
 }
@@ -174,6 +180,7 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
     return "unsupported";
   if (backward) return "simt_ffma_bwd";
   if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
+  if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64";
   return "simt_ffma";
 }
 

@@ -271,12 +271,16 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
     const T* kbase = k + (int64_t)start * row_stride + (int64_t)h * D + sub * EPL;
     const T* vbase = v + (int64_t)start * row_stride + (int64_t)h * D + sub * EPL;
     const int step = kWarps * G;
-    for (int32_t j0 = warp * G + group; j0 < len; j0 += 2 * step) {
-      const int32_t j1 = j0 + step;
-      const bool has1 = j1 < len;
+    // The trip count depends only on the warp, never on the lane group, so the
+    // full-warp shuffles below always see all 32 lanes.
+    for (int32_t base = warp * G; base < len; base += 2 * step) {
+      const int32_t j0 = base + group, j1 = j0 + step;
+      const bool has0 = j0 < len, has1 = j1 < len;
       float k0[EPL], k1[EPL], v0[EPL], v1[EPL];
-      load_slice<T, EPL>(kbase + (int64_t)j0 * row_stride, k0);
-      load_slice<T, EPL>(vbase + (int64_t)j0 * row_stride, v0);
+      if (has0) {
+        load_slice<T, EPL>(kbase + (int64_t)j0 * row_stride, k0);
+        load_slice<T, EPL>(vbase + (int64_t)j0 * row_stride, v0);
+      }
       if (has1) {
         load_slice<T, EPL>(kbase + (int64_t)j1 * row_stride, k1);
         load_slice<T, EPL>(vbase + (int64_t)j1 * row_stride, v1);
@@ -284,7 +288,7 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
       float d0 = 0.f, d1 = 0.f;
 #pragma unroll
       for (int u = 0; u < EPL; ++u) {
-        d0 = fmaf(qv[u], k0[u], d0);
+        if (has0) d0 = fmaf(qv[u], k0[u], d0);
         if (has1) d1 = fmaf(qv[u], k1[u], d1);
       }
 #pragma unroll
@@ -292,13 +296,16 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
         d0 += __shfl_xor_sync(0xffffffffu, d0, off);
         d1 += __shfl_xor_sync(0xffffffffu, d1, off);
       }
+      if (!has0) d0 = -INFINITY;
       if (!has1) d1 = -INFINITY;
       const float m_new = fmaxf(m, fmaxf(d0, d1));
+      if (m_new == -INFINITY) continue;  // this group holds no key yet
       const float corr = ex2(m - m_new);
       const float p0 = ex2(d0 - m_new), p1 = ex2(d1 - m_new);
       l = l * corr + p0 + p1;
 #pragma unroll
-      for (int u = 0; u < EPL; ++u) o[u] = o[u] * corr + p0 * v0[u] + (has1 ? p1 * v1[u] : 0.f);
+      for (int u = 0; u < EPL; ++u)
+        o[u] = o[u] * corr + (has0 ? p0 * v0[u] : 0.f) + (has1 ? p1 * v1[u] : 0.f);
       m = m_new;
     }
     // Merge the per-group states of the CTA.

@@ -1,0 +1,485 @@
+// Packed attention forward on the sm_103a tensor cores, bf16 in and out,
+// head_dim 64 (page "Source code for gigl.nn.packed_attention": every sequence
+// attends only to itself within its cu_seqlens bounds; the op returns the
+// output and the log-sum-exp).
+//
+// Design (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: claims work items from the longest-first tile
+//               plan, publishes them to a two-slot ring in shared memory, and
+//               streams Q tiles and K/V blocks of 128 rows x 64 into a
+//               three-stage ring with 128-byte swizzle.
+//   warp 1      tensor-memory owner and MMA issuer: S_t = Q_t K_j^T
+//               (M=128, N=128, K=64) into TMEM, then O_t += P_t V_j
+//               (M=128, N=64, K=128) with P_t read from TMEM.
+//   warps 4-7   softmax for query tile 0; warps 8-11 for query tile 1. Each
+//               thread owns one query row (one TMEM lane): online softmax in
+//               base 2 with fp32 statistics, P written back to TMEM as bf16,
+//               O rescaled in TMEM when the row maximum grows, and the
+//               epilogue (normalise, store the real rows, log-sum-exp).
+// A work item is (sequence, head, pair of 128-row query tiles); both tiles
+// share every K/V block, and while one tile's softmax runs the tensor cores
+// work on the other tile. Keys past the sequence end are masked to -inf;
+// query rows past it are computed but never stored. TMA zero-fills rows
+// beyond the packed buffer.
+//
+// Tensor memory (512 columns): S0 [0,128) S1 [128,256) P0 [256,320)
+// P1 [320,384) O0 [384,448) O1 [448,512).
+//
+// Every wait is bounded: after two seconds the CTA raises an abort flag,
+// records PE_ERR_DEVICE_TIMEOUT in the workspace status word, drains its own
+// copies and MMAs, frees tensor memory and exits.
+#include <cudaTypedefs.h>
+
+#include "pe_kernels.cuh"
+#include "pe_sm103.cuh"
+
+namespace pe {
+
+namespace {
+
+using namespace sm103;
+
+constexpr int kRows = 128;                         // query rows per tile = keys per block
+constexpr int kD = 64;                             // head_dim
+constexpr int kStages = 3;                         // K/V ring depth
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = kRows * kD * 2;    // 16 KiB
+constexpr int kPairRows = 2 * kRows;               // query rows per work item
+
+// Tensor-memory column of S_t, P_t (bf16 pairs) and O_t for query tile t.
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }
+__host__ __device__ constexpr uint32_t col_p(int t) { return 256u + 64u * t; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 384u + 64u * t; }
+constexpr uint32_t kTmemCols = 512;
+
+struct Item {
+  int32_t seq, head, pair, pad;
+};
+
+struct alignas(1024) Smem {
+  __nv_bfloat16 q[2][kRows * kD];
+  __nv_bfloat16 k[kStages][kRows * kD];
+  __nv_bfloat16 v[kStages][kRows * kD];
+  uint64_t item_full[2], item_empty[2];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t drain;
+  Item items[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdParams {
+  const int32_t* cu;
+  int32_t B, H;
+  float scale_log2;
+  __nv_bfloat16* out;
+  float* lse;
+  int64_t lse_stride;
+  TilePlan plan;
+  DeviceStatus* status;
+};
+
+// Where a wait gave up (recorded in the status word's detail field).
+enum WaitSite { kSiteProducer = 1, kSiteMma = 2, kSiteSoftmax = 3 };
+
+__device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item& it) {
+  int32_t seq, local;
+  plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
+  const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
+  const int32_t npairs = (len + kPairRows - 1) / kPairRows;
+  it.seq = seq;
+  it.head = local / npairs;
+  it.pair = local - it.head * npairs;
+  it.pad = 0;
+}
+
+// A wait taken by all 32 lanes of a warp that succeeds only if it succeeds in
+// every lane, so the warp-collective tcgen05 operations after it never run on
+// a partial warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          DeviceStatus* status, int where) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &S.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&S.item_full[i]), 1);
+      mbar_init(smem_u32(&S.item_empty[i]), 1 + 8);
+      mbar_init(smem_u32(&S.s_full[i]), 1);
+      mbar_init(smem_u32(&S.p_full[i]), 128);
+      mbar_init(smem_u32(&S.o_full[i]), 1);
+    }
+    mbar_init(smem_u32(&S.q_full), 1);
+    mbar_init(smem_u32(&S.q_empty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&S.k_full[s]), 1);
+      mbar_init(smem_u32(&S.v_full[s]), 1);
+      mbar_init(smem_u32(&S.kv_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&S.drain), 1);
+    S.abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&S.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const int32_t total = *p.plan.total_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      uint32_t kv_no = 0;
+      int pending_q = -1;                // parity of the last Q load not yet known complete
+      int pending_kv[kStages];           // parity of the last K/V load per stage
+      for (int s = 0; s < kStages; ++s) pending_kv[s] = -1;
+      bool ok = true;
+      for (uint32_t item_no = 0; ok; ++item_no) {
+        const int slot = item_no & 1;
+        if (!mbar_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
+                       p.status, kSiteProducer)) {
+          ok = false;
+          break;
+        }
+        const int32_t t = atomicAdd(p.plan.counter, 1);
+        Item it;
+        if (t >= total) {
+          it.seq = -1;
+          it.head = it.pair = it.pad = 0;
+        } else {
+          decode_item(p, t, it);
+        }
+        S.items[slot] = it;
+        mbar_arrive(smem_u32(&S.item_full[slot]));
+        if (it.seq < 0) break;
+        const int32_t start = __ldg(p.cu + it.seq);
+        const int32_t len = __ldg(p.cu + it.seq + 1) - start;
+        const int32_t r0 = it.pair * kPairRows;
+        const int ntiles = (len - r0 > kRows) ? 2 : 1;
+        const int32_t nkv = (len + kRows - 1) / kRows;
+        const int32_t x = it.head * kD;
+        if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
+                       kSiteProducer)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
+        for (int tt = 0; tt < ntiles; ++tt)
+          tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full), x, start + r0 + tt * kRows);
+        pending_q = item_no & 1;
+        for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
+          const int s = kv_no % kStages;
+          const uint32_t ph = (kv_no / kStages) & 1;
+          if (!mbar_wait(smem_u32(&S.kv_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
+          tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x, start + j * kRows);
+          mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
+          tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x, start + j * kRows);
+          pending_kv[s] = (int)ph;
+        }
+      }
+      if (!ok) {
+        // Let every copy this thread started land before the CTA exits.
+        if (pending_q >= 0) mbar_drain_wait(smem_u32(&S.q_full), (uint32_t)pending_q);
+        for (int s = 0; s < kStages; ++s)
+          if (pending_kv[s] >= 0) {
+            mbar_drain_wait(smem_u32(&S.k_full[s]), (uint32_t)pending_kv[s]);
+            mbar_drain_wait(smem_u32(&S.v_full[s]), (uint32_t)pending_kv[s]);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kRows, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
+      uint32_t kv_no = 0;
+      uint32_t p_cnt[2] = {0, 0};
+      const uint32_t q_addr[2] = {smem_u32(S.q[0]), smem_u32(S.q[1])};
+      auto issue_qk = [&](int t, int s) {
+        const uint32_t k_addr = smem_u32(S.k[s]);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + col_s(t), smem_desc_sw128(q_addr[t] + kk * 32, 16, 1024),
+                 smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+      };
+      auto issue_pv = [&](int t, int s, bool accumulate) {
+        const uint32_t v_addr = smem_u32(S.v[s]);
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          mma_ts(tmem + col_o(t), tmem + col_p(t) + kk * 8,
+                 smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      for (uint32_t item_no = 0; ok; ++item_no) {
+        const int slot = item_no & 1;
+        if (!mbar_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+                       kSiteMma)) {
+          ok = false;
+          break;
+        }
+        const Item it = S.items[slot];
+        mbar_arrive(smem_u32(&S.item_empty[slot]));
+        if (it.seq < 0) break;
+        const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
+        const int32_t r0 = it.pair * kPairRows;
+        const int ntiles = (len - r0 > kRows) ? 2 : 1;
+        const int32_t nkv = (len + kRows - 1) / kRows;
+        if (!mbar_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) {
+          ok = false;
+          break;
+        }
+        {
+          const int s0 = kv_no % kStages;
+          if (!mbar_wait(smem_u32(&S.k_full[s0]), (kv_no / kStages) & 1, abort_flag, p.status,
+                         kSiteMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int t = 0; t < ntiles; ++t) {
+            issue_qk(t, s0);
+            tc_commit(smem_u32(&S.s_full[t]));
+          }
+        }
+        for (int32_t j = 0; j < nkv && ok; ++j) {
+          const uint32_t c = kv_no + j;
+          const int s = c % kStages;
+          if (!mbar_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
+                         kSiteMma)) {
+            ok = false;
+            break;
+          }
+          const bool has_next = j + 1 < nkv;
+          const int sn = (c + 1) % kStages;
+          if (has_next && !mbar_wait(smem_u32(&S.k_full[sn]), ((c + 1) / kStages) & 1,
+                                     abort_flag, p.status, kSiteMma)) {
+            ok = false;
+            break;
+          }
+          for (int t = 0; t < ntiles; ++t) {
+            if (!mbar_wait(smem_u32(&S.p_full[t]), p_cnt[t] & 1, abort_flag, p.status,
+                           kSiteMma)) {
+              ok = false;
+              break;
+            }
+            ++p_cnt[t];
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            if (has_next) {
+              issue_qk(t, sn);
+              tc_commit(smem_u32(&S.s_full[t]));
+            } else {
+              tc_commit(smem_u32(&S.o_full[t]));
+            }
+          }
+          if (ok) tc_commit(smem_u32(&S.kv_empty[s]));
+        }
+        kv_no += nkv;
+        if (ok) tc_commit(smem_u32(&S.q_empty));
+      }
+      // Every MMA this thread issued must finish before tensor memory is freed.
+      tc_commit(smem_u32(&S.drain));
+      mbar_drain_wait(smem_u32(&S.drain), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;               // query tile of this warpgroup
+    const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
+    const int row = quarter * 32 + lane;         // query row within the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint32_t s_cnt = 0, o_cnt = 0;
+    const float scale_log2 = p.scale_log2;
+    for (uint32_t item_no = 0;; ++item_no) {
+      const int slot = item_no & 1;
+      if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+                     kSiteSoftmax))
+        break;
+      const Item it = S.items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
+      if (it.seq < 0) break;
+      const int32_t start = __ldg(p.cu + it.seq);
+      const int32_t len = __ldg(p.cu + it.seq + 1) - start;
+      const int32_t r0 = it.pair * kPairRows + t * kRows;
+      if (r0 >= len) continue;                   // this tile of the pair is empty
+      const int32_t nkv = (len + kRows - 1) / kRows;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int32_t j = 0; j < nkv; ++j) {
+        if (!warp_wait(smem_u32(&S.s_full[t]), s_cnt & 1, abort_flag, p.status, kSiteSoftmax)) {
+          ok = false;
+          break;
+        }
+        ++s_cnt;
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + col_s(t) + 32 * c, sr[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+        const int32_t kv_valid = len - j * kRows;  // > 0; columns at or past it are masked
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = (32 * c + e < kv_valid) ? __uint_as_float(sr[c][e]) * scale_log2
+                                                    : -INFINITY;
+            sr[c][e] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+        const float m_new = fmaxf(m, mx);
+        const float alpha = ex2(m - m_new);      // 0 on the first block, 1 if the max held
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(__uint_as_float(sr[c][2 * e]) - m_new);
+            const float p1 = ex2(__uint_as_float(sr[c][2 * e + 1]) - m_new);
+            sum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(lane_base + col_p(t) + 16 * c, pk);
+        }
+        l = l * alpha + sum;
+        m = m_new;
+        // O already holds P(j-1) V(j-1): rescale it when the row maximum grew.
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + col_o(t) + 32 * h, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(lane_base + col_o(t) + 32 * h, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&S.p_full[t]));
+      }
+      if (!ok) break;
+      if (!warp_wait(smem_u32(&S.o_full[t]), o_cnt & 1, abort_flag, p.status, kSiteSoftmax))
+        break;
+      ++o_cnt;
+      tc_fence_after();
+      uint32_t o[2][32];
+      tmem_ld32(lane_base + col_o(t), o[0]);
+      tmem_ld32(lane_base + col_o(t) + 32, o[1]);
+      tmem_wait_ld(o[0]);
+      tmem_wait_ld(o[1]);
+      if (r0 + row < len) {
+        const int64_t tok = static_cast<int64_t>(start) + r0 + row;
+        const float inv = 1.f / l;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + it.head) * kD);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t* src = o[g >> 2] + (g & 3) * 8;
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+          dst[g] = w;
+        }
+        if (p.lse) p.lse[static_cast<int64_t>(it.head) * p.lse_stride + tok] =
+            (m + __log2f(l)) * kLn2;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pe_status get_encoder() {
+  if (g_encode) return PE_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult qres;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &qres) != cudaSuccess ||
+      qres != cudaDriverEntryPointSuccess || !fn)
+    return PE_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return PE_OK;
+}
+
+// [N, H*64] bf16 rows; boxes of 128 rows x 64 columns (one head), 128-byte swizzle.
+pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * kD, static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * kD * 2};
+  cuuint32_t box[2] = {kD, kRows};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PE_OK : PE_ERR_CUDA;
+}
+
+}  // namespace
+
+int sm103_fwd_rows_per_item() { return kPairRows; }
+
+pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
+                    int32_t H, int64_t N, float scale, void* out, float* lse, TilePlan plan,
+                    DeviceStatus* status, cudaStream_t stream) {
+  PE_TRY(get_encoder());
+  CUtensorMap mq, mk, mv;
+  PE_TRY(make_map(&mq, q, N, H));
+  PE_TRY(make_map(&mk, k, N, H));
+  PE_TRY(make_map(&mv, v, N, H));
+  const size_t smem = sizeof(Smem) + 1024;
+  PE_CUDA_TRY(cudaFuncSetAttribute(fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(smem)));
+  FwdParams prm;
+  prm.cu = cu;
+  prm.B = B;
+  prm.H = H;
+  prm.scale_log2 = scale * kLog2e;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.lse_stride = N;
+  prm.plan = plan;
+  prm.status = status;
+  fwd_sm103_kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, prm);
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+}  // namespace pe

@@ -177,3 +177,36 @@ def test_unsupported_arguments_raise():
         pe.pe_packed_attention_fwd(q[:, :, :12].contiguous(), k[:, :, :12].contiguous(),
                                    v[:, :, :12].contiguous(), cu_d, 5, 0.3)
     assert e.value.status == 4
+
+
+def test_bf16_d64_runs_on_tensor_cores_and_reports_clean_status():
+    assert pe.pe_attention_kernel(torch.bfloat16, 64) == "tcgen05_bf16_d64"
+    assert pe.pe_attention_kernel(torch.float32, 64) == "simt_ffma"
+    assert pe.pe_attention_kernel(torch.bfloat16, 64, query_is_first_token=True) == \
+        "first_token_gemv"
+    # Lengths chosen so work items hit every case of the 256-row query pair:
+    # second tile empty, second tile partial, both full, and a single row.
+    lengths = [128, 129, 256, 257, 384, 385, 512, 1, 100, 640, 1000]
+    x = workloads.make_custom(lengths, 5, 64, torch.bfloat16, seed=31)
+    s = max(lengths)
+    cu, cu_d, q, k, v = _device_inputs(x)
+    ws = torch.empty(pe.attention_workspace_bytes(torch.bfloat16, len(lengths), q.shape[0], 5, 64,
+                                                  s), dtype=torch.uint8, device=DEV)
+    out, lse = pe.pe_packed_attention_fwd(q, k, v, cu_d, s, 0.125, need_lse=True, workspace=ws)
+    assert pe.pe_read_device_status(ws) == 0
+    ref, ref_lse = oracle.attention_fwd(x.q, x.k, x.v, cu, s, 0.125)
+    check(out, ref, "bf16", "tensor-core pairs")
+    assert float(np.abs(to64(lse) - ref_lse).max()) <= 2e-3
+
+
+def test_many_work_items_per_cta():
+    """More work items than CTAs, so each persistent CTA runs many items and
+    the K/V ring and barriers wrap around many times."""
+    rng = np.random.default_rng(32)
+    lengths = rng.integers(1, 700, 400).astype(np.int32)
+    x = workloads.make_custom(lengths, 8, 64, torch.bfloat16, seed=33)
+    s = int(lengths.max())
+    cu, cu_d, q, k, v = _device_inputs(x)
+    out, _ = pe.pe_packed_attention_fwd(q, k, v, cu_d, s, 0.125)
+    ref, _ = oracle.attention_fwd(x.q, x.k, x.v, cu, s, 0.125)
+    check(out, ref, "bf16", "many items")
