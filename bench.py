@@ -158,7 +158,8 @@ def run_ours(args, rank, world):
     pe.load_library()
     wl = workloads.WORKLOADS[args.workload]
     # Weak scaling: every rank draws its own batch of the same workload.
-    lengths, gq, gk, gv = workloads.make_padded_inputs(args.workload, seed=args.seed + rank)
+    lengths, gq, gk, gv = workloads.make_padded_inputs(args.workload, seed=args.seed + rank,
+                                                       max_sequences=args.sequences)
     s, h, d = wl.max_seq_len, wl.num_heads, wl.head_dim
     n_tokens = int(lengths.astype(np.int64).sum())
     flops = real_flops(lengths, h, d)
@@ -268,7 +269,8 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": args.workload, "description": wl.description,
+        "config": {"workload": args.workload + (f"[:{args.sequences}]" if args.sequences else ""),
+                   "description": wl.description,
                    "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
                    "heads": h, "head_dim": d, "max_seq_len": s,
                    "step": "pack + gather q,k,v + tile plan + attention forward + scatter",
@@ -365,6 +367,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="longdoc_bf16")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sequences", type=int, default=None,
+                    help="keep only the first K sequences of the workload (profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=24576,

@@ -152,16 +152,20 @@ def make_custom(lengths, num_heads: int, head_dim: int, dtype: torch.dtype,
     return Inputs(wl, lengths, q, k, v, dout)
 
 
-def make_padded_inputs(name: str, seed: int = 0) -> tuple[np.ndarray, torch.Tensor, torch.Tensor, torch.Tensor]:
+def make_padded_inputs(name: str, seed: int = 0, max_sequences: int | None = None
+                       ) -> tuple[np.ndarray, torch.Tensor, torch.Tensor, torch.Tensor]:
     """Lengths plus q, k, v drawn directly as padded ``[B, S, H, d]`` grids.
 
-    The lengths come from the same first draw as ``make_inputs``; every grid row,
+    The lengths come from the same first draw as ``make_inputs`` (optionally
+    only the first ``max_sequences`` of them); every grid row,
     pad rows included, then holds fresh N(0, 1) values drawn in float32 (pad rows
     are never meant to be read). These are the inputs of a padded-to-packed step.
     """
     wl = WORKLOADS[name]
     rng = np.random.default_rng(seed)
     lengths = draw_lengths(name, rng)
+    if max_sequences is not None:
+        lengths = np.ascontiguousarray(lengths[:max_sequences])
     shape = (int(lengths.shape[0]), wl.max_seq_len, wl.num_heads, wl.head_dim)
     grids = []
     for _ in range(3):
