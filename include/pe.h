@@ -172,6 +172,32 @@ pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t num_sequences, int64_t
 const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_first_token,
                                 int backward);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free forward. The pages have no counterpart to this call; it
+ * exists for callers that cannot give the library a workspace: a host
+ * runtime that owns every device allocation through its own fixed pool and
+ * exposes no scratch API (a serving process, a framework plugin), or a
+ * latency-critical loop where cudaMalloc/cudaFree would add implicit
+ * device-wide synchronisation.
+ *
+ * Same arguments and results as pe_packed_attention_fwd without the
+ * workspace. The scratch (status word and tile plan) lives in a 512 KiB
+ * device array inside the library that every GPU loading it holds until the
+ * process exits; num_sequences may be at most 65536, larger batches return
+ * PE_ERR_WORKSPACE before anything runs. The call allocates nothing.
+ * The first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * All calls on a device share the array and it keeps the last call's
+ * contents (the call clears what must start at zero itself): calls whose
+ * executions overlap on the GPU race and must be serialised by the caller.
+ * ------------------------------------------------------------------------ */
+pe_status pe_packed_attention_fwd_noalloc(pe_dtype dtype, int32_t num_sequences,
+                                          int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                          int32_t max_seq_len, const void* q, const void* k,
+                                          const void* v, const int32_t* cu_seqlens, float scale,
+                                          int query_is_first_token, void* out, float* lse,
+                                          pe_stream_t stream);
+
 /* Synchronizes `stream` and returns the device-side status that the last
  * attention call on `workspace` left in its first 4 bytes (PE_OK when every
  * pipeline wait completed). */
