@@ -158,35 +158,58 @@ def run_ours(args, rank, world):
     pe.load_library()
     wl = workloads.WORKLOADS[args.workload]
     # Weak scaling: every rank draws its own batch of the same workload.
-    lengths, gq, gk, gv = workloads.make_padded_inputs(args.workload, seed=args.seed + rank,
-                                                       max_sequences=args.sequences)
+    train = wl.backward
+    drawn = workloads.make_padded_inputs(args.workload, seed=args.seed + rank,
+                                         max_sequences=args.sequences, with_dout=train)
+    lengths, gq, gk, gv = drawn[:4]
+    gdo = drawn[4] if train else None
     s, h, d = wl.max_seq_len, wl.num_heads, wl.head_dim
     n_tokens = int(lengths.astype(np.int64).sum())
-    flops = real_flops(lengths, h, d)
+    fwd_flops = real_flops(lengths, h, d)
+    bwd_flops = 2.5 * fwd_flops if train else 0.0   # 10 sum L^2 H d: five GEMM-shaped products
+    flops = fwd_flops + bwd_flops
     kernel = pe.pe_attention_kernel(wl.torch_dtype, d)
+    bwd_kernel = pe.pe_attention_kernel(wl.torch_dtype, d, backward=True) if train else None
 
     lengths_d = torch.from_numpy(lengths).to(dev)
     qg, kg, vg = gq.to(dev), gk.to(dev), gv.to(dev)
+    dog = gdo.to(dev) if train else None
     og = torch.empty_like(qg)
+    grad_grids = [torch.empty_like(qg) for _ in range(3)] if train else None
     stream = torch.cuda.current_stream(dev)
-    fwd_events = []
+    fwd_events, bwd_events = [], []
 
-    def step(lengths_t, q_grid, k_grid, v_grid, out_grid, record):
+    def timed(record, events, fn):
+        if not record:
+            return fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        result = fn()
+        e1.record(stream)
+        events.append((e0, e1))
+        return result
+
+    def step(lengths_t, q_grid, k_grid, v_grid, out_grid, record, do_grid=None):
         flat, cu, n = pe.pe_pack_sequences(lengths_t, s)
         q = pe.pe_gather_packed(q_grid, flat, n)
         k = pe.pe_gather_packed(k_grid, flat, n)
         v = pe.pe_gather_packed(v_grid, flat, n)
-        if record:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        out, _ = pe.pe_packed_attention_fwd(q, k, v, cu, s, wl.scale)
-        if record:
-            e1.record(stream)
-            fwd_events.append((e0, e1))
+        out, lse = timed(record, fwd_events,
+                         lambda: pe.pe_packed_attention_fwd(q, k, v, cu, s, wl.scale,
+                                                            need_lse=train))
         pe.pe_scatter_padded(out, cu, s, out=out_grid)
+        if train:
+            do = pe.pe_gather_packed(do_grid, flat, n)
+            grads = timed(record, bwd_events,
+                          lambda: pe.pe_packed_attention_bwd(do, q, k, v, out, lse, cu, s,
+                                                             wl.scale))
+            for g, grid in zip(grads, grad_grids):
+                pe.pe_scatter_padded(g, cu, s, out=grid)
         return n
 
-    launches_per_step = 2 + 3 + 2 + 1  # pack scan+fill, 3 gathers, plan+attention, scatter
+    # pack scan+fill, 3 gathers, plan+attention, scatter; training adds the dO
+    # gather, the backward (delta, plan, key pass, plan, query pass) and 3 scatters.
+    launches_per_step = 2 + 3 + 2 + 1 + ((1 + 5 + 3) if train else 0)
 
     def barrier():
         if world > 1:
@@ -194,17 +217,18 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step(lengths_d, qg, kg, vg, og, False)
+        step(lengths_d, qg, kg, vg, og, False, dog)
     barrier()
     with ClockSampler(local_rank) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for _ in range(args.steps):
-            step(lengths_d, qg, kg, vg, og, True)
+            step(lengths_d, qg, kg, vg, og, True, dog)
         end.record(stream)
         barrier()
     elapsed_ms = start.elapsed_time(end)
     fwd_ms = sum(a.elapsed_time(b) for a, b in fwd_events) / len(fwd_events)
+    bwd_ms = sum(a.elapsed_time(b) for a, b in bwd_events) / len(bwd_events) if train else 0.0
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -215,19 +239,20 @@ def run_ours(args, rank, world):
     # output back to pinned host memory, copies inside the timed region.
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv = (t.pin_memory() for t in (gq, gk, gv))
+        host_in = [t.pin_memory() for t in ((gq, gk, gv, gdo) if train else (gq, gk, gv))]
         hlen = torch.from_numpy(lengths).pin_memory()
-        hout = torch.empty_like(gq).pin_memory()
-        dq, dk, dv = torch.empty_like(qg), torch.empty_like(kg), torch.empty_like(vg)
+        dev_in = [torch.empty_like(t, device=dev) for t in host_in]
         dlen = torch.empty_like(lengths_d)
+        results = [og] + (grad_grids if train else [])
+        host_out = [torch.empty_like(gq).pin_memory() for _ in results]
 
         def e2e_step():
             dlen.copy_(hlen, non_blocking=True)
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            step(dlen, dq, dk, dv, og, False)
-            hout.copy_(og, non_blocking=True)
+            for dst, src in zip(dev_in, host_in):
+                dst.copy_(src, non_blocking=True)
+            step(dlen, *dev_in[:3], og, False, dev_in[3] if train else None)
+            for dst, src in zip(host_out, results):
+                dst.copy_(src, non_blocking=True)
 
         for _ in range(max(1, min(args.warmup, 3))):
             e2e_step()
@@ -245,16 +270,21 @@ def run_ours(args, rank, world):
             t = torch.tensor([e2e_ms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        h2d = sum(x.numel() * x.element_size() for x in (hlen, hq, hk, hv))
-        d2h = hout.numel() * hout.element_size()
+        h2d = sum(x.numel() * x.element_size() for x in [hlen] + host_in)
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks, peaks_src = load_peaks()
-    if kernel.startswith("tcgen05"):
+    # The dominant kernel: the forward, or the backward when it takes longer.
+    if train and bwd_ms > fwd_ms:
+        dom_kernel, dom_flops, dom_ms = bwd_kernel, bwd_flops, bwd_ms
+    else:
+        dom_kernel, dom_flops, dom_ms = kernel, fwd_flops, fwd_ms
+    if dom_kernel.startswith("tcgen05"):
         bound, peak, unit = "tensor", float(peaks["bf16_tflops"]), "TFLOP/s"
         peak_note = f"dense bf16 burst, {peaks_src}"
-    elif kernel == "first_token_gemv":
+    elif dom_kernel == "first_token_gemv":
         bound, peak, unit = "hbm", float(peaks["hbm_gbs"]), "GB/s"
         peak_note = f"HBM copy, {peaks_src}"
     else:
@@ -262,8 +292,8 @@ def run_ours(args, rank, world):
                 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12)
         bound, peak, unit = "alu", ffma, "TFLOP/s"
         peak_note = "FFMA: SMs x 128 lanes x 2 flop x max SM clock"
-    achieved = flops / (fwd_ms * 1e-3) / 1e12
-    traffic = committed_traffic(kernel, KERNEL_SOURCES.get(kernel, ""))
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    traffic = committed_traffic(dom_kernel, KERNEL_SOURCES.get(dom_kernel, ""))
     value = world * flops / (ms_per_step * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -273,14 +303,20 @@ def run_ours(args, rank, world):
                    "description": wl.description,
                    "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
                    "heads": h, "head_dim": d, "max_seq_len": s,
-                   "step": "pack + gather q,k,v + tile plan + attention forward + scatter",
-                   "l2": "inputs larger than L2 (three padded grids of "
-                         f"{gq.numel() * gq.element_size() / 1e9:.2f} GB); no flush",
+                   "step": ("pack + gather q,k,v,dO + tile plan + attention forward + scatter "
+                            "+ attention backward + scatter dq,dk,dv" if train else
+                            "pack + gather q,k,v + tile plan + attention forward + scatter"),
+                   "flops_per_step": flops,
+                   "l2": (f"inputs larger than L2 ({len(drawn) - 1} padded grids of "
+                          f"{gq.numel() * gq.element_size() / 1e9:.2f} GB); no flush"),
                    "parallelism": f"dp{world} (independent batches per GPU, no collective)"},
         "tokens_per_s": world * n_tokens / (ms_per_step * 1e-3),
         "pct_of_tensor_peak": 100.0 * value / world / float(peaks["bf16_tflops"]),
         "attention_kernel": kernel,
         "attention_ms": fwd_ms,
+        "backward_kernel": bwd_kernel,
+        "backward_ms": bwd_ms if train else None,
+        "roofline_kernel": dom_kernel,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
                      "frac_of_sustained": (achieved / float(peaks["bf16_tflops_sustained"])

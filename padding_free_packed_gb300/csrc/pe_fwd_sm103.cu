@@ -342,35 +342,57 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
         const int32_t kv_valid = len - j * kRows;  // > 0; columns at or past it are masked
-        float mx = -INFINITY;
+        if (kv_valid < kRows) {                    // only a sequence's last key block
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e >= kv_valid) sr[c][e] = 0xff800000u;  // -inf
+        }
+        // Row maximum of the raw scores (scale > 0 commutes with max), four
+        // independent chains of 3-input max.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = (32 * c + e < kv_valid) ? __uint_as_float(sr[c][e]) * scale_log2
-                                                    : -INFINITY;
-            sr[c][e] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
-          }
-        const float m_new = fmaxf(m, mx);
-        const float alpha = ex2(m - m_new);      // 0 on the first block, 1 if the max held
-        float sum = 0.f;
+          for (int e = 0; e < 32; e += 8)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              mx[u] = max3(mx[u], __uint_as_float(sr[c][e + 2 * u]),
+                           __uint_as_float(sr[c][e + 2 * u + 1]));
+        const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+        // Lazy rescaling: the running maximum moves only when the block's
+        // maximum exceeds it by more than 2^8; until then exponents stay <= 2^8.
+        const bool grow = m_blk > m + 8.f;
+        const float m_new = grow ? m_blk : m;
+        const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first block
+        const uint64_t c2 = f2(scale_log2, scale_log2), nm2 = f2(-m_new, -m_new);
+        uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(__uint_as_float(sr[c][2 * e]) - m_new);
-            const float p1 = ex2(__uint_as_float(sr[c][2 * e + 1]) - m_new);
-            sum += p0 + p1;
+            const uint64_t x = ffma2(f2(__uint_as_float(sr[c][2 * e]),
+                                        __uint_as_float(sr[c][2 * e + 1])), c2, nm2);
+            float p0, p1;
+            f2_split(x, p0, p1);
+            p0 = ex2(p0);
+            p1 = ex2(p1);
+            acc[e & 3] = fadd2(acc[e & 3], f2(p0, p1));
             pk[e] = pack_bf16x2(p0, p1);
           }
           tmem_st16(lane_base + col_p(t) + 16 * c, pk);
         }
-        l = l * alpha + sum;
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2_split(acc[0], s0, s1);
+        f2_split(acc[1], s2, s3);
+        f2_split(acc[2], s4, s5);
+        f2_split(acc[3], s6, s7);
+        l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
         m = m_new;
-        // O already holds P(j-1) V(j-1): rescale it when the row maximum grew.
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O already holds P(j-1) V(j-1): rescale it when some row's maximum moved.
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t o[32];

@@ -152,14 +152,15 @@ def make_custom(lengths, num_heads: int, head_dim: int, dtype: torch.dtype,
     return Inputs(wl, lengths, q, k, v, dout)
 
 
-def make_padded_inputs(name: str, seed: int = 0, max_sequences: int | None = None
-                       ) -> tuple[np.ndarray, torch.Tensor, torch.Tensor, torch.Tensor]:
+def make_padded_inputs(name: str, seed: int = 0, max_sequences: int | None = None,
+                       with_dout: bool = False) -> tuple:
     """Lengths plus q, k, v drawn directly as padded ``[B, S, H, d]`` grids.
 
     The lengths come from the same first draw as ``make_inputs`` (optionally
     only the first ``max_sequences`` of them); every grid row,
     pad rows included, then holds fresh N(0, 1) values drawn in float32 (pad rows
     are never meant to be read). These are the inputs of a padded-to-packed step.
+    Returns (lengths, q, k, v), plus a dO grid drawn last when ``with_dout``.
     """
     wl = WORKLOADS[name]
     rng = np.random.default_rng(seed)
@@ -168,7 +169,7 @@ def make_padded_inputs(name: str, seed: int = 0, max_sequences: int | None = Non
         lengths = np.ascontiguousarray(lengths[:max_sequences])
     shape = (int(lengths.shape[0]), wl.max_seq_len, wl.num_heads, wl.head_dim)
     grids = []
-    for _ in range(3):
+    for _ in range(4 if with_dout else 3):
         x = torch.from_numpy(rng.standard_normal(shape, dtype=np.float32))
         grids.append(x.to(wl.torch_dtype) if wl.torch_dtype != torch.float32 else x)
-    return lengths, grids[0], grids[1], grids[2]
+    return (lengths, *grids)
