@@ -7,10 +7,14 @@
 //   warp 0      TMA producer: claims work items from the longest-first tile
 //               plan, publishes them to a two-slot ring in shared memory, and
 //               streams Q tiles and K/V blocks of 128 rows x 64 into a
-//               three-stage ring with 128-byte swizzle.
-//   warp 1      tensor-memory owner and MMA issuer: S_t = Q_t K_j^T
-//               (M=128, N=128, K=64) into TMEM, then O_t += P_t V_j
-//               (M=128, N=64, K=128) with P_t read from TMEM.
+//               four-stage ring with 128-byte swizzle.
+//   warps 1, 2  MMA issuers, one per query tile (warp 1 also owns tensor
+//               memory): S_t = Q_t K_j^T (M=128, N=128, K=64) into TMEM as soon
+//               as the softmax has read S_t of the previous block, so the next
+//               scores are computed during this block's softmax; then
+//               O_t += P_t V_j (M=128, N=64, K=128) with P_t read from TMEM.
+//               A thread issues at most one MMA per ~130 cycles, so issue is
+//               spread over two warps (whole warps, elect.sync).
 //   warps 4-7   softmax for query tile 0; warps 8-11 for query tile 1. Each
 //               thread owns one query row (one TMEM lane): online softmax in
 //               base 2 with fp32 statistics, P written back to TMEM as bf16,
@@ -41,7 +45,8 @@ using namespace sm103;
 
 constexpr int kRows = 128;                         // query rows per tile = keys per block
 constexpr int kD = 64;                             // head_dim
-constexpr int kStages = 3;                         // K/V ring depth
+constexpr int kStages = 4;                         // K/V ring depth
+constexpr int kIssueWarps = 2;                     // MMA-issuing warps: 1 (both tiles) or 2 (one per tile)
 constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = kRows * kD * 2;    // 16 KiB
 constexpr int kPairRows = 2 * kRows;               // query rows per work item
@@ -63,8 +68,8 @@ struct alignas(1024) Smem {
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t drain;
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2];
+  uint64_t drain[2];
   Item items[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -95,15 +100,6 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
   it.pad = 0;
 }
 
-// A wait taken by all 32 lanes of a warp that succeeds only if it succeeds in
-// every lane, so the warp-collective tcgen05 operations after it never run on
-// a partial warp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          DeviceStatus* status, int where) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, status, where);
-  return __all_sync(0xffffffffu, ok);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -116,19 +112,22 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&S.item_full[i]), 1);
-      mbar_init(smem_u32(&S.item_empty[i]), 1 + 8);
+      mbar_init(smem_u32(&S.item_empty[i]), kIssueWarps + 8);
       mbar_init(smem_u32(&S.s_full[i]), 1);
+      mbar_init(smem_u32(&S.s_free[i]), 4);
+      mbar_init(smem_u32(&S.pv_done[i]), 1);
       mbar_init(smem_u32(&S.p_full[i]), 128);
       mbar_init(smem_u32(&S.o_full[i]), 1);
     }
     mbar_init(smem_u32(&S.q_full), 1);
-    mbar_init(smem_u32(&S.q_empty), 1);
+    mbar_init(smem_u32(&S.q_empty), kIssueWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&S.k_full[s]), 1);
       mbar_init(smem_u32(&S.v_full[s]), 1);
-      mbar_init(smem_u32(&S.kv_empty[s]), 1);
+      mbar_init(smem_u32(&S.kv_empty[s]), kIssueWarps);
     }
-    mbar_init(smem_u32(&S.drain), 1);
+    mbar_init(smem_u32(&S.drain[0]), 1);
+    mbar_init(smem_u32(&S.drain[1]), 1);
     S.abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -139,7 +138,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = S.tmem_base;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, S.tmem_base, 0);
   const int32_t total = *p.plan.total_tiles;
 
   if (warp == 0) {
@@ -210,108 +209,121 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kRows, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
-      uint32_t kv_no = 0;
-      uint32_t p_cnt[2] = {0, 0};
-      const uint32_t q_addr[2] = {smem_u32(S.q[0]), smem_u32(S.q[1])};
-      auto issue_qk = [&](int t, int s) {
-        const uint32_t k_addr = smem_u32(S.k[s]);
+  } else if (warp == 1 || (kIssueWarps == 2 && warp == 2)) {
+    // ------------------------------------------------------------ MMA issuers (whole warps)
+    // S_t for key block j+1 is computed as soon as the softmax has read S_t(j),
+    // so it overlaps that softmax; P_t V_j follows when P_t(j) arrives.
+    const int my_tile = warp - 1;
+    constexpr uint32_t idesc_qk = idesc_bf16(kRows, kRows, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
+    uint32_t kv_no = 0;
+    uint32_t n_qk[2] = {0, 0}, n_pv[2] = {0, 0};   // MMAs issued per tile, all items
+    auto issue_qk = [&](int t, int s) {
+      const uint32_t q_addr = smem_u32(S.q[t]), k_addr = smem_u32(S.k[s]);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + col_s(t), smem_desc_sw128(q_addr[t] + kk * 32, 16, 1024),
-                 smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-      };
-      auto issue_pv = [&](int t, int s, bool accumulate) {
-        const uint32_t v_addr = smem_u32(S.v[s]);
+      for (int kk = 0; kk < kD / 16; ++kk)
+        mma_ss_warp(tmem + col_s(t), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
+                    smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+    };
+    auto issue_pv = [&](int t, int s, bool accumulate) {
+      const uint32_t v_addr = smem_u32(S.v[s]);
 #pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk)
-          mma_ts(tmem + col_o(t), tmem + col_p(t) + kk * 8,
-                 smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
-                 (accumulate || kk > 0) ? 1u : 0u);
-      };
-      bool ok = true;
-      for (uint32_t item_no = 0; ok; ++item_no) {
-        const int slot = item_no & 1;
-        if (!mbar_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+      for (int kk = 0; kk < kRows / 16; ++kk)
+        mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
+                    smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
+                    (accumulate || kk > 0) ? 1u : 0u);
+    };
+    // Issues S_t = Q_t K_s^T once the softmax has read the previous S_t.
+    auto qk = [&](int t, int s) -> bool {
+      if (n_qk[t] > 0 &&
+          !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag, p.status, kSiteMma))
+        return false;
+      tc_fence_after();
+      issue_qk(t, s);
+      tc_commit_warp(smem_u32(&S.s_full[t]));
+      ++n_qk[t];
+      return true;
+    };
+    bool ok = true;
+    for (uint32_t item_no = 0; ok; ++item_no) {
+      const int slot = item_no & 1;
+      if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+                     kSiteMma))
+        break;
+      const Item it = S.items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
+      if (it.seq < 0) break;
+      const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
+      const int32_t r0 = it.pair * kPairRows;
+      const int ntiles = (len - r0 > kRows) ? 2 : 1;
+      const int32_t nkv = (len + kRows - 1) / kRows;
+      int t_lo = 0, t_hi = ntiles, releases = 1;
+      if (kIssueWarps == 2) {
+        // One warp per tile; with a single tile, the tile-0 warp also makes
+        // the tile-1 warp's arrivals on the shared K/V and Q release barriers.
+        t_lo = my_tile;
+        t_hi = my_tile < ntiles ? my_tile + 1 : my_tile;
+        releases = (ntiles == 1) ? 2 : 1;
+        if (t_lo == t_hi) {
+          kv_no += nkv;
+          continue;
+        }
+      }
+      if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
+      {
+        const int s0 = kv_no % kStages;
+        if (!warp_wait(smem_u32(&S.k_full[s0]), (kv_no / kStages) & 1, abort_flag, p.status,
+                       kSiteMma))
+          break;
+        for (int t = t_lo; t < t_hi && ok; ++t) ok = qk(t, s0);
+      }
+      for (int32_t j = 0; j < nkv && ok; ++j) {
+        const uint32_t c = kv_no + j;
+        const int s = c % kStages;
+        if (j + 1 < nkv) {
+          const int sn = (c + 1) % kStages;
+          if (!warp_wait(smem_u32(&S.k_full[sn]), ((c + 1) / kStages) & 1, abort_flag, p.status,
+                         kSiteMma)) {
+            ok = false;
+            break;
+          }
+          for (int t = t_lo; t < t_hi && ok; ++t) ok = qk(t, sn);
+          if (!ok) break;
+        }
+        if (!warp_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
                        kSiteMma)) {
           ok = false;
           break;
         }
-        const Item it = S.items[slot];
-        mbar_arrive(smem_u32(&S.item_empty[slot]));
-        if (it.seq < 0) break;
-        const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-        const int32_t r0 = it.pair * kPairRows;
-        const int ntiles = (len - r0 > kRows) ? 2 : 1;
-        const int32_t nkv = (len + kRows - 1) / kRows;
-        if (!mbar_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) {
-          ok = false;
-          break;
-        }
-        {
-          const int s0 = kv_no % kStages;
-          if (!mbar_wait(smem_u32(&S.k_full[s0]), (kv_no / kStages) & 1, abort_flag, p.status,
-                         kSiteMma)) {
+        for (int t = t_lo; t < t_hi; ++t) {
+          if (!warp_wait(smem_u32(&S.p_full[t]), n_pv[t] & 1, abort_flag, p.status, kSiteMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          for (int t = 0; t < ntiles; ++t) {
-            issue_qk(t, s0);
-            tc_commit(smem_u32(&S.s_full[t]));
-          }
+          issue_pv(t, s, j > 0);
+          tc_commit_warp(smem_u32(&S.pv_done[t]));
+          if (j + 1 == nkv) tc_commit_warp(smem_u32(&S.o_full[t]));
+          ++n_pv[t];
         }
-        for (int32_t j = 0; j < nkv && ok; ++j) {
-          const uint32_t c = kv_no + j;
-          const int s = c % kStages;
-          if (!mbar_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
-                         kSiteMma)) {
-            ok = false;
-            break;
-          }
-          const bool has_next = j + 1 < nkv;
-          const int sn = (c + 1) % kStages;
-          if (has_next && !mbar_wait(smem_u32(&S.k_full[sn]), ((c + 1) / kStages) & 1,
-                                     abort_flag, p.status, kSiteMma)) {
-            ok = false;
-            break;
-          }
-          for (int t = 0; t < ntiles; ++t) {
-            if (!mbar_wait(smem_u32(&S.p_full[t]), p_cnt[t] & 1, abort_flag, p.status,
-                           kSiteMma)) {
-              ok = false;
-              break;
-            }
-            ++p_cnt[t];
-            tc_fence_after();
-            issue_pv(t, s, j > 0);
-            if (has_next) {
-              issue_qk(t, sn);
-              tc_commit(smem_u32(&S.s_full[t]));
-            } else {
-              tc_commit(smem_u32(&S.o_full[t]));
-            }
-          }
-          if (ok) tc_commit(smem_u32(&S.kv_empty[s]));
-        }
-        kv_no += nkv;
-        if (ok) tc_commit(smem_u32(&S.q_empty));
+        if (!ok) break;
+        for (int r = 0; r < releases; ++r) tc_commit_warp(smem_u32(&S.kv_empty[s]));
       }
-      // Every MMA this thread issued must finish before tensor memory is freed.
-      tc_commit(smem_u32(&S.drain));
-      mbar_drain_wait(smem_u32(&S.drain), 0);
+      kv_no += nkv;
+      if (ok)
+        for (int r = 0; r < releases; ++r) tc_commit_warp(smem_u32(&S.q_empty));
     }
+    // Every MMA this warp issued must finish before tensor memory is freed.
+    tc_commit_warp(smem_u32(&S.drain[my_tile]));
+    mbar_drain_wait(smem_u32(&S.drain[my_tile]), 0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;               // query tile of this warpgroup
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;         // query row within the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t s_cnt = 0, o_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;               // S blocks and items consumed by this tile
     const float scale_log2 = p.scale_log2;
     for (uint32_t item_no = 0;; ++item_no) {
       const int slot = item_no & 1;
@@ -341,6 +353,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + col_s(t) + 32 * c, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+        // S_t is in registers: the next block's scores may overwrite it.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.s_free[t]));
         const int32_t kv_valid = len - j * kRows;  // > 0; columns at or past it are masked
         if (kv_valid < kRows) {                    // only a sequence's last key block
 #pragma unroll
@@ -366,6 +382,15 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool grow = m_blk > m + 8.f;
         const float m_new = grow ? m_blk : m;
         const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first block
+        if (j > 0) {
+          // P_t(j-1) V must have finished before P_t is overwritten or O_t rescaled.
+          if (!warp_wait(smem_u32(&S.pv_done[t]), (s_cnt - 2) & 1, abort_flag, p.status,
+                         kSiteSoftmax)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
         const uint64_t c2 = f2(scale_log2, scale_log2), nm2 = f2(-m_new, -m_new);
         uint64_t acc[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -391,7 +416,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         f2_split(acc[3], s6, s7);
         l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
         m = m_new;
-        // O already holds P(j-1) V(j-1): rescale it when some row's maximum moved.
+        // O holds P(j-1) V(j-1): rescale it when some row's maximum moved.
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {

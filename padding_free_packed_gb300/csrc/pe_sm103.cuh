@@ -147,6 +147,44 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Warp-collective forms: every lane of the warp executes them with the same
+// (warp-uniform) operands and one lane, chosen by elect.sync, issues the
+// instruction. A single thread issues one tcgen05.mma per ~130 cycles at best,
+// so kernels spread MMA issue over several warps.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 r;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "elect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
+}
+
+// A wait taken by all 32 lanes of a warp that succeeds only if it succeeds in
+// every lane, so warp-collective operations after it never run on a partial warp.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          DeviceStatus* status, int where) {
+  const bool ok = mbar_wait(bar, parity, abort_flag, status, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Shared-memory matrix descriptor for a tile written by TMA with 128-byte
 // swizzling (rows of 128 bytes, 8-row swizzle atoms of 1024 bytes).
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
