@@ -407,7 +407,7 @@ def main():
                     help="keep only the first K sequences of the workload (profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=24576,
+    ap.add_argument("--cpu-rows", type=int, default=98304,
                     help="query rows in the cpu_baseline sample (about 10-30 s of CPU work)")
     ap.add_argument("--ref-rows", type=int, default=2048,
                     help="query rows per reference-arm step")
