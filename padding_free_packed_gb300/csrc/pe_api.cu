@@ -170,6 +170,11 @@ extern "C" pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t B, int64_t 
   if (B == 0) return PE_OK;
   TilePlan plan = plan_view(workspace, B);
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
+  if (dtype == PE_BF16 && D == 64 && !query_is_first_token) {
+    PE_TRY(bwd_preprocess(dtype, D, out, dout, N, H, delta, stream));
+    return bwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, lse, dout, delta, dq, dk, dv, plan,
+                     static_cast<DeviceStatus*>(workspace), stream);
+  }
   return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, out, lse,
                   dout, dq, dk, dv, delta, plan, stream);
 }
@@ -178,7 +183,9 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
                                           int backward) {
   if ((dtype != PE_BF16 && dtype != PE_FP32) || D < 8 || D % 8 != 0 || D > kMaxHeadDim)
     return "unsupported";
-  if (backward) return "simt_ffma_bwd";
+  if (backward)
+    return (dtype == PE_BF16 && D == 64 && !query_is_first_token) ? "tcgen05_bf16_d64_bwd"
+                                                                   : "simt_ffma_bwd";
   if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
   if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64";
   return "simt_ffma";

@@ -381,6 +381,20 @@ pe_status dispatch_bwd(int D, BwdArgs a, const void* out, float* delta, TilePlan
 
 }  // namespace
 
+pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dout, int64_t Nq,
+                         int32_t H, float* delta, cudaStream_t stream) {
+  int64_t blocks = ceil_div(Nq * H, 8);
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks <= 0) return PE_OK;
+  if (dtype != PE_BF16 || D != 64) return PE_ERR_UNSUPPORTED;
+  bwd_preprocess_kernel<__nv_bfloat16, 64><<<(unsigned)blocks, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), Nq, H,
+      delta);
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
 pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,
                    int first_token, const void* out, const float* lse, const void* dout,

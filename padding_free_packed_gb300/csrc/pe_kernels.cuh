@@ -31,4 +31,15 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     int32_t H, int64_t N, float scale, void* out, float* lse, TilePlan plan,
                     DeviceStatus* status, cudaStream_t stream);
 
+// Delta[h, r] = dO_r . O_r (bf16, head_dim 64) into [H, Nq] fp32.
+pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dout, int64_t Nq,
+                         int32_t H, float* delta, cudaStream_t stream);
+
+// Tensor-core backward, bf16, head_dim 64, full mode (sm_103a): a key pass
+// (dK, dV) and a query pass (dQ), each with its own tile plan over 128-row blocks.
+pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
+                    int32_t H, int64_t N, float scale, const float* lse, const void* dout,
+                    const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
+                    DeviceStatus* status, cudaStream_t stream);
+
 }  // namespace pe
