@@ -116,7 +116,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(smem_u32(&S.s_full[i]), 1);
       mbar_init(smem_u32(&S.s_free[i]), 4);
       mbar_init(smem_u32(&S.pv_done[i]), 1);
-      mbar_init(smem_u32(&S.p_full[i]), 128);
+      mbar_init(smem_u32(&S.p_full[i]), 4);
       mbar_init(smem_u32(&S.o_full[i]), 1);
     }
     mbar_init(smem_u32(&S.q_full), 1);
@@ -382,20 +382,13 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool grow = m_blk > m + 8.f;
         const float m_new = grow ? m_blk : m;
         const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first block
-        if (j > 0) {
-          // P_t(j-1) V must have finished before P_t is overwritten or O_t rescaled.
-          if (!warp_wait(smem_u32(&S.pv_done[t]), (s_cnt - 2) & 1, abort_flag, p.status,
-                         kSiteSoftmax)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
+        // Exponents first, into registers: the wait for P_t(j-1) V below then
+        // hides behind this work instead of delaying it.
         const uint64_t c2 = f2(scale_log2, scale_log2), nm2 = f2(-m_new, -m_new);
         uint64_t acc[4] = {0, 0, 0, 0};
+        uint32_t pk[4][16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const uint64_t x = ffma2(f2(__uint_as_float(sr[c][2 * e]),
@@ -405,9 +398,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             p0 = ex2(p0);
             p1 = ex2(p1);
             acc[e & 3] = fadd2(acc[e & 3], f2(p0, p1));
-            pk[e] = pack_bf16x2(p0, p1);
+            pk[c][e] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(lane_base + col_p(t) + 16 * c, pk);
         }
         float s0, s1, s2, s3, s4, s5, s6, s7;
         f2_split(acc[0], s0, s1);
@@ -416,6 +408,17 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         f2_split(acc[3], s6, s7);
         l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
         m = m_new;
+        if (j > 0) {
+          // P_t(j-1) V must have finished before P_t is overwritten or O_t rescaled.
+          if (!warp_wait(smem_u32(&S.pv_done[t]), (s_cnt - 2) & 1, abort_flag, p.status,
+                         kSiteSoftmax)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(lane_base + col_p(t) + 16 * c, pk[c]);
         // O holds P(j-1) V(j-1): rescale it when some row's maximum moved.
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
@@ -430,7 +433,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&S.p_full[t]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.p_full[t]));
       }
       if (!ok) break;
       if (!warp_wait(smem_u32(&S.o_full[t]), o_cnt & 1, abort_flag, p.status, kSiteSoftmax))
