@@ -132,7 +132,10 @@ pe_status pe_scatter_padded(const void* packed, const int32_t* cu_seqlens, int32
  * All tensor pointers 16-byte aligned.
  * workspace: device, >= pe_attention_workspace_size(...) bytes. Its first 4
  *   bytes receive a device-side status (PE_OK or PE_ERR_DEVICE_TIMEOUT),
- *   readable with pe_read_device_status after the call.
+ *   readable with pe_read_device_status after the call. In first-token mode
+ *   with max_seq_len > 1024 the reported size includes room to split each
+ *   sequence's keys over several CTAs; a workspace without that room (but
+ *   large enough otherwise) is accepted and runs one CTA per sequence and head.
  * ------------------------------------------------------------------------ */
 size_t pe_attention_workspace_size(pe_dtype dtype, int32_t num_sequences, int64_t num_tokens,
                                    int32_t num_heads, int32_t head_dim, int32_t max_seq_len,

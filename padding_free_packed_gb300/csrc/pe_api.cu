@@ -45,6 +45,10 @@ namespace {
 
 inline size_t round16(size_t x) { return (x + 15) / 16 * 16; }
 
+// Bytes a call requires. First-token forwards may also use
+// first_token_partial_bytes() more (reported by pe_attention_workspace_size)
+// to split long sequences over several CTAs; without them they run one CTA
+// per (sequence, head).
 size_t attention_ws_bytes(int32_t B, int64_t N, int32_t H, int query_is_first_token,
                           int backward) {
   size_t bytes = plan_bytes(B);
@@ -103,10 +107,12 @@ extern "C" const char* pe_status_string(int status) {
 extern "C" int pe_abi_version(void) { return 1; }
 
 extern "C" size_t pe_attention_workspace_size(pe_dtype /*dtype*/, int32_t B, int64_t N,
-                                              int32_t H, int32_t /*D*/, int32_t /*S*/,
+                                              int32_t H, int32_t D, int32_t S,
                                               int query_is_first_token, int backward) {
-  if (B < 0 || N < 0 || H < 1) return 0;
-  return attention_ws_bytes(B, N, H, query_is_first_token, backward);
+  if (B < 0 || N < 0 || H < 1 || D < 0 || S < 1) return 0;
+  size_t bytes = attention_ws_bytes(B, N, H, query_is_first_token, backward);
+  if (query_is_first_token && !backward) bytes += first_token_partial_bytes(B, H, D, S);
+  return bytes;
 }
 
 extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
@@ -130,8 +136,17 @@ extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t 
   if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
   PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (B == 0) return PE_OK;
-  if (query_is_first_token)
-    return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, scale, out, lse, stream);
+  if (query_is_first_token) {
+    // Split sequences over key chunks when they are long on average (more
+    // than two chunks) and the workspace has room for the chunk partials.
+    const size_t part_bytes = first_token_partial_bytes(B, H, D, S);
+    float* part = nullptr;
+    if (part_bytes > 0 && N > 2LL * kFirstTokenChunk * B &&
+        workspace_bytes >= plan_bytes(B) + part_bytes)
+      part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
+    return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, S, scale, out, lse, part,
+                           plan_view(workspace, B), stream);
+  }
   TilePlan plan = plan_view(workspace, B);
   if (dtype == PE_BF16 && D == 64) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(), S, plan, nullptr,

@@ -115,6 +115,22 @@ pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
                            int32_t rows_per_tile, int32_t max_seq_len, TilePlan plan,
                            DeviceStatus* status, cudaStream_t stream);
 
+// First-token queries split each sequence's keys into chunks of this many keys
+// (one CTA each) when sequences are long (see the forward entry point); chunk
+// partials are merged after.
+constexpr int32_t kFirstTokenChunk = 1024;
+inline int32_t first_token_splits(int32_t max_seq_len) {
+  return max_seq_len <= kFirstTokenChunk
+             ? 1
+             : static_cast<int32_t>((max_seq_len + kFirstTokenChunk - 1) / kFirstTokenChunk);
+}
+// Bytes of chunk partials (m, l, o[D] per chunk) of a first-token call.
+inline size_t first_token_partial_bytes(int32_t B, int32_t H, int32_t D, int32_t max_seq_len) {
+  const int32_t ns = first_token_splits(max_seq_len);
+  if (ns == 1) return 0;
+  return ((size_t)B * H * ns * (D + 2) * sizeof(float) + 15) / 16 * 16;
+}
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 // True if the current device is compute capability 10.3.

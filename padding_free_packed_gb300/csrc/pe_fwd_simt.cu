@@ -244,11 +244,17 @@ __device__ __forceinline__ void load_slice(const T* __restrict__ p, float (&x)[E
   }
 }
 
+// One CTA per (sequence, head, chunk of `chunk` keys), grid-stride. With one
+// chunk per sequence (nsplit == 1) it writes the output and lse directly;
+// otherwise it writes the chunk's unnormalised partial state (m, l, o[D]) to
+// `part` ([B][H][nsplit]), and first_token_merge_kernel combines the chunks
+// in chunk order. Chunks past a sequence's end leave an empty state (l = 0).
 template <typename T, int D>
 __global__ void __launch_bounds__(kFtThreads)
 fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                        const int32_t* __restrict__ cu, int32_t B, int32_t H, float scale_log2,
-                       T* __restrict__ out, float* __restrict__ lse) {
+                       T* __restrict__ out, float* __restrict__ lse, int32_t nsplit,
+                       int32_t chunk, float* __restrict__ part) {
   using S = FtShape<T, D>;
   constexpr int EPL = S::kEPL, LPK = S::kLPK, G = S::kGroups;
   constexpr int kWarps = kFtThreads / 32;
@@ -258,9 +264,15 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
   const int group = lane / LPK, sub = lane % LPK;
   const int64_t row_stride = (int64_t)H * D;
 
-  for (int64_t item = blockIdx.x; item < (int64_t)B * H; item += gridDim.x) {
-    const int32_t i = (int32_t)(item / H), h = (int32_t)(item - (int64_t)i * H);
-    const int32_t start = __ldg(cu + i), len = __ldg(cu + i + 1) - start;
+  const int64_t items = (int64_t)B * H * nsplit;
+  for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    const int64_t ih = item / nsplit;
+    const int32_t split = (int32_t)(item - ih * nsplit);
+    const int32_t i = (int32_t)(ih / H), h = (int32_t)(ih - (int64_t)i * H);
+    const int32_t seq_start = __ldg(cu + i), seq_len = __ldg(cu + i + 1) - seq_start;
+    const int32_t key0 = split * chunk;
+    const int32_t start = seq_start + key0;
+    const int32_t len = max(0, min(chunk, seq_len - key0));  // keys of this chunk
     float qv[EPL];
     load_slice<T, EPL>(q + ((int64_t)i * H + h) * D + sub * EPL, qv);
 #pragma unroll
@@ -327,10 +339,50 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
         gl += s_l[s2] * w;
         go += s_o[s2][c] * w;
       }
-      out[((int64_t)i * H + h) * D + c] = from_f32<T>(go / gl);
-      if (lse && c == 0) lse[(int64_t)h * B + i] = (gm + __log2f(gl)) * kLn2;
+      if (nsplit == 1) {
+        out[((int64_t)i * H + h) * D + c] = from_f32<T>(go / gl);
+        if (lse && c == 0) lse[(int64_t)h * B + i] = (gm + __log2f(gl)) * kLn2;
+      } else {
+        float* dst = part + item * (D + 2);
+        dst[2 + c] = go;
+        if (c == 0) {
+          dst[0] = gm;  // -inf, with l = 0, for a chunk past the sequence end
+          dst[1] = gl;
+        }
+      }
     }
     __syncthreads();
+  }
+}
+
+// Combines the chunk partials of each (sequence, head), one warp each, in
+// chunk order: m = max m_s, l = sum l_s 2^(m_s - m), o = sum o_s 2^(m_s - m) / l.
+template <typename T, int D>
+__global__ void first_token_merge_kernel(const float* __restrict__ part, int32_t B, int32_t H,
+                                         int32_t nsplit, T* __restrict__ out,
+                                         float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t ih = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       ih < (int64_t)B * H; ih += warps) {
+    const float* base = part + ih * nsplit * (D + 2);
+    float gm = -INFINITY;
+    for (int32_t s2 = 0; s2 < nsplit; ++s2) gm = fmaxf(gm, base[(int64_t)s2 * (D + 2)]);
+    float gl = 0.f;
+    for (int32_t s2 = 0; s2 < nsplit; ++s2) {
+      const float* ps = base + (int64_t)s2 * (D + 2);
+      if (ps[1] > 0.f) gl += ps[1] * ex2(ps[0] - gm);
+    }
+    const int32_t i = (int32_t)(ih / H), h = (int32_t)(ih - (int64_t)i * H);
+    for (int c = lane; c < D; c += 32) {
+      float go = 0.f;
+      for (int32_t s2 = 0; s2 < nsplit; ++s2) {
+        const float* ps = base + (int64_t)s2 * (D + 2);
+        if (ps[1] > 0.f) go += ps[2 + c] * ex2(ps[0] - gm);
+      }
+      out[((int64_t)i * H + h) * D + c] = from_f32<T>(go / gl);
+    }
+    if (lse && lane == 0) lse[(int64_t)h * B + i] = (gm + __log2f(gl)) * kLn2;
   }
 }
 
@@ -353,14 +405,25 @@ pe_status launch_full(const void* q, const void* k, const void* v, const int32_t
 
 template <typename T, int D>
 pe_status launch_first(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                       int32_t H, float scale, void* out, float* lse, cudaStream_t stream) {
-  int64_t blocks = (int64_t)B * H;
+                       int32_t H, int32_t S, float scale, void* out, float* lse, float* part,
+                       cudaStream_t stream) {
+  // Without room for chunk partials every sequence is a single chunk.
+  const int32_t nsplit = part ? first_token_splits(S) : 1;
   const int64_t cap = (int64_t)device_sm_count() * 16;
+  int64_t blocks = (int64_t)B * H * nsplit;
   if (blocks > cap) blocks = cap;
   fwd_first_token_kernel<T, D><<<(unsigned)blocks, kFtThreads, 0, stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, H,
-      scale * kLog2e, static_cast<T*>(out), lse);
+      scale * kLog2e, static_cast<T*>(out), lse, nsplit, nsplit == 1 ? S : kFirstTokenChunk,
+      part);
   PE_CUDA_TRY(cudaGetLastError());
+  if (nsplit > 1) {
+    int64_t mblocks = ceil_div((int64_t)B * H, 8);
+    if (mblocks > cap) mblocks = cap;
+    first_token_merge_kernel<T, D><<<(unsigned)mblocks, 256, 0, stream>>>(
+        part, B, H, nsplit, static_cast<T*>(out), lse);
+    PE_CUDA_TRY(cudaGetLastError());
+  }
   return PE_OK;
 }
 
@@ -381,10 +444,11 @@ pe_status dispatch_full(int D, const void* q, const void* k, const void* v, cons
 
 template <typename T>
 pe_status dispatch_first(int D, const void* q, const void* k, const void* v, const int32_t* cu,
-                         int32_t B, int32_t H, float scale, void* out, float* lse,
-                         cudaStream_t stream) {
+                         int32_t B, int32_t H, int32_t S, float scale, void* out, float* lse,
+                         float* part, cudaStream_t stream) {
   switch (D) {
-#define PE_CASE(d) case d: return launch_first<T, d>(q, k, v, cu, B, H, scale, out, lse, stream);
+#define PE_CASE(d) \
+  case d: return launch_first<T, d>(q, k, v, cu, B, H, S, scale, out, lse, part, stream);
     PE_CASE(8) PE_CASE(16) PE_CASE(32) PE_CASE(64) PE_CASE(128)
 #undef PE_CASE
     default: return PE_ERR_UNSUPPORTED;
@@ -406,11 +470,12 @@ pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
 bool first_token_supported(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D == 128; }
 
 pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
-                          const int32_t* cu, int32_t B, int32_t H, float scale, void* out,
-                          float* lse, cudaStream_t stream) {
+                          const int32_t* cu, int32_t B, int32_t H, int32_t S, float scale,
+                          void* out, float* lse, float* part, TilePlan /*plan*/,
+                          cudaStream_t stream) {
   if (dtype == PE_FP32)
-    return dispatch_first<float>(D, q, k, v, cu, B, H, scale, out, lse, stream);
-  return dispatch_first<__nv_bfloat16>(D, q, k, v, cu, B, H, scale, out, lse, stream);
+    return dispatch_first<float>(D, q, k, v, cu, B, H, S, scale, out, lse, part, stream);
+  return dispatch_first<__nv_bfloat16>(D, q, k, v, cu, B, H, S, scale, out, lse, part, stream);
 }
 
 }  // namespace pe

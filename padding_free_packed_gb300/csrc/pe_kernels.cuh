@@ -14,8 +14,9 @@ pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
 // First-token query (one query row per sequence).
 bool first_token_supported(int D);
 pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
-                          const int32_t* cu, int32_t B, int32_t H, float scale, void* out,
-                          float* lse, cudaStream_t stream);
+                          const int32_t* cu, int32_t B, int32_t H, int32_t S, float scale,
+                          void* out, float* lse, float* part, TilePlan plan,
+                          cudaStream_t stream);
 
 // CUDA-core backward; delta is [H, Nq] fp32 scratch.
 pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,

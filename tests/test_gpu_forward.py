@@ -210,3 +210,33 @@ def test_many_work_items_per_cta():
     out, _ = pe.pe_packed_attention_fwd(q, k, v, cu_d, s, 0.125)
     ref, _ = oracle.attention_fwd(x.q, x.k, x.v, cu, s, 0.125)
     check(out, ref, "bf16", "many items")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_first_token_split_over_key_chunks(dtype):
+    """Sequences longer than one 1024-key chunk are split across CTAs and the
+    chunk partials merged; lengths straddle the chunk edges, and max_seq_len
+    leaves whole chunks past the end of most sequences."""
+    lengths = [1, 1023, 1024, 1025, 3000, 2048, 4100, 4500, 3900, 4999]  # mean > 2 chunks
+    x = workloads.make_custom(lengths, 3, 64, dtype, seed=34)
+    s = 5000
+    cu, cu_d, q, k, v = _device_inputs(x)
+    first = torch.from_numpy(cu[:-1].astype(np.int64)).to(DEV)
+    out, lse = pe.pe_packed_attention_fwd(q[first].contiguous(), k, v, cu_d, s, 0.125,
+                                          query_is_first_token=True, need_lse=True)
+    rows = cu[:-1].astype(np.int64).repeat(3)
+    heads = np.tile(np.arange(3), len(lengths))
+    ref, ref_lse = oracle.attention_fwd_rows(x.q, x.k, x.v, cu, 0.125, False, rows, heads)
+    tag = "fp32" if dtype == torch.float32 else "bf16"
+    got = out[torch.arange(len(lengths)).repeat_interleave(3), torch.from_numpy(heads).to(DEV)]
+    check(got, ref, tag, "first-token split")
+    got_lse = lse[torch.from_numpy(heads).to(DEV), torch.arange(len(lengths)).repeat_interleave(3).to(DEV)]
+    assert float(np.abs(to64(got_lse) - ref_lse).max()) <= _lse_tol(tag)
+    # With only the base workspace (no room for chunk partials) the call runs
+    # one CTA per (sequence, head) and gives the same answer.
+    small = torch.empty(pe.attention_workspace_bytes(dtype, len(lengths), q.shape[0], 3, 64, s),
+                        dtype=torch.uint8, device=DEV)
+    out2, _ = pe.pe_packed_attention_fwd(q[first].contiguous(), k, v, cu_d, s, 0.125,
+                                         query_is_first_token=True, workspace=small)
+    check(out2[torch.arange(len(lengths)).repeat_interleave(3), torch.from_numpy(heads).to(DEV)],
+          ref, tag, "first-token single pass")
