@@ -159,23 +159,40 @@ def run_ours(args, rank, world):
     wl = workloads.WORKLOADS[args.workload]
     # Weak scaling: every rank draws its own batch of the same workload.
     train = wl.backward
-    drawn = workloads.make_padded_inputs(args.workload, seed=args.seed + rank,
-                                         max_sequences=args.sequences, with_dout=train)
-    lengths, gq, gk, gv = drawn[:4]
-    gdo = drawn[4] if train else None
+    if args.packed:
+        # Already-packed inputs (a pipeline that collates without padding):
+        # the step is the attention forward (and backward) alone.
+        lengths = workloads.draw_lengths(args.workload, np.random.default_rng(args.seed + rank))
+        if args.sequences:
+            lengths = np.ascontiguousarray(lengths[: args.sequences])
+        xin = workloads.make_custom(lengths, wl.num_heads, wl.head_dim, wl.torch_dtype,
+                                    seed=args.seed + rank, with_dout=train)
+        host_grids = [xin.q, xin.k, xin.v] + ([xin.dout] if train else [])
+    else:
+        drawn = workloads.make_padded_inputs(args.workload, seed=args.seed + rank,
+                                             max_sequences=args.sequences, with_dout=train)
+        lengths = drawn[0]
+        host_grids = list(drawn[1:])
+    gq = host_grids[0]
     s, h, d = wl.max_seq_len, wl.num_heads, wl.head_dim
     n_tokens = int(lengths.astype(np.int64).sum())
-    fwd_flops = real_flops(lengths, h, d)
+    if args.first_token:
+        if not args.packed:
+            raise SystemExit("--first-token needs --packed")
+        train = False
+    fwd_flops = real_flops(lengths, h, d, first_token=args.first_token)
     bwd_flops = 2.5 * fwd_flops if train else 0.0   # 10 sum L^2 H d: five GEMM-shaped products
     flops = fwd_flops + bwd_flops
-    kernel = pe.pe_attention_kernel(wl.torch_dtype, d)
+    kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token)
     bwd_kernel = pe.pe_attention_kernel(wl.torch_dtype, d, backward=True) if train else None
 
     lengths_d = torch.from_numpy(lengths).to(dev)
-    qg, kg, vg = gq.to(dev), gk.to(dev), gv.to(dev)
-    dog = gdo.to(dev) if train else None
-    og = torch.empty_like(qg)
-    grad_grids = [torch.empty_like(qg) for _ in range(3)] if train else None
+    dev_grids = [t.to(dev) for t in host_grids]
+    og = torch.empty_like(dev_grids[0])
+    grad_grids = [torch.empty_like(dev_grids[0]) for _ in range(3)] if train else None
+    packed_cu = pe.pe_pack_sequences(lengths_d, s)[1] if args.packed else None
+    q_first = (dev_grids[0][packed_cu[:-1].long()].contiguous()
+               if args.packed and args.first_token else None)
     stream = torch.cuda.current_stream(dev)
     fwd_events, bwd_events = [], []
 
@@ -189,27 +206,43 @@ def run_ours(args, rank, world):
         events.append((e0, e1))
         return result
 
-    def step(lengths_t, q_grid, k_grid, v_grid, out_grid, record, do_grid=None):
-        flat, cu, n = pe.pe_pack_sequences(lengths_t, s)
-        q = pe.pe_gather_packed(q_grid, flat, n)
-        k = pe.pe_gather_packed(k_grid, flat, n)
-        v = pe.pe_gather_packed(v_grid, flat, n)
+    def step(lengths_t, grids, record):
+        if args.packed:
+            cu = packed_cu
+            q, k, v = grids[:3]
+            if args.first_token:
+                out, _ = timed(record, fwd_events, lambda: pe.pe_packed_attention_fwd(
+                    q_first, k, v, cu, s, wl.scale, query_is_first_token=True))
+                return n_tokens
+        else:
+            flat, cu, n = pe.pe_pack_sequences(lengths_t, s)
+            q, k, v = (pe.pe_gather_packed(g, flat, n) for g in grids[:3])
         out, lse = timed(record, fwd_events,
                          lambda: pe.pe_packed_attention_fwd(q, k, v, cu, s, wl.scale,
                                                             need_lse=train))
-        pe.pe_scatter_padded(out, cu, s, out=out_grid)
+        if args.packed:
+            og.copy_(out)
+        else:
+            pe.pe_scatter_padded(out, cu, s, out=og)
         if train:
-            do = pe.pe_gather_packed(do_grid, flat, n)
+            do = grids[3] if args.packed else pe.pe_gather_packed(grids[3], flat, n)
             grads = timed(record, bwd_events,
                           lambda: pe.pe_packed_attention_bwd(do, q, k, v, out, lse, cu, s,
                                                              wl.scale))
             for g, grid in zip(grads, grad_grids):
-                pe.pe_scatter_padded(g, cu, s, out=grid)
-        return n
+                if args.packed:
+                    grid.copy_(g)
+                else:
+                    pe.pe_scatter_padded(g, cu, s, out=grid)
+        return n_tokens
 
-    # pack scan+fill, 3 gathers, plan+attention, scatter; training adds the dO
-    # gather, the backward (delta, plan, key pass, plan, query pass) and 3 scatters.
-    launches_per_step = 2 + 3 + 2 + 1 + ((1 + 5 + 3) if train else 0)
+    # Padded steps: pack scan+fill, 3 gathers, plan+attention, scatter; training
+    # adds the dO gather, the backward (delta, plan, key pass, plan, query pass)
+    # and 3 scatters. Packed steps: plan+attention (+ the 5 backward launches).
+    if args.packed:
+        launches_per_step = 2 + (5 if train else 0)
+    else:
+        launches_per_step = 2 + 3 + 2 + 1 + ((1 + 5 + 3) if train else 0)
 
     def barrier():
         if world > 1:
@@ -217,13 +250,13 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize(dev)
 
     for _ in range(args.warmup):
-        step(lengths_d, qg, kg, vg, og, False, dog)
+        step(lengths_d, dev_grids, False)
     barrier()
     with ClockSampler(local_rank) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for _ in range(args.steps):
-            step(lengths_d, qg, kg, vg, og, True, dog)
+            step(lengths_d, dev_grids, True)
         end.record(stream)
         barrier()
     elapsed_ms = start.elapsed_time(end)
@@ -239,18 +272,18 @@ def run_ours(args, rank, world):
     # output back to pinned host memory, copies inside the timed region.
     e2e = None
     if not args.no_e2e:
-        host_in = [t.pin_memory() for t in ((gq, gk, gv, gdo) if train else (gq, gk, gv))]
+        host_in = [t.pin_memory() for t in host_grids]
         hlen = torch.from_numpy(lengths).pin_memory()
         dev_in = [torch.empty_like(t, device=dev) for t in host_in]
         dlen = torch.empty_like(lengths_d)
         results = [og] + (grad_grids if train else [])
-        host_out = [torch.empty_like(gq).pin_memory() for _ in results]
+        host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in results]
 
         def e2e_step():
             dlen.copy_(hlen, non_blocking=True)
             for dst, src in zip(dev_in, host_in):
                 dst.copy_(src, non_blocking=True)
-            step(dlen, *dev_in[:3], og, False, dev_in[3] if train else None)
+            step(dlen, dev_in, False)
             for dst, src in zip(host_out, results):
                 dst.copy_(src, non_blocking=True)
 
@@ -292,7 +325,13 @@ def run_ours(args, rank, world):
                 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12)
         bound, peak, unit = "alu", ffma, "TFLOP/s"
         peak_note = "FFMA: SMs x 128 lanes x 2 flop x max SM clock"
-    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    if bound == "hbm":
+        # k and v read once, q read and the output written once per sequence and head.
+        esize = 4 if wl.dtype == "fp32" else 2
+        hbm_bytes = (2 * n_tokens + 2 * len(lengths)) * h * d * esize
+        achieved = hbm_bytes / (dom_ms * 1e-3) / 1e9
+    else:
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     traffic = committed_traffic(dom_kernel, KERNEL_SOURCES.get(dom_kernel, ""))
     value = world * flops / (ms_per_step * 1e-3) / 1e12
     line = {
@@ -303,12 +342,18 @@ def run_ours(args, rank, world):
                    "description": wl.description,
                    "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
                    "heads": h, "head_dim": d, "max_seq_len": s,
-                   "step": ("pack + gather q,k,v,dO + tile plan + attention forward + scatter "
-                            "+ attention backward + scatter dq,dk,dv" if train else
-                            "pack + gather q,k,v + tile plan + attention forward + scatter"),
+                   "step": (("tile plan + attention forward + backward on packed inputs"
+                             if train else "tile plan + attention forward on packed inputs")
+                            if args.packed else
+                            ("pack + gather q,k,v,dO + tile plan + attention forward + scatter "
+                             "+ attention backward + scatter dq,dk,dv" if train else
+                             "pack + gather q,k,v + tile plan + attention forward + scatter")),
                    "flops_per_step": flops,
-                   "l2": (f"inputs larger than L2 ({len(drawn) - 1} padded grids of "
-                          f"{gq.numel() * gq.element_size() / 1e9:.2f} GB); no flush"),
+                   "l2": (f"{len(host_grids)} {'packed buffers' if args.packed else 'padded grids'}"
+                          f" of {gq.numel() * gq.element_size() / 1e9:.2f} GB"
+                          + ("; larger than L2, no flush"
+                             if gq.numel() * gq.element_size() > 129e6 else
+                             "; smaller than L2 (profiling case)")),
                    "parallelism": f"dp{world} (independent batches per GPU, no collective)"},
         "tokens_per_s": world * n_tokens / (ms_per_step * 1e-3),
         "pct_of_tensor_peak": 100.0 * value / world / float(peaks["bf16_tflops"]),
@@ -405,6 +450,10 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--sequences", type=int, default=None,
                     help="keep only the first K sequences of the workload (profiling cases)")
+    ap.add_argument("--packed", action="store_true",
+                    help="inputs already packed: time the attention calls alone")
+    ap.add_argument("--first-token", action="store_true",
+                    help="with --packed: one query per sequence (its first token)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=98304,
