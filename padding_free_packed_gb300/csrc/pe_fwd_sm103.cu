@@ -8,13 +8,16 @@
 //               plan, publishes them to a two-slot ring in shared memory, and
 //               streams Q tiles and K/V blocks of 128 rows x 64 into a
 //               four-stage ring with 128-byte swizzle.
-//   warps 1, 2  MMA issuers, one per query tile (warp 1 also owns tensor
-//               memory): S_t = Q_t K_j^T (M=128, N=128, K=64) into TMEM as soon
-//               as the softmax has read S_t of the previous block, so the next
-//               scores are computed during this block's softmax; then
-//               O_t += P_t V_j (M=128, N=64, K=128) with P_t read from TMEM.
-//               A thread issues at most one MMA per ~130 cycles, so issue is
-//               spread over two warps (whole warps, elect.sync).
+//   warp 1      issues S_t = Q_t K_j^T (M=128, N=128, K=64) for both query
+//               tiles into TMEM as soon as the softmax has read S_t of the
+//               previous block, so the next scores are computed during this
+//               block's softmax (warp 1 also owns tensor memory).
+//   warps 2, 3  issue O_t += P_t V_j (M=128, N=64, K=128) for tile 0 and tile
+//               1, P_t read from TMEM, when P_t(j) arrives.
+//               A thread issues at most one MMA per ~130 cycles whatever its
+//               size, and a block needs 4 QK and 8 PV MMAs per tile, so issue
+//               is spread over three warps (whole warps, elect.sync) that each
+//               commit their own completion barriers.
 //   warps 4-7   softmax for query tile 0; warps 8-11 for query tile 1. Each
 //               thread owns one query row (one TMEM lane): online softmax in
 //               base 2 with fp32 statistics, P written back to TMEM as bf16,
@@ -46,7 +49,7 @@ using namespace sm103;
 constexpr int kRows = 128;                         // query rows per tile = keys per block
 constexpr int kD = 64;                             // head_dim
 constexpr int kStages = 4;                         // K/V ring depth
-constexpr int kIssueWarps = 2;                     // MMA-issuing warps: 1 (both tiles) or 2 (one per tile)
+constexpr int kIssueWarps = 3;                     // QK issuer + one PV issuer per tile
 constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = kRows * kD * 2;    // 16 KiB
 constexpr int kPairRows = 2 * kRows;               // query rows per work item
@@ -67,9 +70,9 @@ struct alignas(1024) Smem {
   __nv_bfloat16 v[kStages][kRows * kD];
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_empty;
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2];
-  uint64_t drain[2];
+  uint64_t drain[kIssueWarps];
   Item items[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -120,14 +123,14 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(smem_u32(&S.o_full[i]), 1);
     }
     mbar_init(smem_u32(&S.q_full), 1);
-    mbar_init(smem_u32(&S.q_empty), kIssueWarps);
+    mbar_init(smem_u32(&S.q_empty), 1);            // the QK issuer, after an item's last QK
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&S.k_full[s]), 1);
       mbar_init(smem_u32(&S.v_full[s]), 1);
-      mbar_init(smem_u32(&S.kv_empty[s]), kIssueWarps);
+      mbar_init(smem_u32(&S.k_empty[s]), 1);       // the QK issuer, after both tiles' QK
+      mbar_init(smem_u32(&S.v_empty[s]), 2);       // each PV issuer (tile 0's twice for a lone tile)
     }
-    mbar_init(smem_u32(&S.drain[0]), 1);
-    mbar_init(smem_u32(&S.drain[1]), 1);
+    for (int w = 0; w < kIssueWarps; ++w) mbar_init(smem_u32(&S.drain[w]), 1);
     S.abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -149,8 +152,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       prefetch_tensormap(&tm_v);
       uint32_t kv_no = 0;
       int pending_q = -1;                // parity of the last Q load not yet known complete
-      int pending_kv[kStages];           // parity of the last K/V load per stage
-      for (int s = 0; s < kStages; ++s) pending_kv[s] = -1;
+      int pending_k[kStages], pending_v[kStages];  // parity of the last K / V load per stage
+      for (int s = 0; s < kStages; ++s) pending_k[s] = pending_v[s] = -1;
       bool ok = true;
       for (uint32_t item_no = 0; ok; ++item_no) {
         const int slot = item_no & 1;
@@ -188,62 +191,38 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
           const int s = kv_no % kStages;
           const uint32_t ph = (kv_no / kStages) & 1;
-          if (!mbar_wait(smem_u32(&S.kv_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+          if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
           tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x, start + j * kRows);
+          pending_k[s] = (int)ph;
+          if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
           tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x, start + j * kRows);
-          pending_kv[s] = (int)ph;
+          pending_v[s] = (int)ph;
         }
       }
       if (!ok) {
         // Let every copy this thread started land before the CTA exits.
         if (pending_q >= 0) mbar_drain_wait(smem_u32(&S.q_full), (uint32_t)pending_q);
-        for (int s = 0; s < kStages; ++s)
-          if (pending_kv[s] >= 0) {
-            mbar_drain_wait(smem_u32(&S.k_full[s]), (uint32_t)pending_kv[s]);
-            mbar_drain_wait(smem_u32(&S.v_full[s]), (uint32_t)pending_kv[s]);
-          }
+        for (int s = 0; s < kStages; ++s) {
+          if (pending_k[s] >= 0) mbar_drain_wait(smem_u32(&S.k_full[s]), (uint32_t)pending_k[s]);
+          if (pending_v[s] >= 0) mbar_drain_wait(smem_u32(&S.v_full[s]), (uint32_t)pending_v[s]);
+        }
       }
     }
-  } else if (warp == 1 || (kIssueWarps == 2 && warp == 2)) {
-    // ------------------------------------------------------------ MMA issuers (whole warps)
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ QK issuer (whole warp)
     // S_t for key block j+1 is computed as soon as the softmax has read S_t(j),
-    // so it overlaps that softmax; P_t V_j follows when P_t(j) arrives.
-    const int my_tile = warp - 1;
+    // so it overlaps that softmax.
     constexpr uint32_t idesc_qk = idesc_bf16(kRows, kRows, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
     uint32_t kv_no = 0;
-    uint32_t n_qk[2] = {0, 0}, n_pv[2] = {0, 0};   // MMAs issued per tile, all items
-    auto issue_qk = [&](int t, int s) {
-      const uint32_t q_addr = smem_u32(S.q[t]), k_addr = smem_u32(S.k[s]);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk)
-        mma_ss_warp(tmem + col_s(t), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
-                    smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-    };
-    auto issue_pv = [&](int t, int s, bool accumulate) {
-      const uint32_t v_addr = smem_u32(S.v[s]);
-#pragma unroll
-      for (int kk = 0; kk < kRows / 16; ++kk)
-        mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
-                    smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
-                    (accumulate || kk > 0) ? 1u : 0u);
-    };
-    // Issues S_t = Q_t K_s^T once the softmax has read the previous S_t.
-    auto qk = [&](int t, int s) -> bool {
-      if (n_qk[t] > 0 &&
-          !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag, p.status, kSiteMma))
-        return false;
-      tc_fence_after();
-      issue_qk(t, s);
-      tc_commit_warp(smem_u32(&S.s_full[t]));
-      ++n_qk[t];
-      return true;
-    };
+    uint32_t n_qk[2] = {0, 0};                     // QK MMA groups issued per tile, all items
     bool ok = true;
     for (uint32_t item_no = 0; ok; ++item_no) {
       const int slot = item_no & 1;
@@ -258,65 +237,93 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t r0 = it.pair * kPairRows;
       const int ntiles = (len - r0 > kRows) ? 2 : 1;
       const int32_t nkv = (len + kRows - 1) / kRows;
-      int t_lo = 0, t_hi = ntiles, releases = 1;
-      if (kIssueWarps == 2) {
-        // One warp per tile; with a single tile, the tile-0 warp also makes
-        // the tile-1 warp's arrivals on the shared K/V and Q release barriers.
-        t_lo = my_tile;
-        t_hi = my_tile < ntiles ? my_tile + 1 : my_tile;
-        releases = (ntiles == 1) ? 2 : 1;
-        if (t_lo == t_hi) {
-          kv_no += nkv;
-          continue;
-        }
-      }
       if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
-      {
-        const int s0 = kv_no % kStages;
-        if (!warp_wait(smem_u32(&S.k_full[s0]), (kv_no / kStages) & 1, abort_flag, p.status,
-                       kSiteMma))
-          break;
-        for (int t = t_lo; t < t_hi && ok; ++t) ok = qk(t, s0);
-      }
       for (int32_t j = 0; j < nkv && ok; ++j) {
         const uint32_t c = kv_no + j;
         const int s = c % kStages;
-        if (j + 1 < nkv) {
-          const int sn = (c + 1) % kStages;
-          if (!warp_wait(smem_u32(&S.k_full[sn]), ((c + 1) / kStages) & 1, abort_flag, p.status,
-                         kSiteMma)) {
-            ok = false;
-            break;
-          }
-          for (int t = t_lo; t < t_hi && ok; ++t) ok = qk(t, sn);
-          if (!ok) break;
-        }
-        if (!warp_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
+        if (!warp_wait(smem_u32(&S.k_full[s]), (c / kStages) & 1, abort_flag, p.status,
                        kSiteMma)) {
           ok = false;
           break;
         }
-        for (int t = t_lo; t < t_hi; ++t) {
-          if (!warp_wait(smem_u32(&S.p_full[t]), n_pv[t] & 1, abort_flag, p.status, kSiteMma)) {
+        const uint32_t k_addr = smem_u32(S.k[s]);
+        for (int t = 0; t < ntiles; ++t) {
+          // The softmax must have read the previous S_t before it is overwritten.
+          if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag,
+                                        p.status, kSiteMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(t, s, j > 0);
-          tc_commit_warp(smem_u32(&S.pv_done[t]));
-          if (j + 1 == nkv) tc_commit_warp(smem_u32(&S.o_full[t]));
-          ++n_pv[t];
+          const uint32_t q_addr = smem_u32(S.q[t]);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss_warp(tmem + col_s(t), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
+                        smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          tc_commit_warp(smem_u32(&S.s_full[t]));
+          ++n_qk[t];
         }
         if (!ok) break;
-        for (int r = 0; r < releases; ++r) tc_commit_warp(smem_u32(&S.kv_empty[s]));
+        tc_commit_warp(smem_u32(&S.k_empty[s]));  // K_j no longer needed by either tile
       }
       kv_no += nkv;
-      if (ok)
-        for (int r = 0; r < releases; ++r) tc_commit_warp(smem_u32(&S.q_empty));
+      if (ok) tc_commit_warp(smem_u32(&S.q_empty));
     }
     // Every MMA this warp issued must finish before tensor memory is freed.
-    tc_commit_warp(smem_u32(&S.drain[my_tile]));
-    mbar_drain_wait(smem_u32(&S.drain[my_tile]), 0);
+    tc_commit_warp(smem_u32(&S.drain[0]));
+    mbar_drain_wait(smem_u32(&S.drain[0]), 0);
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ PV issuers (whole warps)
+    // O_t += P_t V_j as soon as the softmax has written P_t(j).
+    const int t = warp - 2;
+    constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
+    uint32_t kv_no = 0, n_pv = 0;
+    bool ok = true;
+    for (uint32_t item_no = 0; ok; ++item_no) {
+      const int slot = item_no & 1;
+      if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+                     kSiteMma))
+        break;
+      const Item it = S.items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
+      if (it.seq < 0) break;
+      const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
+      const int32_t r0 = it.pair * kPairRows;
+      const int ntiles = (len - r0 > kRows) ? 2 : 1;
+      const int32_t nkv = (len + kRows - 1) / kRows;
+      if (t >= ntiles) {                           // tile 1 of a lone tile: nothing to do
+        kv_no += nkv;
+        continue;
+      }
+      // With a single tile, tile 0's warp also makes tile 1's arrival on the
+      // V release barrier.
+      const int releases = ntiles == 1 ? 2 : 1;
+      for (int32_t j = 0; j < nkv; ++j) {
+        const uint32_t c = kv_no + j;
+        const int s = c % kStages;
+        if (!warp_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
+                       kSiteMma) ||
+            !warp_wait(smem_u32(&S.p_full[t]), n_pv & 1, abort_flag, p.status, kSiteMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(S.v[s]);
+#pragma unroll
+        for (int kk = 0; kk < kRows / 16; ++kk)
+          mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
+                      smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_warp(smem_u32(&S.pv_done[t]));
+        if (j + 1 == nkv) tc_commit_warp(smem_u32(&S.o_full[t]));
+        ++n_pv;
+        for (int r = 0; r < releases; ++r) tc_commit_warp(smem_u32(&S.v_empty[s]));
+      }
+      kv_no += nkv;
+    }
+    tc_commit_warp(smem_u32(&S.drain[1 + t]));
+    mbar_drain_wait(smem_u32(&S.drain[1 + t]), 0);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;               // query tile of this warpgroup
