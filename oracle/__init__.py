@@ -64,6 +64,18 @@ def _load():
         lib.orc_attention_bwd.argtypes = [dp, dp, dp, dp, i32p, i64, i64, i64, ctypes.c_double,
                                           ctypes.c_int, dp, dp, dp, ctypes.c_int]
         lib.orc_attention_bwd.restype = ctypes.c_int
+        lib.orc_attention_fwd_local.argtypes = [dp, dp, dp, i32p, i64, i64, i64, i64,
+                                                ctypes.c_double, ctypes.c_int, i64, i64, dp, dp,
+                                                ctypes.c_int]
+        lib.orc_attention_fwd_local.restype = ctypes.c_int
+        lib.orc_attention_fwd_rows_local.argtypes = [dp, dp, dp, i32p, i64, i64, i64,
+                                                     ctypes.c_double, ctypes.c_int, i64, i64,
+                                                     i64p, i64p, i64, dp, dp, ctypes.c_int]
+        lib.orc_attention_fwd_rows_local.restype = ctypes.c_int
+        lib.orc_attention_bwd_local.argtypes = [dp, dp, dp, dp, i32p, i64, i64, i64,
+                                                ctypes.c_double, ctypes.c_int, i64, i64, dp, dp,
+                                                dp, ctypes.c_int]
+        lib.orc_attention_bwd_local.restype = ctypes.c_int
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = ctypes.c_int
         _lib = lib
@@ -138,8 +150,12 @@ def scatter_rows(packed: np.ndarray, cu_seqlens: np.ndarray, max_seq_len: int) -
 
 
 def attention_fwd(q, k, v, cu_seqlens, max_seq_len: int, scale: float,
-                  first_token: bool = False, threads: int | None = None):
-    """Padded-grid packed attention forward. Returns (o [Nq,H,D], lse [H,Nq]) in fp64."""
+                  first_token: bool = False, threads: int | None = None,
+                  window: tuple[int, int] = (-1, -1)):
+    """Padded-grid packed attention forward. Returns (o [Nq,H,D], lse [H,Nq]) in fp64.
+
+    window = (left, right): the key at position j is visible from the query at
+    position r iff r - left <= j <= r + right; a negative bound is unbounded."""
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
@@ -149,18 +165,20 @@ def attention_fwd(q, k, v, cu_seqlens, max_seq_len: int, scale: float,
     assert q.shape == (nq, h, d), (q.shape, nq, h, d)
     o = np.zeros((nq, h, d), dtype=np.float64)
     lse = np.zeros((h, nq), dtype=np.float64)
-    rc = lib.orc_attention_fwd(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
-                               _ptr(v, ctypes.c_double), _ptr(cu, ctypes.c_int32), b,
-                               int(max_seq_len), h, d, float(scale), int(bool(first_token)),
-                               _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
-                               threads or default_threads())
+    rc = lib.orc_attention_fwd_local(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+                                     _ptr(v, ctypes.c_double), _ptr(cu, ctypes.c_int32), b,
+                                     int(max_seq_len), h, d, float(scale), int(bool(first_token)),
+                                     int(window[0]), int(window[1]),
+                                     _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
+                                     threads or default_threads())
     if rc != 0:
         raise OracleError(rc)
     return o, lse
 
 
 def attention_fwd_rows(q, k, v, cu_seqlens, scale: float, first_token: bool,
-                       rows, heads, threads: int | None = None):
+                       rows, heads, threads: int | None = None,
+                       window: tuple[int, int] = (-1, -1)):
     """Forward for chosen (row, head) pairs. Returns (o [R,D], lse [R]) in fp64."""
     lib = _load()
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -172,9 +190,10 @@ def attention_fwd_rows(q, k, v, cu_seqlens, scale: float, first_token: bool,
     r = int(rows.shape[0])
     o = np.zeros((r, d), dtype=np.float64)
     lse = np.zeros((r,), dtype=np.float64)
-    rc = lib.orc_attention_fwd_rows(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+    rc = lib.orc_attention_fwd_rows_local(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
                                     _ptr(v, ctypes.c_double), _ptr(cu, ctypes.c_int32), b, h, d,
                                     float(scale), int(bool(first_token)),
+                                    int(window[0]), int(window[1]),
                                     _ptr(rows, ctypes.c_int64), _ptr(heads, ctypes.c_int64), r,
                                     _ptr(o, ctypes.c_double), _ptr(lse, ctypes.c_double),
                                     threads or default_threads())
@@ -184,7 +203,7 @@ def attention_fwd_rows(q, k, v, cu_seqlens, scale: float, first_token: bool,
 
 
 def attention_bwd(q, k, v, dout, cu_seqlens, scale: float, first_token: bool = False,
-                  threads: int | None = None):
+                  threads: int | None = None, window: tuple[int, int] = (-1, -1)):
     """Analytic gradients. Returns (dq, dk, dv) in fp64."""
     lib = _load()
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
@@ -194,10 +213,11 @@ def attention_bwd(q, k, v, dout, cu_seqlens, scale: float, first_token: bool = F
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    rc = lib.orc_attention_bwd(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+    rc = lib.orc_attention_bwd_local(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
                                _ptr(v, ctypes.c_double), _ptr(dout, ctypes.c_double),
                                _ptr(cu, ctypes.c_int32), b, h, d, float(scale),
-                               int(bool(first_token)), _ptr(dq, ctypes.c_double),
+                               int(bool(first_token)), int(window[0]), int(window[1]),
+                               _ptr(dq, ctypes.c_double),
                                _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
                                threads or default_threads())
     if rc != 0:

@@ -33,6 +33,14 @@
  *   - log-sum-exp layout: [H, Nq] fp64, natural log, no row padding.
  *   - the backward is the analytic gradient of softmax attention (the pages
  *     hand it to aten's backward kernel, which computes the same gradient).
+ *   - local (sliding-window) attention: the packed-encoders README lists a
+ *     "local-64" mode for ModernBERT geometry and FlashAttention's
+ *     sliding-window pruning without defining them. Read as: the key at
+ *     position j of a sequence is visible from the query at position r of the
+ *     same sequence iff r - window_left <= j <= r + window_right; a negative
+ *     bound is unbounded, so (-1, -1) is full attention and local-64 is
+ *     (64, 64). A first-token query sits at position 0. Invisible keys get a
+ *     score of -inf, i.e. weight exactly zero.
  *
  * Everything is fp64, written as plain loops over the definition, with a
  * pthread pool over (sequence, head) pairs and no blocking or fusion.
@@ -153,6 +161,11 @@ static int orc_run(orc_task_fn fn, void* ctx, int64_t num_items, size_t scratch_
   return atomic_load(&pool.failed) ? ORC_NO_MEMORY : ORC_OK;
 }
 
+/* Local-attention visibility of key position j from query position r. */
+static int orc_visible(int64_t r, int64_t j, int64_t wl, int64_t wr) {
+  return (wl < 0 || j >= r - wl) && (wr < 0 || j <= r + wr);
+}
+
 /* ------------------------------------------------------------------------- */
 /* Forward on the padded grid (_padded_packed_attention).                     */
 /* q: [Nq, H, D] with Nq = N (full) or B (first token). k, v: [N, H, D].      */
@@ -164,6 +177,7 @@ typedef struct {
   int64_t B, S, H, D, Nq;
   double scale;
   int first_token;
+  int64_t wl, wr;
   double *o, *lse;
 } orc_fwd_ctx;
 
@@ -199,7 +213,7 @@ static void orc_fwd_task(void* vctx, int64_t item, double* scratch) {
       if (j >= len) continue; /* padded key: excluded from the softmax */
       double acc = 0.0;
       for (int64_t c2 = 0; c2 < D; ++c2) acc += Qp[r * D + c2] * Kp[j * D + c2];
-      s[j] = c->scale * acc;
+      s[j] = orc_visible(r, j, c->wl, c->wr) ? c->scale * acc : -INFINITY;
       if (s[j] > m) m = s[j];
     }
     double z = 0.0;
@@ -217,17 +231,25 @@ static void orc_fwd_task(void* vctx, int64_t item, double* scratch) {
   }
 }
 
-int orc_attention_fwd(const double* q, const double* k, const double* v, const int32_t* cu,
-                      int64_t B, int64_t S, int64_t H, int64_t D, double scale,
-                      int first_token, double* o, double* lse, int nthreads) {
+int orc_attention_fwd_local(const double* q, const double* k, const double* v,
+                            const int32_t* cu, int64_t B, int64_t S, int64_t H, int64_t D,
+                            double scale, int first_token, int64_t window_left,
+                            int64_t window_right, double* o, double* lse, int nthreads) {
   if (B < 0 || S < 1 || H < 1 || D < 1) return ORC_INVALID;
   for (int64_t i = 0; i < B; ++i) {
     int64_t len = (int64_t)cu[i + 1] - cu[i];
     if (len < 1 || len > S) return ORC_BAD_LENGTH;
   }
   orc_fwd_ctx ctx = {q, k, v, cu, B, S, H, D, first_token ? B : (B ? cu[B] : 0),
-                     scale, first_token, o, lse};
+                     scale, first_token, window_left, window_right, o, lse};
   return orc_run(orc_fwd_task, &ctx, B * H, (size_t)(3 * S * D + S), nthreads);
+}
+
+int orc_attention_fwd(const double* q, const double* k, const double* v, const int32_t* cu,
+                      int64_t B, int64_t S, int64_t H, int64_t D, double scale,
+                      int first_token, double* o, double* lse, int nthreads) {
+  return orc_attention_fwd_local(q, k, v, cu, B, S, H, D, scale, first_token, -1, -1, o, lse,
+                                 nthreads);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -242,6 +264,7 @@ typedef struct {
   int64_t B, H, D;
   double scale;
   int first_token;
+  int64_t wl, wr;
   const int64_t *rows, *heads;
   double *o, *lse;
 } orc_rows_ctx;
@@ -261,12 +284,13 @@ static void orc_rows_task(void* vctx, int64_t r, double* s) {
   const int64_t i = c->first_token ? c->rows[r] : orc_sequence_of(c->cu, c->B, c->rows[r]);
   const int64_t start = c->cu[i], len = (int64_t)c->cu[i + 1] - c->cu[i];
   const double* qv = c->q + (c->rows[r] * H + h) * D;
+  const int64_t pos = c->first_token ? 0 : c->rows[r] - start; /* query position */
   double m = -INFINITY;
   for (int64_t j = 0; j < len; ++j) {
     const double* kv = c->k + ((start + j) * H + h) * D;
     double acc = 0.0;
     for (int64_t c2 = 0; c2 < D; ++c2) acc += qv[c2] * kv[c2];
-    s[j] = c->scale * acc;
+    s[j] = orc_visible(pos, j, c->wl, c->wr) ? c->scale * acc : -INFINITY;
     if (s[j] > m) m = s[j];
   }
   double z = 0.0;
@@ -282,18 +306,29 @@ static void orc_rows_task(void* vctx, int64_t r, double* s) {
   c->lse[r] = m + log(z);
 }
 
-int orc_attention_fwd_rows(const double* q, const double* k, const double* v,
-                           const int32_t* cu, int64_t B, int64_t H, int64_t D, double scale,
-                           int first_token, const int64_t* rows, const int64_t* heads,
-                           int64_t R, double* o, double* lse, int nthreads) {
+int orc_attention_fwd_rows_local(const double* q, const double* k, const double* v,
+                                 const int32_t* cu, int64_t B, int64_t H, int64_t D,
+                                 double scale, int first_token, int64_t window_left,
+                                 int64_t window_right, const int64_t* rows,
+                                 const int64_t* heads, int64_t R, double* o, double* lse,
+                                 int nthreads) {
   int64_t max_len = 0;
   for (int64_t i = 0; i < B; ++i) {
     int64_t len = (int64_t)cu[i + 1] - cu[i];
     if (len < 1) return ORC_BAD_LENGTH;
     if (len > max_len) max_len = len;
   }
-  orc_rows_ctx ctx = {q, k, v, cu, B, H, D, scale, first_token, rows, heads, o, lse};
+  orc_rows_ctx ctx = {q, k, v, cu, B, H, D, scale, first_token, window_left, window_right,
+                      rows, heads, o, lse};
   return orc_run(orc_rows_task, &ctx, R, (size_t)max_len, nthreads);
+}
+
+int orc_attention_fwd_rows(const double* q, const double* k, const double* v,
+                           const int32_t* cu, int64_t B, int64_t H, int64_t D, double scale,
+                           int first_token, const int64_t* rows, const int64_t* heads,
+                           int64_t R, double* o, double* lse, int nthreads) {
+  return orc_attention_fwd_rows_local(q, k, v, cu, B, H, D, scale, first_token, -1, -1, rows,
+                                      heads, R, o, lse, nthreads);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -313,6 +348,7 @@ typedef struct {
   int64_t B, H, D;
   double scale;
   int first_token;
+  int64_t wl, wr;
   double *dq, *dk, *dv;
 } orc_bwd_ctx;
 
@@ -338,7 +374,7 @@ static void orc_bwd_task(void* vctx, int64_t item, double* scratch) {
       const double* kv = c->k + ((start + j) * H + h) * D;
       double acc = 0.0;
       for (int64_t c2 = 0; c2 < D; ++c2) acc += qv[c2] * kv[c2];
-      p[j] = c->scale * acc;
+      p[j] = orc_visible(r, j, c->wl, c->wr) ? c->scale * acc : -INFINITY;
       if (p[j] > m) m = p[j];
     }
     double z = 0.0;
@@ -373,17 +409,27 @@ static void orc_bwd_task(void* vctx, int64_t item, double* scratch) {
   }
 }
 
-int orc_attention_bwd(const double* q, const double* k, const double* v, const double* dout,
-                      const int32_t* cu, int64_t B, int64_t H, int64_t D, double scale,
-                      int first_token, double* dq, double* dk, double* dv, int nthreads) {
+int orc_attention_bwd_local(const double* q, const double* k, const double* v,
+                            const double* dout, const int32_t* cu, int64_t B, int64_t H,
+                            int64_t D, double scale, int first_token, int64_t window_left,
+                            int64_t window_right, double* dq, double* dk, double* dv,
+                            int nthreads) {
   int64_t max_len = 0;
   for (int64_t i = 0; i < B; ++i) {
     int64_t len = (int64_t)cu[i + 1] - cu[i];
     if (len < 1) return ORC_BAD_LENGTH;
     if (len > max_len) max_len = len;
   }
-  orc_bwd_ctx ctx = {q, k, v, dout, cu, B, H, D, scale, first_token, dq, dk, dv};
+  orc_bwd_ctx ctx = {q, k, v, dout, cu, B, H, D, scale, first_token, window_left,
+                     window_right, dq, dk, dv};
   return orc_run(orc_bwd_task, &ctx, B * H, (size_t)(max_len + D), nthreads);
+}
+
+int orc_attention_bwd(const double* q, const double* k, const double* v, const double* dout,
+                      const int32_t* cu, int64_t B, int64_t H, int64_t D, double scale,
+                      int first_token, double* dq, double* dk, double* dv, int nthreads) {
+  return orc_attention_bwd_local(q, k, v, dout, cu, B, H, D, scale, first_token, -1, -1, dq, dk,
+                                 dv, nthreads);
 }
 
 int orc_hardware_threads(void) {

@@ -324,6 +324,159 @@ def test_backward_invariants():
         np.testing.assert_allclose(dv[rows].sum(0), dout[rows].sum(0), atol=1e-12)
 
 
+# --------------------------------------------------------------------------- local attention
+# Reading of the packed-encoders README's "local-64" mode and FlashAttention's
+# sliding-window pruning: the key at position j is visible from the query at
+# position r of the same sequence iff r - left <= j <= r + right (negative =
+# unbounded); a first-token query sits at position 0.
+
+WINDOWS = [(0, 0), (1, 1), (2, 0), (0, 3), (3, 5), (-1, 2), (4, -1), (-1, -1), (100, 100)]
+
+
+def _band_mask_grid(lengths, s, window, first_token):
+    """[B, Sq, S] boolean from positions on the padded grid: key j real and inside the window."""
+    wl, wr = window
+    rq = np.zeros((1, 1)) if first_token else np.arange(s)[:, None]
+    j = np.arange(s)[None, :]
+    band = np.ones((rq.shape[0], s), dtype=bool)
+    if wl >= 0:
+        band &= j >= rq - wl
+    if wr >= 0:
+        band &= j <= rq + wr
+    real = np.arange(s)[None, None, :] < np.asarray(lengths)[:, None, None]
+    return band[None, :, :] & real
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+@pytest.mark.parametrize("first_token", [False, True])
+def test_local_forward_matches_sdpa_band_mask(window, first_token):
+    for seed in range(3):
+        lengths, s, q, k, v = _random_case(80 + seed, s_max=17)
+        _, cu, n = oracle.pack_sequences(lengths, s)
+        scale = 0.41
+        first = cu[:-1].astype(np.int64)
+        qq = q[first] if first_token else q
+        o, lse = oracle.attention_fwd(qq, k, v, cu, s, scale, first_token=first_token,
+                                      window=window)
+        qg, mask = _padded(q, lengths, s)
+        kg, _ = _padded(k, lengths, s)
+        vg, _ = _padded(v, lengths, s)
+        if first_token:
+            qg = qg[:, :1]
+        tq, tk, tv = (torch.from_numpy(x).transpose(1, 2) for x in (qg, kg, vg))
+        band = torch.from_numpy(_band_mask_grid(lengths, s, window, first_token))[:, None]
+        ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=band, scale=scale)
+        ref = ref.transpose(1, 2).numpy()
+        ref = ref[:, 0] if first_token else ref[mask]
+        scores = (torch.einsum("bhqd,bhkd->bhqk", tq, tk) * scale).masked_fill(~band, float("-inf"))
+        ref_lse = torch.logsumexp(scores, dim=-1).transpose(1, 2).numpy()
+        ref_lse = ref_lse[:, 0] if first_token else ref_lse[mask]
+        # Rows of padded queries may be fully masked in SDPA (NaN); only real rows are compared.
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse.T, ref_lse, rtol=0, atol=1e-12)
+
+
+def test_local_window_zero_is_the_value_row():
+    """Window (0, 0): each query sees only its own key, so o_r = v_r and
+    lse_r = scale * q_r . k_r exactly (a softmax over one element)."""
+    lengths, s, q, k, v = _random_case(90, s_max=9)
+    _, cu, _ = oracle.pack_sequences(lengths, s)
+    o, lse = oracle.attention_fwd(q, k, v, cu, s, 0.7, window=(0, 0))
+    np.testing.assert_array_equal(o, v)
+    np.testing.assert_allclose(lse.T, 0.7 * np.einsum("nhd,nhd->nh", q, k), rtol=0, atol=1e-13)
+
+
+def test_local_window_counts_keys():
+    """With v = 1 in one coordinate and q = 0 (uniform weights), the output is
+    1 and lse = log(number of visible keys) = log(min(r+R, L-1) - max(r-L', 0) + 1)."""
+    lengths = np.array([9, 1, 5], np.int32)
+    s, h, d = 9, 1, 2
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    q = np.zeros((n, h, d))
+    k = np.random.default_rng(91).standard_normal((n, h, d))
+    v = np.zeros((n, h, d))
+    v[..., 0] = 1.0
+    for wl, wr in [(2, 1), (0, 4), (3, 0)]:
+        o, lse = oracle.attention_fwd(q, k, v, cu, s, 1.0, window=(wl, wr))
+        np.testing.assert_allclose(o[..., 0], 1.0, rtol=0, atol=1e-15)
+        for i, length in enumerate(lengths):
+            for r in range(length):
+                count = min(r + wr, length - 1) - max(r - wl, 0) + 1
+                assert abs(lse[0, cu[i] + r] - math.log(count)) < 1e-14
+
+
+@pytest.mark.parametrize("window", [(1, 2), (0, 0), (3, -1)])
+def test_local_sampled_rows_match_full_forward(window):
+    lengths, s, q, k, v = _random_case(93, s_max=15)
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    o, lse = oracle.attention_fwd(q, k, v, cu, s, 0.5, window=window)
+    rng = np.random.default_rng(94)
+    rows = rng.integers(0, n, 20)
+    heads = rng.integers(0, q.shape[1], 20)
+    o2, lse2 = oracle.attention_fwd_rows(q, k, v, cu, 0.5, False, rows, heads, window=window)
+    np.testing.assert_allclose(o2, o[rows, heads], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse[heads, rows], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [(1, 1), (2, 0), (0, 3), (-1, 1)])
+@pytest.mark.parametrize("first_token", [False, True])
+def test_local_backward_matches_torch_autograd(window, first_token):
+    lengths, s, q, k, v = _random_case(95, s_max=12)
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    first = cu[:-1].astype(np.int64)
+    qq = q[first] if first_token else q
+    dout = np.random.default_rng(96).standard_normal(qq.shape)
+    scale = 0.55
+    dq, dk, dv = oracle.attention_bwd(qq, k, v, dout, cu, scale, first_token=first_token,
+                                      window=window)
+    qg, mask = _padded(q, lengths, s)
+    kg, _ = _padded(k, lengths, s)
+    vg, _ = _padded(v, lengths, s)
+    if first_token:
+        qg = qg[:, :1]
+        gg = dout[:, None]
+    else:
+        gg = _padded(dout, lengths, s)[0]
+    tq, tk, tv = (torch.from_numpy(x).transpose(1, 2).requires_grad_(True) for x in (qg, kg, vg))
+    band = torch.from_numpy(_band_mask_grid(lengths, s, window, first_token))[:, None]
+    out = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=band, scale=scale)
+    # Padded query rows of the grid carry no gradient: their dO is zero.
+    out.backward(torch.from_numpy(np.ascontiguousarray(gg)).transpose(1, 2))
+    ref_dq = tq.grad.transpose(1, 2).numpy()
+    ref_dq = ref_dq[:, 0] if first_token else ref_dq[mask]
+    np.testing.assert_allclose(dq, ref_dq, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.transpose(1, 2).numpy()[mask], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.transpose(1, 2).numpy()[mask], rtol=0, atol=1e-12)
+
+
+def test_local_backward_matches_finite_differences():
+    rng = np.random.default_rng(97)
+    lengths = np.array([5, 2], np.int32)
+    s, h, d, scale, window = 5, 1, 3, 0.8, (1, 2)
+    _, cu, n = oracle.pack_sequences(lengths, s)
+    q, k, v, dout = (rng.standard_normal((n, h, d)) for _ in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, cu, scale, window=window)
+    eps = 1e-6
+
+    def loss(qx, kx, vx):
+        o, _ = oracle.attention_fwd(qx, kx, vx, cu, s, scale, threads=1, window=window)
+        return float(np.sum(o * dout))
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            args = {"q": q, "k": k, "v": v}
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args[name] = xp
+            fp = loss(args["q"], args["k"], args["v"])
+            args[name] = xm
+            fm = loss(args["q"], args["k"], args["v"])
+            fd[idx] = (fp - fm) / (2 * eps)
+        np.testing.assert_allclose(g, fd, rtol=0, atol=2e-8, err_msg=name)
+
+
 # --------------------------------------------------------------------------- input recipes
 
 def test_workload_recipes():
