@@ -50,11 +50,25 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def real_flops(lengths, heads, head_dim, first_token=False):
+def visible_pairs(lengths, first_token=False, window=None):
+    """(query, key) pairs that attention computes: L^2 per sequence (L with a
+    first-token query); with a local window (left, right) each query at
+    position r sees keys max(r - left, 0) .. min(r + right, L - 1)."""
     lengths = np.asarray(lengths, dtype=np.int64)
-    if first_token:
-        return float(4 * lengths.sum() * heads * head_dim)
-    return float(4 * (lengths ** 2).sum() * heads * head_dim)
+    if window is None:
+        return int(lengths.sum()) if first_token else int((lengths ** 2).sum())
+    left, right = window
+    total = 0
+    for length in lengths:
+        pos = np.zeros(1, np.int64) if first_token else np.arange(length, dtype=np.int64)
+        lo = np.maximum(pos - left, 0) if left >= 0 else np.zeros_like(pos)
+        hi = np.minimum(pos + right, length - 1) if right >= 0 else np.full_like(pos, length - 1)
+        total += int((hi - lo + 1).sum())
+    return total
+
+
+def real_flops(lengths, heads, head_dim, first_token=False, window=None):
+    return float(4 * visible_pairs(lengths, first_token, window) * heads * head_dim)
 
 
 # --------------------------------------------------------------------------- clocks
@@ -180,7 +194,8 @@ def run_ours(args, rank, world):
         if not args.packed:
             raise SystemExit("--first-token needs --packed")
         train = False
-    fwd_flops = real_flops(lengths, h, d, first_token=args.first_token)
+    window = tuple(args.window) if args.window else None
+    fwd_flops = real_flops(lengths, h, d, first_token=args.first_token, window=window)
     bwd_flops = 2.5 * fwd_flops if train else 0.0   # 10 sum L^2 H d: five GEMM-shaped products
     flops = fwd_flops + bwd_flops
     kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token)
@@ -195,6 +210,19 @@ def run_ours(args, rank, world):
                if args.packed and args.first_token else None)
     stream = torch.cuda.current_stream(dev)
     fwd_events, bwd_events = [], []
+
+    # Full attention, or local attention with the --window bounds.
+    def attention_fwd(*a, **kw):
+        if window is None:
+            return pe.pe_packed_attention_fwd(*a, **kw)
+        q_, k_, v_, cu_, s_, scale_ = a
+        return pe.pe_packed_attention_fwd_local(q_, k_, v_, cu_, s_, window[0], window[1],
+                                                scale_, **kw)
+
+    def attention_bwd(*a):
+        if window is None:
+            return pe.pe_packed_attention_bwd(*a)
+        return pe.pe_packed_attention_bwd_local(*a[:8], window[0], window[1], a[8])
 
     def timed(record, events, fn):
         if not record:
@@ -211,15 +239,14 @@ def run_ours(args, rank, world):
             cu = packed_cu
             q, k, v = grids[:3]
             if args.first_token:
-                out, _ = timed(record, fwd_events, lambda: pe.pe_packed_attention_fwd(
+                out, _ = timed(record, fwd_events, lambda: attention_fwd(
                     q_first, k, v, cu, s, wl.scale, query_is_first_token=True))
                 return n_tokens
         else:
             flat, cu, n = pe.pe_pack_sequences(lengths_t, s)
             q, k, v = (pe.pe_gather_packed(g, flat, n) for g in grids[:3])
         out, lse = timed(record, fwd_events,
-                         lambda: pe.pe_packed_attention_fwd(q, k, v, cu, s, wl.scale,
-                                                            need_lse=train))
+                         lambda: attention_fwd(q, k, v, cu, s, wl.scale, need_lse=train))
         if args.packed:
             og.copy_(out)
         else:
@@ -227,8 +254,7 @@ def run_ours(args, rank, world):
         if train:
             do = grids[3] if args.packed else pe.pe_gather_packed(grids[3], flat, n)
             grads = timed(record, bwd_events,
-                          lambda: pe.pe_packed_attention_bwd(do, q, k, v, out, lse, cu, s,
-                                                             wl.scale))
+                          lambda: attention_bwd(do, q, k, v, out, lse, cu, s, wl.scale))
             for g, grid in zip(grads, grad_grids):
                 if args.packed:
                     grid.copy_(g)
@@ -342,6 +368,9 @@ def run_ours(args, rank, world):
                    "description": wl.description,
                    "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
                    "heads": h, "head_dim": d, "max_seq_len": s,
+                   "attention": (f"local window ({window[0]}, {window[1]})" if window
+                                 else "full") + (", first-token query" if args.first_token
+                                                 else ""),
                    "step": (("tile plan + attention forward + backward on packed inputs"
                              if train else "tile plan + attention forward on packed inputs")
                             if args.packed else
@@ -371,15 +400,15 @@ def run_ours(args, rank, world):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows, args.seed)
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows, args.seed, window)
     return line
 
 
 # --------------------------------------------------------------------------- oracle arms
 
-def _oracle_sample(workload: str, rows: int, seed: int):
+def _oracle_sample(workload: str, rows: int, seed: int, window=None):
     """A bounded sample of the workload for the oracle: `rows` random (token,
-    head) query rows, each attending over its whole sequence."""
+    head) query rows, each attending over its whole sequence (or its window)."""
     from padding_free_packed_gb300 import workloads
     x = workloads.make_inputs(workload, seed=seed)
     import oracle
@@ -389,27 +418,34 @@ def _oracle_sample(workload: str, rows: int, seed: int):
     hs = rng.integers(0, x.workload.num_heads, rows)
     seq = np.searchsorted(cu, r, side="right") - 1
     lens = (cu[1:] - cu[:-1]).astype(np.int64)[seq]
+    if window is not None:   # keys each sampled query sees inside its window
+        pos = r - cu[seq]
+        lo = np.maximum(pos - window[0], 0) if window[0] >= 0 else np.zeros_like(pos)
+        hi = np.minimum(pos + window[1], lens - 1) if window[1] >= 0 else lens - 1
+        lens = hi - lo + 1
     flops = float(4 * lens.sum() * x.workload.head_dim)
     # Widen to fp64 once, outside any timed region.
     x.q, x.k, x.v = (t.double().numpy() for t in (x.q, x.k, x.v))
     return x, cu, r, hs, flops
 
 
-def _time_oracle(x, cu, r, hs):
+def _time_oracle(x, cu, r, hs, window=None):
     import oracle
     threads = oracle.default_threads()
     t0 = time.perf_counter()
-    oracle.attention_fwd_rows(x.q, x.k, x.v, cu, x.workload.scale, False, r, hs, threads=threads)
+    oracle.attention_fwd_rows(x.q, x.k, x.v, cu, x.workload.scale, False, r, hs, threads=threads,
+                              window=window or (-1, -1))
     return time.perf_counter() - t0, threads
 
 
-def cpu_baseline(workload: str, rows: int, seed: int):
-    x, cu, r, hs, flops = _oracle_sample(workload, rows, seed)
-    dt, threads = _time_oracle(x, cu, r, hs)
+def cpu_baseline(workload: str, rows: int, seed: int, window=None):
+    x, cu, r, hs, flops = _oracle_sample(workload, rows, seed, window)
+    dt, threads = _time_oracle(x, cu, r, hs, window)
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
             "seconds": dt,
             "sample": f"{rows} random (token, head) query rows of {workload} (seed {seed}), each "
-                      "over its whole sequence, fp64 oracle row path"}
+                      + ("over its whole sequence" if window is None else
+                         f"over its local window {tuple(window)}") + ", fp64 oracle row path"}
 
 
 def run_reference(args, rank, world):
@@ -417,18 +453,20 @@ def run_reference(args, rank, world):
         return None
     from padding_free_packed_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
-    x, cu, r, hs, flops = _oracle_sample(args.workload, args.ref_rows, args.seed)
+    window = tuple(args.window) if args.window else None
+    x, cu, r, hs, flops = _oracle_sample(args.workload, args.ref_rows, args.seed, window)
     for _ in range(args.warmup):
-        _time_oracle(x, cu, r, hs)
+        _time_oracle(x, cu, r, hs, window)
     times = []
     threads = 1
     for _ in range(args.steps):
-        dt, threads = _time_oracle(x, cu, r, hs)
+        dt, threads = _time_oracle(x, cu, r, hs, window)
         times.append(dt)
     total = sum(times)
     value = flops * args.steps / total / 1e12
     sample = (f"{args.ref_rows} random (token, head) query rows of {args.workload} per step, "
-              "each over its whole sequence, fp64 oracle row path")
+              + ("each over its whole sequence" if window is None else
+                 f"each over its local window {window}") + ", fp64 oracle row path")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -454,6 +492,9 @@ def main():
                     help="inputs already packed: time the attention calls alone")
     ap.add_argument("--first-token", action="store_true",
                     help="with --packed: one query per sequence (its first token)")
+    ap.add_argument("--window", type=int, nargs=2, metavar=("LEFT", "RIGHT"), default=None,
+                    help="local attention: query at position r sees keys r-LEFT .. r+RIGHT "
+                         "(negative = unbounded); e.g. 64 64 for ModernBERT's local layers")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=98304,

@@ -50,7 +50,8 @@ typedef enum pe_dtype { PE_BF16 = 0, PE_FP32 = 1 } pe_dtype;
 /* Text for a status code; never NULL. */
 const char* pe_status_string(int status);
 
-/* Version of this ABI (incremented on any signature change). */
+/* Version of this ABI (incremented when an entry point is added or changed;
+ * 2 added pe_packed_attention_fwd_local and pe_packed_attention_bwd_local). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -166,6 +167,41 @@ pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t num_sequences, int64_t
                                   const void* out, const float* lse, const void* dout,
                                   void* dq, void* dk, void* dv,
                                   void* workspace, size_t workspace_bytes, pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Local (sliding-window) packed attention: the same forward and backward with
+ * each query restricted to a window of key positions around its own. The
+ * pages name the mode without defining it (packed-encoders README: the packed
+ * kernel's "global or local-64 attention" for ModernBERT geometry, and
+ * FlashAttention's sliding-window pruning); here the key at position j of a
+ * sequence is visible from the query at position r of the same sequence iff
+ *     r - window_left <= j <= r + window_right,
+ * positions counted from the sequence start, a first-token query sitting at
+ * position 0. A negative bound is unbounded, so (-1, -1) is exactly
+ * pe_packed_attention_fwd / _bwd; ModernBERT's local-64 is (64, 64). Every
+ * query sees at least its own key. Kernels visit only the key blocks inside
+ * the band, so the work per query is O(window) rather than O(length).
+ * All other arguments, layouts, workspace sizes and errors are those of
+ * pe_packed_attention_fwd / pe_packed_attention_bwd (out and lse passed to
+ * the backward must come from the forward with the same window).
+ * ------------------------------------------------------------------------ */
+pe_status pe_packed_attention_fwd_local(pe_dtype dtype, int32_t num_sequences,
+                                        int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                        int32_t max_seq_len, const void* q, const void* k,
+                                        const void* v, const int32_t* cu_seqlens, float scale,
+                                        int32_t window_left, int32_t window_right,
+                                        int query_is_first_token, void* out, float* lse,
+                                        void* workspace, size_t workspace_bytes,
+                                        pe_stream_t stream);
+pe_status pe_packed_attention_bwd_local(pe_dtype dtype, int32_t num_sequences,
+                                        int64_t num_tokens, int32_t num_heads, int32_t head_dim,
+                                        int32_t max_seq_len, const void* q, const void* k,
+                                        const void* v, const int32_t* cu_seqlens, float scale,
+                                        int32_t window_left, int32_t window_right,
+                                        int query_is_first_token, const void* out,
+                                        const float* lse, const void* dout, void* dq, void* dk,
+                                        void* dv, void* workspace, size_t workspace_bytes,
+                                        pe_stream_t stream);
 
 /* Name of the kernel family that pe_packed_attention_fwd (backward = 0) or
  * pe_packed_attention_bwd (backward = 1) runs for these arguments on an sm_103a

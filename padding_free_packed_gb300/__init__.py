@@ -14,7 +14,9 @@ from .binding import (  # noqa: F401
     pe_gather_packed,
     pe_pack_sequences,
     pe_packed_attention_bwd,
+    pe_packed_attention_bwd_local,
     pe_packed_attention_fwd,
+    pe_packed_attention_fwd_local,
     pe_read_device_status,
     pe_scatter_padded,
 )

@@ -23,8 +23,8 @@ PE_FP32 = 1
 EXPORTED = (
     "pe_status_string", "pe_abi_version", "pe_pack_workspace_size", "pe_pack_sequences",
     "pe_gather_packed", "pe_scatter_padded", "pe_attention_workspace_size",
-    "pe_packed_attention_fwd", "pe_packed_attention_bwd", "pe_read_device_status",
-    "pe_attention_kernel",
+    "pe_packed_attention_fwd", "pe_packed_attention_bwd", "pe_packed_attention_fwd_local",
+    "pe_packed_attention_bwd_local", "pe_read_device_status", "pe_attention_kernel",
 )
 
 _lib = None
@@ -69,6 +69,14 @@ def load_library(path: str = LIB_PATH):
                                             c.c_float, c.c_int, vp, vp, vp, vp, vp, vp, vp, sz,
                                             vp]
     lib.pe_packed_attention_bwd.restype = c.c_int
+    lib.pe_packed_attention_fwd_local.argtypes = [c.c_int, i32, i64, i32, i32, i32, vp, vp, vp,
+                                                  vp, c.c_float, i32, i32, c.c_int, vp, vp, vp,
+                                                  sz, vp]
+    lib.pe_packed_attention_fwd_local.restype = c.c_int
+    lib.pe_packed_attention_bwd_local.argtypes = [c.c_int, i32, i64, i32, i32, i32, vp, vp, vp,
+                                                  vp, c.c_float, i32, i32, c.c_int, vp, vp, vp,
+                                                  vp, vp, vp, vp, sz, vp]
+    lib.pe_packed_attention_bwd_local.restype = c.c_int
     lib.pe_attention_kernel.argtypes = [c.c_int, i32, c.c_int, c.c_int]
     lib.pe_attention_kernel.restype = c.c_char_p
     lib.pe_read_device_status.argtypes = [vp, vp]
@@ -169,6 +177,23 @@ def pe_packed_attention_fwd(q, k, v, cu_seqlens, max_seq_len: int, scale: float 
                             query_is_first_token: bool = False, need_lse: bool = False,
                             out=None, lse=None, workspace=None):
     """Packed attention forward. Returns (out, lse or None)."""
+    return _forward(None, q, k, v, cu_seqlens, max_seq_len, scale, query_is_first_token,
+                    need_lse, out, lse, workspace)
+
+
+def pe_packed_attention_fwd_local(q, k, v, cu_seqlens, max_seq_len: int, window_left: int,
+                                  window_right: int, scale: float | None = None,
+                                  query_is_first_token: bool = False, need_lse: bool = False,
+                                  out=None, lse=None, workspace=None):
+    """Local (sliding-window) packed attention forward: the query at position r
+    sees keys r - window_left .. r + window_right of its own sequence (a negative
+    bound is unbounded). Returns (out, lse or None)."""
+    return _forward((int(window_left), int(window_right)), q, k, v, cu_seqlens, max_seq_len,
+                    scale, query_is_first_token, need_lse, out, lse, workspace)
+
+
+def _forward(window, q, k, v, cu_seqlens, max_seq_len, scale, query_is_first_token, need_lse,
+             out, lse, workspace):
     lib = load_library()
     q, k, v = _cuda(q, "q"), _cuda(k, "k"), _cuda(v, "v")
     cu_seqlens = _cuda(cu_seqlens, "cu_seqlens")
@@ -185,11 +210,15 @@ def pe_packed_attention_fwd(q, k, v, cu_seqlens, max_seq_len: int, scale: float 
     if workspace is None:
         workspace = _workspace(attention_workspace_bytes(q.dtype, b, n, h, d, max_seq_len,
                                                          query_is_first_token, False), q.device)
-    _check("pe_packed_attention_fwd",
-           lib.pe_packed_attention_fwd(_dtype_code(q.dtype), b, n, h, d, int(max_seq_len),
-                                       _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), scale,
-                                       int(bool(query_is_first_token)), _ptr(out), _ptr(lse),
-                                       _ptr(workspace), workspace.numel(), _stream(q.device)))
+    head = (_dtype_code(q.dtype), b, n, h, d, int(max_seq_len), _ptr(q), _ptr(k), _ptr(v),
+            _ptr(cu_seqlens), scale)
+    tail = (int(bool(query_is_first_token)), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel(), _stream(q.device))
+    if window is None:
+        _check("pe_packed_attention_fwd", lib.pe_packed_attention_fwd(*head, *tail))
+    else:
+        _check("pe_packed_attention_fwd_local",
+               lib.pe_packed_attention_fwd_local(*head, window[0], window[1], *tail))
     return out, lse
 
 
@@ -197,6 +226,22 @@ def pe_packed_attention_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seq_len: in
                             scale: float | None = None, query_is_first_token: bool = False,
                             workspace=None):
     """Packed attention backward. Returns (dq, dk, dv)."""
+    return _backward(None, dout, q, k, v, out, lse, cu_seqlens, max_seq_len, scale,
+                     query_is_first_token, workspace)
+
+
+def pe_packed_attention_bwd_local(dout, q, k, v, out, lse, cu_seqlens, max_seq_len: int,
+                                  window_left: int, window_right: int,
+                                  scale: float | None = None, query_is_first_token: bool = False,
+                                  workspace=None):
+    """Local (sliding-window) packed attention backward; out and lse come from
+    pe_packed_attention_fwd_local with the same window. Returns (dq, dk, dv)."""
+    return _backward((int(window_left), int(window_right)), dout, q, k, v, out, lse, cu_seqlens,
+                     max_seq_len, scale, query_is_first_token, workspace)
+
+
+def _backward(window, dout, q, k, v, out, lse, cu_seqlens, max_seq_len, scale,
+              query_is_first_token, workspace):
     lib = load_library()
     q, k, v = _cuda(q, "q"), _cuda(k, "k"), _cuda(v, "v")
     out, dout, lse = _cuda(out, "out"), _cuda(dout, "dout"), _cuda(lse, "lse")
@@ -208,12 +253,15 @@ def pe_packed_attention_bwd(dout, q, k, v, out, lse, cu_seqlens, max_seq_len: in
     if workspace is None:
         workspace = _workspace(attention_workspace_bytes(q.dtype, b, n, h, d, max_seq_len,
                                                          query_is_first_token, True), q.device)
-    _check("pe_packed_attention_bwd",
-           lib.pe_packed_attention_bwd(_dtype_code(q.dtype), b, n, h, d, int(max_seq_len),
-                                       _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), scale,
-                                       int(bool(query_is_first_token)), _ptr(out), _ptr(lse),
-                                       _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                                       _ptr(workspace), workspace.numel(), _stream(q.device)))
+    head = (_dtype_code(q.dtype), b, n, h, d, int(max_seq_len), _ptr(q), _ptr(k), _ptr(v),
+            _ptr(cu_seqlens), scale)
+    tail = (int(bool(query_is_first_token)), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+            _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), _stream(q.device))
+    if window is None:
+        _check("pe_packed_attention_bwd", lib.pe_packed_attention_bwd(*head, *tail))
+    else:
+        _check("pe_packed_attention_bwd_local",
+               lib.pe_packed_attention_bwd_local(*head, window[0], window[1], *tail))
     return dq, dk, dv
 
 

@@ -104,7 +104,7 @@ extern "C" const char* pe_status_string(int status) {
   }
 }
 
-extern "C" int pe_abi_version(void) { return 1; }
+extern "C" int pe_abi_version(void) { return 2; }
 
 extern "C" size_t pe_attention_workspace_size(pe_dtype /*dtype*/, int32_t B, int64_t N,
                                               int32_t H, int32_t D, int32_t S,
@@ -115,12 +115,11 @@ extern "C" size_t pe_attention_workspace_size(pe_dtype /*dtype*/, int32_t B, int
   return bytes;
 }
 
-extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
-                                             int32_t D, int32_t S, const void* q, const void* k,
-                                             const void* v, const int32_t* cu_seqlens,
-                                             float scale, int query_is_first_token, void* out,
-                                             float* lse, void* workspace, size_t workspace_bytes,
-                                             pe_stream_t stream_) {
+extern "C" pe_status pe_packed_attention_fwd_local(
+    pe_dtype dtype, int32_t B, int64_t N, int32_t H, int32_t D, int32_t S, const void* q,
+    const void* k, const void* v, const int32_t* cu_seqlens, float scale, int32_t window_left,
+    int32_t window_right, int query_is_first_token, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, pe_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   PE_TRY(check_common(dtype, B, N, H, D, S, scale));
   const int64_t nq = query_is_first_token ? B : N;
@@ -134,6 +133,7 @@ extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t 
                          attention_ws_bytes(B, N, H, query_is_first_token, 0)));
   if (query_is_first_token && !first_token_supported(D)) return PE_ERR_UNSUPPORTED;
   if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  const Window win = make_window(window_left, window_right, S);
   PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (B == 0) return PE_OK;
   if (query_is_first_token) {
@@ -144,27 +144,37 @@ extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t 
     if (part_bytes > 0 && N > 2LL * kFirstTokenChunk * B &&
         workspace_bytes >= plan_bytes(B) + part_bytes)
       part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
-    return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, S, scale, out, lse, part,
+    return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, S, scale, win, out, lse, part,
                            plan_view(workspace, B), stream);
   }
   TilePlan plan = plan_view(workspace, B);
   if (dtype == PE_BF16 && D == 64) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(), S, plan, nullptr,
                             stream));
-    return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, out, lse, plan,
+    return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan,
                      static_cast<DeviceStatus*>(workspace), stream);
   }
   PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_tile(), S, plan, nullptr, stream));
-  return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, out, lse, N, plan, stream);
+  return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, win, out, lse, N, plan, stream);
 }
 
-extern "C" pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
+extern "C" pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
                                              int32_t D, int32_t S, const void* q, const void* k,
                                              const void* v, const int32_t* cu_seqlens,
-                                             float scale, int query_is_first_token,
-                                             const void* out, const float* lse, const void* dout,
-                                             void* dq, void* dk, void* dv, void* workspace,
-                                             size_t workspace_bytes, pe_stream_t stream_) {
+                                             float scale, int query_is_first_token, void* out,
+                                             float* lse, void* workspace, size_t workspace_bytes,
+                                             pe_stream_t stream) {
+  return pe_packed_attention_fwd_local(dtype, B, N, H, D, S, q, k, v, cu_seqlens, scale, -1, -1,
+                                       query_is_first_token, out, lse, workspace,
+                                       workspace_bytes, stream);
+}
+
+extern "C" pe_status pe_packed_attention_bwd_local(
+    pe_dtype dtype, int32_t B, int64_t N, int32_t H, int32_t D, int32_t S, const void* q,
+    const void* k, const void* v, const int32_t* cu_seqlens, float scale, int32_t window_left,
+    int32_t window_right, int query_is_first_token, const void* out, const float* lse,
+    const void* dout, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+    pe_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   PE_TRY(check_common(dtype, B, N, H, D, S, scale));
   const int64_t nq = query_is_first_token ? B : N;
@@ -181,17 +191,30 @@ extern "C" pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t B, int64_t 
   PE_TRY(check_workspace(workspace, workspace_bytes,
                          attention_ws_bytes(B, N, H, query_is_first_token, 1)));
   if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  const Window win = make_window(window_left, window_right, S);
   PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (B == 0) return PE_OK;
   TilePlan plan = plan_view(workspace, B);
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
   if (dtype == PE_BF16 && D == 64 && !query_is_first_token) {
     PE_TRY(bwd_preprocess(dtype, D, out, dout, N, H, delta, stream));
-    return bwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, lse, dout, delta, dq, dk, dv, plan,
-                     static_cast<DeviceStatus*>(workspace), stream);
+    return bwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, lse, dout, delta, dq, dk, dv,
+                     plan, static_cast<DeviceStatus*>(workspace), stream);
   }
-  return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, out, lse,
-                  dout, dq, dk, dv, delta, plan, stream);
+  return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, win, out,
+                  lse, dout, dq, dk, dv, delta, plan, stream);
+}
+
+extern "C" pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
+                                             int32_t D, int32_t S, const void* q, const void* k,
+                                             const void* v, const int32_t* cu_seqlens,
+                                             float scale, int query_is_first_token,
+                                             const void* out, const float* lse, const void* dout,
+                                             void* dq, void* dk, void* dv, void* workspace,
+                                             size_t workspace_bytes, pe_stream_t stream) {
+  return pe_packed_attention_bwd_local(dtype, B, N, H, D, S, q, k, v, cu_seqlens, scale, -1, -1,
+                                       query_is_first_token, out, lse, dout, dq, dk, dv,
+                                       workspace, workspace_bytes, stream);
 }
 
 extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_is_first_token,

@@ -29,6 +29,9 @@
 //                epilogue (scale, store the rows inside the sequence).
 // Tensor memory: T1 [0,128) T2 [128,256) P [256,320) dS [320,384)
 // ACC1 [384,448) ACC2 [448,512). Every wait is bounded as in the forward.
+// With local attention an item streams only the blocks inside the window band
+// (key pass: the queries that can see its keys; query pass: the keys its rows
+// can see) and the elementwise step zeroes P outside each row's window.
 #include <cudaTypedefs.h>
 
 #include "pe_kernels.cuh"
@@ -78,12 +81,34 @@ struct BwdParams {
   __nv_bfloat16* out1;         // key pass: dK; query pass: dQ
   __nv_bfloat16* out2;         // key pass: dV
   TilePlan plan;
+  Window win;
   DeviceStatus* status;
 };
 
+// Streaming blocks [i0, i0 + nblk) of the item block `blk` of a sequence of
+// len rows: in the key pass the query blocks whose rows see one of the item's
+// keys, in the query pass the key blocks that one of the item's rows sees
+// (every block without a window). Never empty: a key is visible from its own
+// position.
+template <bool kKeyPass, bool kLocal>
+__device__ __forceinline__ void stream_blocks(const BwdParams& p, int32_t len, int32_t blk,
+                                              int32_t& i0, int32_t& nblk) {
+  if (!kLocal) {
+    i0 = 0;
+    nblk = (len + kRows - 1) / kRows;
+    return;
+  }
+  const Window w = kKeyPass ? Window{p.win.right, p.win.left} : p.win;
+  const int32_t first = blk * kRows, last = min(first + kRows, len) - 1;
+  i0 = window_lo(w, first) / kRows;
+  nblk = window_hi(w, last, len) / kRows - i0 + 1;
+}
+
 enum WaitSite { kSiteProducer = 11, kSiteT = 12, kSiteAcc = 13, kSiteEw = 14 };
 
-template <bool kKeyPass>
+// kLocal selects the local-attention variant (block ranges and window masks);
+// full attention compiles without them.
+template <bool kKeyPass, bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -186,7 +211,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.seq < 0) break;
       const int32_t start = __ldg(p.cu + it.seq);
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      const int32_t nb = (len + kRows - 1) / kRows;
+      int32_t i0, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
       const int32_t x = it.head * kD;
       if (!warp_wait(smem_u32(&S.st_empty), (item_no & 1) ^ 1, abort_flag, p.status,
                      kSiteProducer)) {
@@ -209,11 +235,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (kKeyPass) {
           // lse*log2e and Delta of the block's 128 queries; +inf / 0 past the
           // sequence end, so those columns get P = 0.
-          const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + i * kRows;
+          const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + (i0 + i) * kRows;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int r = lane + 32 * u;
-            const bool in = i * kRows + r < len;
+            const bool in = (i0 + i) * kRows + r < len;
             S.vec[s][0][r] = in ? __ldg(p.lse + base + r) * kLog2e : INFINITY;
             S.vec[s][1][r] = in ? __ldg(p.delta + base + r) : 0.f;
           }
@@ -221,8 +247,10 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         __syncwarp();
         if (lane == 0) {
           mbar_arrive_expect_tx(smem_u32(&S.u_full[s]), 2 * kTileBytes);
-          tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x, start + i * kRows);
-          tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x, start + i * kRows);
+          tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x,
+                      start + (i0 + i) * kRows);
+          tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x,
+                      start + (i0 + i) * kRows);
         }
         if (kKeyPass) mbar_arrive(smem_u32(&S.u_full[s]));
         pending_u[s] = static_cast<int>(ph);
@@ -246,7 +274,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!read_item(item_no, it, kSiteT)) break;
       if (it.seq < 0) break;
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      const int32_t nb = (len + kRows - 1) / kRows;
+      int32_t i0, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
       if (!warp_wait(smem_u32(&S.st_full), item_no & 1, abort_flag, p.status, kSiteT)) break;
       for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_t) {
         const int s = u_no % kStages;
@@ -287,7 +316,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!read_item(item_no, it, kSiteAcc)) break;
       if (it.seq < 0) break;
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      const int32_t nb = (len + kRows - 1) / kRows;
+      int32_t i0, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
       // The previous item's accumulators must have been read by the epilogue.
       if (!warp_wait(smem_u32(&S.o_free), (item_no & 1) ^ 1, abort_flag, p.status, kSiteAcc))
         break;
@@ -328,8 +358,14 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.seq < 0) break;
       const int32_t start = __ldg(p.cu + it.seq);
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      const int32_t nb = (len + kRows - 1) / kRows;
+      int32_t i0, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
       const int32_t r0 = it.blk * kRows;
+      // Streaming positions this row pairs with inside the window: the queries
+      // that see this key (key pass) or the keys this query sees (query pass).
+      constexpr bool windowed = kLocal;
+      const Window wrow = kKeyPass ? Window{p.win.right, p.win.left} : p.win;
+      const int32_t vis_lo = window_lo(wrow, r0 + row), vis_hi = window_hi(wrow, r0 + row, len);
       // Query pass: this thread's query row carries its own lse and Delta.
       float row_lse2 = 0.f, row_delta = 0.f;
       if (!kKeyPass && r0 + row < len) {
@@ -358,7 +394,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           tc_fence_after();
         }
-        const int32_t col_valid = len - i * kRows - 64 * h;  // query pass: valid keys in this half
+        const int32_t col_valid = len - (i0 + i) * kRows - 64 * h;  // query pass: valid keys in this half
+        const int32_t clo = vis_lo - (i0 + i) * kRows - 64 * h;  // window, relative to this half
+        const int32_t chi = vis_hi - (i0 + i) * kRows - 64 * h;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * h + 32 * c;
@@ -384,6 +422,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               }
               float pv = ex2(fmaf(__uint_as_float(sv[cc]), scale_log2, -lse2));
               if (!kKeyPass && 32 * c + cc >= col_valid) pv = 0.f;  // key past the sequence
+              if (windowed && (32 * c + cc < clo || 32 * c + cc > chi)) pv = 0.f;
               pr[u] = pv;
               ds[u] = pv * (__uint_as_float(dv[cc]) - dlt);
             }
@@ -487,7 +526,8 @@ pe_status make_map_bwd(CUtensorMap* map, const void* base, int64_t N, int32_t H)
 template <bool kKeyPass>
 pe_status launch_pass(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                       const CUtensorMap& mdo, const BwdParams& prm, cudaStream_t stream) {
-  auto kernel = bwd_sm103_kernel<kKeyPass>;
+  auto kernel = prm.win.active() ? bwd_sm103_kernel<kKeyPass, true>
+                                 : bwd_sm103_kernel<kKeyPass, false>;
   const size_t smem = sizeof(Smem) + 1024;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
@@ -500,7 +540,8 @@ pe_status launch_pass(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
 }  // namespace
 
 pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                    int32_t H, int64_t N, float scale, const float* lse, const void* dout,
+                    int32_t H, int64_t N, float scale, Window win, const float* lse,
+                    const void* dout,
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
                     DeviceStatus* status, cudaStream_t stream) {
   PE_TRY(get_encoder_bwd());
@@ -516,6 +557,7 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.Nq = N;
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
+  prm.win = win;
   prm.lse = lse;
   prm.delta = delta;
   prm.plan = plan;

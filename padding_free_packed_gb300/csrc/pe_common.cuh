@@ -75,6 +75,34 @@ struct TilePlan {
   int32_t* tile_end;       // [B] inclusive prefix of tiles over positions
 };
 
+// Local (sliding-window) attention: the key at position j of a sequence is
+// visible from the query at position r iff r - left <= j <= r + right. Both
+// bounds are >= 0; kUnbounded stands for no bound (full attention).
+constexpr int32_t kUnbounded = 0x7fffffff;
+struct Window {
+  int32_t left, right;
+  __host__ __device__ bool active() const { return left != kUnbounded || right != kUnbounded; }
+};
+// The ABI's (left, right) with a negative bound meaning unbounded; a bound of
+// max_seq_len - 1 or more reaches every key, so it is unbounded too.
+inline Window make_window(int32_t left, int32_t right, int32_t max_seq_len) {
+  Window w;
+  w.left = (left < 0 || left >= max_seq_len - 1) ? kUnbounded : left;
+  w.right = (right < 0 || right >= max_seq_len - 1) ? kUnbounded : right;
+  return w;
+}
+constexpr Window kFullWindow = {kUnbounded, kUnbounded};
+// First visible key position of the query at position r (r >= 0).
+__host__ __device__ __forceinline__ int32_t window_lo(Window w, int32_t r) {
+  return r - (w.left < r ? w.left : r);
+}
+// Last visible key position of the query at position r < len in a sequence of
+// len keys (len - 1 for r >= len, rows that are computed but never stored).
+__host__ __device__ __forceinline__ int32_t window_hi(Window w, int32_t r, int32_t len) {
+  const int32_t room = len - 1 - r;
+  return r + (w.right < room ? w.right : room);
+}
+
 // Workspace layout shared by the attention entry points:
 //   [0, 16)        DeviceStatus
 //   [16, 32)       counter, total_tiles

@@ -13,6 +13,10 @@
 // columns tx*CPT .. tx*CPT+CPT-1. Softmax is online, in the base-2 domain, with
 // the row statistics reduced across the 16 tx lanes by warp shuffles.
 //
+// Local attention (a window of key positions around each query position)
+// restricts the key blocks a tile visits to those its rows can see and masks
+// the rest of those blocks per element.
+//
 // First-token mode: the query of sequence i is one row, so the work is a
 // matrix-vector product bounded by reading k and v once. One CTA per
 // (sequence, head); lanes are grouped so that each group reads whole 16-byte
@@ -68,11 +72,14 @@ __device__ __forceinline__ void stage_rows(float* __restrict__ smem, const T* __
   }
 }
 
-template <typename T, int D>
+// kLocal selects the local-attention variant (key range and window masks);
+// full attention compiles without them.
+template <typename T, int D, bool kLocal>
 __global__ void __launch_bounds__(kThreads)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                 const int32_t* __restrict__ cu, int32_t B, int32_t H, float scale_log2,
-                T* __restrict__ out, float* __restrict__ lse, int64_t lse_stride, TilePlan plan) {
+                Window win, T* __restrict__ out, float* __restrict__ lse, int64_t lse_stride,
+                TilePlan plan) {
   using Shape = SimtShape<D>;
   constexpr int P = Shape::kPitch;
   constexpr int CPT = Shape::kCPT;
@@ -104,16 +111,24 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     stage_rows<T, D>(Qs, q + ((int64_t)(start + q0) * H + h) * D, row_stride, rows_valid);
 
     float m[4], l[4], o[4][CPT];
+    int32_t vis_lo[4], vis_hi[4];  // visible key positions of each row (local attention)
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii) {
       m[ii] = -INFINITY;
       l[ii] = 0.f;
 #pragma unroll
       for (int c = 0; c < CPT; ++c) o[ii][c] = 0.f;
+      vis_lo[ii] = window_lo(win, q0 + ty + 16 * ii);
+      vis_hi[ii] = window_hi(win, q0 + ty + 16 * ii, len);
     }
+    // Keys any real row of the tile can see: from the first row's first
+    // visible key to the last row's last one.
+    constexpr bool windowed = kLocal;
+    const int32_t kb_begin = windowed ? window_lo(win, q0) : 0;
+    const int32_t kb_end = windowed ? window_hi(win, q0 + rows_valid - 1, len) + 1 : len;
 
-    for (int32_t kb = 0; kb < len; kb += kBN) {
-      const int keys_valid = min(kBN, len - kb);
+    for (int32_t kb = kb_begin; kb < kb_end; kb += kBN) {
+      const int keys_valid = min(kBN, kb_end - kb);
       __syncthreads();  // previous block's Ks/Vs/Ps fully consumed
       stage_rows<T, D>(Ks, k + ((int64_t)(start + kb) * H + h) * D, row_stride, keys_valid);
       stage_rows<T, D>(Vs, v + ((int64_t)(start + kb) * H + h) * D, row_stride, keys_valid);
@@ -145,24 +160,32 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
           }
       }
 
-      // Online softmax (base 2). Keys past the sequence end are excluded.
+      // Online softmax (base 2). Keys past the sequence end, or outside a
+      // row's window, are excluded.
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii) {
         float bmax = -INFINITY;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          s[ii][jj] = (tx + 16 * jj < keys_valid) ? s[ii][jj] * scale_log2 : -INFINITY;
+          const int32_t kp = kb + tx + 16 * jj;
+          const bool vis = (tx + 16 * jj < keys_valid) &&
+                           (!windowed || (kp >= vis_lo[ii] && kp <= vis_hi[ii]));
+          s[ii][jj] = vis ? s[ii][jj] * scale_log2 : -INFINITY;
           bmax = fmaxf(bmax, s[ii][jj]);
         }
 #pragma unroll
         for (int off = 1; off < 16; off <<= 1)
           bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, off));
-        const float m_new = fmaxf(m[ii], bmax);  // finite: every block has a real key
-        const float corr = ex2(m[ii] - m_new);   // 0 on the first block (m = -inf)
+        // -inf while a row has seen no visible key (possible with a window):
+        // then exponents are taken against 0 and stay exactly 0. Without a
+        // window every block holds a real key for every row.
+        const float m_new = fmaxf(m[ii], bmax);
+        const float m_use = (kLocal && m_new == -INFINITY) ? 0.f : m_new;
+        const float corr = ex2(m[ii] - m_use);   // 0 while m = -inf
         float bsum = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const float p = ex2(s[ii][jj] - m_new);
+          const float p = ex2(s[ii][jj] - m_use);
           bsum += p;
           Ps[(ty + 16 * ii) * (kBN + 4) + tx + 16 * jj] = p;
         }
@@ -253,8 +276,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kFtThreads)
 fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                        const int32_t* __restrict__ cu, int32_t B, int32_t H, float scale_log2,
-                       T* __restrict__ out, float* __restrict__ lse, int32_t nsplit,
-                       int32_t chunk, float* __restrict__ part) {
+                       int32_t key_limit, T* __restrict__ out, float* __restrict__ lse,
+                       int32_t nsplit, int32_t chunk, float* __restrict__ part) {
   using S = FtShape<T, D>;
   constexpr int EPL = S::kEPL, LPK = S::kLPK, G = S::kGroups;
   constexpr int kWarps = kFtThreads / 32;
@@ -269,7 +292,9 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
     const int64_t ih = item / nsplit;
     const int32_t split = (int32_t)(item - ih * nsplit);
     const int32_t i = (int32_t)(ih / H), h = (int32_t)(ih - (int64_t)i * H);
-    const int32_t seq_start = __ldg(cu + i), seq_len = __ldg(cu + i + 1) - seq_start;
+    const int32_t seq_start = __ldg(cu + i);
+    // The query sits at position 0: with a window it sees keys 0 .. key_limit-1.
+    const int32_t seq_len = min(__ldg(cu + i + 1) - seq_start, key_limit);
     const int32_t key0 = split * chunk;
     const int32_t start = seq_start + key0;
     const int32_t len = max(0, min(chunk, seq_len - key0));  // keys of this chunk
@@ -388,9 +413,9 @@ __global__ void first_token_merge_kernel(const float* __restrict__ part, int32_t
 
 template <typename T, int D>
 pe_status launch_full(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                      int32_t H, float scale, void* out, float* lse, int64_t N, TilePlan plan,
-                      cudaStream_t stream) {
-  auto kernel = fwd_simt_kernel<T, D>;
+                      int32_t H, float scale, Window win, void* out, float* lse, int64_t N,
+                      TilePlan plan, cudaStream_t stream) {
+  auto kernel = win.active() ? fwd_simt_kernel<T, D, true> : fwd_simt_kernel<T, D, false>;
   const size_t smem = SimtShape<D>::kSmemBytes;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   int per_sm = 0;
@@ -398,24 +423,26 @@ pe_status launch_full(const void* q, const void* k, const void* v, const int32_t
   if (per_sm < 1) return PE_ERR_UNSUPPORTED;
   kernel<<<device_sm_count() * per_sm, kThreads, smem, stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, H,
-      scale * kLog2e, static_cast<T*>(out), lse, N, plan);
+      scale * kLog2e, win, static_cast<T*>(out), lse, N, plan);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }
 
 template <typename T, int D>
 pe_status launch_first(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                       int32_t H, int32_t S, float scale, void* out, float* lse, float* part,
-                       cudaStream_t stream) {
+                       int32_t H, int32_t S, float scale, Window win, void* out, float* lse,
+                       float* part, cudaStream_t stream) {
+  // With a window the query sees at most right + 1 keys.
+  const int32_t key_limit = win.right == kUnbounded ? S : min(S, win.right + 1);
   // Without room for chunk partials every sequence is a single chunk.
-  const int32_t nsplit = part ? first_token_splits(S) : 1;
+  const int32_t nsplit = part ? first_token_splits(key_limit) : 1;
   const int64_t cap = (int64_t)device_sm_count() * 16;
   int64_t blocks = (int64_t)B * H * nsplit;
   if (blocks > cap) blocks = cap;
   fwd_first_token_kernel<T, D><<<(unsigned)blocks, kFtThreads, 0, stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, H,
-      scale * kLog2e, static_cast<T*>(out), lse, nsplit, nsplit == 1 ? S : kFirstTokenChunk,
-      part);
+      scale * kLog2e, key_limit, static_cast<T*>(out), lse, nsplit,
+      nsplit == 1 ? key_limit : kFirstTokenChunk, part);
   PE_CUDA_TRY(cudaGetLastError());
   if (nsplit > 1) {
     int64_t mblocks = ceil_div((int64_t)B * H, 8);
@@ -429,11 +456,11 @@ pe_status launch_first(const void* q, const void* k, const void* v, const int32_
 
 template <typename T>
 pe_status dispatch_full(int D, const void* q, const void* k, const void* v, const int32_t* cu,
-                        int32_t B, int32_t H, float scale, void* out, float* lse, int64_t N,
-                        TilePlan plan, cudaStream_t stream) {
+                        int32_t B, int32_t H, float scale, Window win, void* out, float* lse,
+                        int64_t N, TilePlan plan, cudaStream_t stream) {
   switch (D) {
 #define PE_CASE(d) \
-  case d: return launch_full<T, d>(q, k, v, cu, B, H, scale, out, lse, N, plan, stream);
+  case d: return launch_full<T, d>(q, k, v, cu, B, H, scale, win, out, lse, N, plan, stream);
     PE_CASE(8) PE_CASE(16) PE_CASE(24) PE_CASE(32) PE_CASE(40) PE_CASE(48) PE_CASE(56)
     PE_CASE(64) PE_CASE(72) PE_CASE(80) PE_CASE(88) PE_CASE(96) PE_CASE(104) PE_CASE(112)
     PE_CASE(120) PE_CASE(128)
@@ -444,11 +471,11 @@ pe_status dispatch_full(int D, const void* q, const void* k, const void* v, cons
 
 template <typename T>
 pe_status dispatch_first(int D, const void* q, const void* k, const void* v, const int32_t* cu,
-                         int32_t B, int32_t H, int32_t S, float scale, void* out, float* lse,
-                         float* part, cudaStream_t stream) {
+                         int32_t B, int32_t H, int32_t S, float scale, Window win, void* out,
+                         float* lse, float* part, cudaStream_t stream) {
   switch (D) {
 #define PE_CASE(d) \
-  case d: return launch_first<T, d>(q, k, v, cu, B, H, S, scale, out, lse, part, stream);
+  case d: return launch_first<T, d>(q, k, v, cu, B, H, S, scale, win, out, lse, part, stream);
     PE_CASE(8) PE_CASE(16) PE_CASE(32) PE_CASE(64) PE_CASE(128)
 #undef PE_CASE
     default: return PE_ERR_UNSUPPORTED;
@@ -460,22 +487,24 @@ pe_status dispatch_first(int D, const void* q, const void* k, const void* v, con
 int simt_rows_per_tile() { return kBM; }
 
 pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
-                   const int32_t* cu, int32_t B, int32_t H, float scale, void* out, float* lse,
-                   int64_t N, TilePlan plan, cudaStream_t stream) {
+                   const int32_t* cu, int32_t B, int32_t H, float scale, Window win, void* out,
+                   float* lse, int64_t N, TilePlan plan, cudaStream_t stream) {
   if (dtype == PE_FP32)
-    return dispatch_full<float>(D, q, k, v, cu, B, H, scale, out, lse, N, plan, stream);
-  return dispatch_full<__nv_bfloat16>(D, q, k, v, cu, B, H, scale, out, lse, N, plan, stream);
+    return dispatch_full<float>(D, q, k, v, cu, B, H, scale, win, out, lse, N, plan, stream);
+  return dispatch_full<__nv_bfloat16>(D, q, k, v, cu, B, H, scale, win, out, lse, N, plan,
+                                      stream);
 }
 
 bool first_token_supported(int D) { return D == 8 || D == 16 || D == 32 || D == 64 || D == 128; }
 
 pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                           const int32_t* cu, int32_t B, int32_t H, int32_t S, float scale,
-                          void* out, float* lse, float* part, TilePlan /*plan*/,
+                          Window win, void* out, float* lse, float* part, TilePlan /*plan*/,
                           cudaStream_t stream) {
   if (dtype == PE_FP32)
-    return dispatch_first<float>(D, q, k, v, cu, B, H, S, scale, out, lse, part, stream);
-  return dispatch_first<__nv_bfloat16>(D, q, k, v, cu, B, H, S, scale, out, lse, part, stream);
+    return dispatch_first<float>(D, q, k, v, cu, B, H, S, scale, win, out, lse, part, stream);
+  return dispatch_first<__nv_bfloat16>(D, q, k, v, cu, B, H, S, scale, win, out, lse, part,
+                                       stream);
 }
 
 }  // namespace pe

@@ -25,7 +25,9 @@
 //               epilogue (normalise, store the real rows, log-sum-exp).
 // A work item is (sequence, head, pair of 128-row query tiles); both tiles
 // share every K/V block, and while one tile's softmax runs the tensor cores
-// work on the other tile. Keys past the sequence end are masked to -inf;
+// work on the other tile. With local attention (a window of key positions
+// around each query position) an item visits only the key blocks its rows can
+// see, and the softmax masks each row to its window. Keys past the sequence end are masked to -inf;
 // query rows past it are computed but never stored. TMA zero-fills rows
 // beyond the packed buffer.
 //
@@ -86,11 +88,27 @@ struct FwdParams {
   float* lse;
   int64_t lse_stride;
   TilePlan plan;
+  Window win;
   DeviceStatus* status;
 };
 
 // Where a wait gave up (recorded in the status word's detail field).
 enum WaitSite { kSiteProducer = 1, kSiteMma = 2, kSiteSoftmax = 3 };
+
+// Key blocks [j0, j0 + nkv) that the real rows r0 .. min(r0 + 256, len) - 1
+// of an item can see (every block of the sequence without a window).
+template <bool kLocal>
+__device__ __forceinline__ void item_blocks(const FwdParams& p, int32_t len, int32_t r0,
+                                            int32_t& j0, int32_t& nkv) {
+  if (!kLocal) {
+    j0 = 0;
+    nkv = (len + kRows - 1) / kRows;
+    return;
+  }
+  const int32_t last = min(r0 + kPairRows, len) - 1;
+  j0 = window_lo(p.win, r0) / kRows;
+  nkv = window_hi(p.win, last, len) / kRows - j0 + 1;
+}
 
 __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item& it) {
   int32_t seq, local;
@@ -103,6 +121,10 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
   it.pad = 0;
 }
 
+// kLocal selects the local-attention variant (window masks, block ranges and
+// the guard for rows that have seen no visible key); full attention compiles
+// without any of it.
+template <bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -177,7 +199,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int32_t len = __ldg(p.cu + it.seq + 1) - start;
         const int32_t r0 = it.pair * kPairRows;
         const int ntiles = (len - r0 > kRows) ? 2 : 1;
-        const int32_t nkv = (len + kRows - 1) / kRows;
+        int32_t j0, nkv;
+        item_blocks<kLocal>(p, len, r0, j0, nkv);
         const int32_t x = it.head * kD;
         if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
                        kSiteProducer)) {
@@ -196,14 +219,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
-          tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x, start + j * kRows);
+          tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x,
+                      start + (j0 + j) * kRows);
           pending_k[s] = (int)ph;
           if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
-          tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x, start + j * kRows);
+          tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x,
+                      start + (j0 + j) * kRows);
           pending_v[s] = (int)ph;
         }
       }
@@ -236,7 +261,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
       const int32_t r0 = it.pair * kPairRows;
       const int ntiles = (len - r0 > kRows) ? 2 : 1;
-      const int32_t nkv = (len + kRows - 1) / kRows;
+      int32_t j0, nkv;
+      item_blocks<kLocal>(p, len, r0, j0, nkv);
       if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
       for (int32_t j = 0; j < nkv && ok; ++j) {
         const uint32_t c = kv_no + j;
@@ -291,7 +317,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
       const int32_t r0 = it.pair * kPairRows;
       const int ntiles = (len - r0 > kRows) ? 2 : 1;
-      const int32_t nkv = (len + kRows - 1) / kRows;
+      int32_t j0, nkv;
+      item_blocks<kLocal>(p, len, r0, j0, nkv);
       if (t >= ntiles) {                           // tile 1 of a lone tile: nothing to do
         kv_no += nkv;
         continue;
@@ -345,7 +372,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
       const int32_t r0 = it.pair * kPairRows + t * kRows;
       if (r0 >= len) continue;                   // this tile of the pair is empty
-      const int32_t nkv = (len + kRows - 1) / kRows;
+      int32_t j0, nkv;
+      item_blocks<kLocal>(p, len, it.pair * kPairRows, j0, nkv);
+      // This row's visible key positions (local attention).
+      const int32_t vis_lo = kLocal ? window_lo(p.win, r0 + row) : 0;
+      const int32_t vis_hi = kLocal ? window_hi(p.win, r0 + row, len) : len - 1;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int32_t j = 0; j < nkv; ++j) {
@@ -364,8 +395,19 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.s_free[t]));
-        const int32_t kv_valid = len - j * kRows;  // > 0; columns at or past it are masked
-        if (kv_valid < kRows) {                    // only a sequence's last key block
+        const int32_t kb = (j0 + j) * kRows;      // key position of column 0
+        const int32_t kv_valid = len - kb;         // > 0; columns at or past it are masked
+        if (kLocal) {
+          // Columns outside [vis_lo, vis_hi] (which also ends before len).
+          const int32_t clo = vis_lo - kb, chi = vis_hi - kb;
+          if (__any_sync(0xffffffffu, clo > 0 || chi < kRows - 1)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (32 * c + e < clo || 32 * c + e > chi) sr[c][e] = 0xff800000u;  // -inf
+          }
+        } else if (kv_valid < kRows) {             // only a sequence's last key block
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -391,7 +433,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float alpha = grow ? ex2(m - m_new) : 1.f;  // 0 on the first block
         // Exponents first, into registers: the wait for P_t(j-1) V below then
         // hides behind this work instead of delaying it.
-        const uint64_t c2 = f2(scale_log2, scale_log2), nm2 = f2(-m_new, -m_new);
+        // With a window a row may have seen no visible key yet (m_new = -inf):
+        // its exponents are then taken against 0 and stay exactly 0. Without
+        // one every block holds a visible key for every row.
+        const float m_use = (kLocal && m_new == -INFINITY) ? 0.f : m_new;
+        const uint64_t c2 = f2(scale_log2, scale_log2), nm2 = f2(-m_use, -m_use);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[4][16];
 #pragma unroll
@@ -515,15 +561,16 @@ pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H) {
 int sm103_fwd_rows_per_item() { return kPairRows; }
 
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                    int32_t H, int64_t N, float scale, void* out, float* lse, TilePlan plan,
-                    DeviceStatus* status, cudaStream_t stream) {
+                    int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
+                    TilePlan plan, DeviceStatus* status, cudaStream_t stream) {
   PE_TRY(get_encoder());
   CUtensorMap mq, mk, mv;
   PE_TRY(make_map(&mq, q, N, H));
   PE_TRY(make_map(&mk, k, N, H));
   PE_TRY(make_map(&mv, v, N, H));
   const size_t smem = sizeof(Smem) + 1024;
-  PE_CUDA_TRY(cudaFuncSetAttribute(fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = win.active() ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
+  PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
   FwdParams prm;
   prm.cu = cu;
@@ -534,8 +581,9 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.lse = lse;
   prm.lse_stride = N;
   prm.plan = plan;
+  prm.win = win;
   prm.status = status;
-  fwd_sm103_kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, prm);
+  kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

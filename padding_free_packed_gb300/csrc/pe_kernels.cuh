@@ -8,20 +8,21 @@ namespace pe {
 // CUDA-core forward (fp32 any head_dim; bf16 head_dims without a tensor-core kernel).
 int simt_rows_per_tile();
 pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
-                   const int32_t* cu, int32_t B, int32_t H, float scale, void* out, float* lse,
-                   int64_t N, TilePlan plan, cudaStream_t stream);
+                   const int32_t* cu, int32_t B, int32_t H, float scale, Window win, void* out,
+                   float* lse, int64_t N, TilePlan plan, cudaStream_t stream);
 
 // First-token query (one query row per sequence).
 bool first_token_supported(int D);
+// With a window the query at position 0 sees keys 0 .. win.right.
 pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                           const int32_t* cu, int32_t B, int32_t H, int32_t S, float scale,
-                          void* out, float* lse, float* part, TilePlan plan,
+                          Window win, void* out, float* lse, float* part, TilePlan plan,
                           cudaStream_t stream);
 
 // CUDA-core backward; delta is [H, Nq] fp32 scratch.
 pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,
-                   int first_token, const void* out, const float* lse, const void* dout,
+                   int first_token, Window win, const void* out, const float* lse, const void* dout,
                    void* dq, void* dk, void* dv, float* delta, TilePlan plan,
                    cudaStream_t stream);
 
@@ -29,8 +30,8 @@ pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
 // 128-row query tiles, so the tile plan is built with sm103_fwd_rows_per_item().
 int sm103_fwd_rows_per_item();
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                    int32_t H, int64_t N, float scale, void* out, float* lse, TilePlan plan,
-                    DeviceStatus* status, cudaStream_t stream);
+                    int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
+                    TilePlan plan, DeviceStatus* status, cudaStream_t stream);
 
 // Delta[h, r] = dO_r . O_r (bf16, head_dim 64) into [H, Nq] fp32.
 pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dout, int64_t Nq,
@@ -39,7 +40,8 @@ pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dou
 // Tensor-core backward, bf16, head_dim 64, full mode (sm_103a): a key pass
 // (dK, dV) and a query pass (dQ), each with its own tile plan over 128-row blocks.
 pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
-                    int32_t H, int64_t N, float scale, const float* lse, const void* dout,
+                    int32_t H, int64_t N, float scale, Window win, const float* lse,
+                    const void* dout,
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
                     DeviceStatus* status, cudaStream_t stream);
 

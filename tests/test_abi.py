@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.pe_abi_version() == 1
+    assert lib.pe_abi_version() == 2
     for code in range(8):
         assert lib.pe_status_string(code)
     assert lib.pe_status_string(0) == b"ok"
