@@ -85,23 +85,24 @@ struct BwdParams {
   DeviceStatus* status;
 };
 
-// Streaming blocks [i0, i0 + nblk) of the item block `blk` of a sequence of
-// len rows: in the key pass the query blocks whose rows see one of the item's
-// keys, in the query pass the key blocks that one of the item's rows sees
-// (every block without a window). Never empty: a key is visible from its own
-// position.
+// The nblk streaming blocks of 128 rows of the item block `blk` of a sequence
+// of len rows, the first one starting at row position org: in the key pass the
+// query rows that see one of the item's keys, in the query pass the keys that
+// one of the item's rows sees (the whole sequence without a window; with one
+// the blocks start at the first row of the band, as TMA rows need no
+// alignment). Never empty: a key is visible from its own position.
 template <bool kKeyPass, bool kLocal>
 __device__ __forceinline__ void stream_blocks(const BwdParams& p, int32_t len, int32_t blk,
-                                              int32_t& i0, int32_t& nblk) {
+                                              int32_t& org, int32_t& nblk) {
   if (!kLocal) {
-    i0 = 0;
+    org = 0;
     nblk = (len + kRows - 1) / kRows;
     return;
   }
   const Window w = kKeyPass ? Window{p.win.right, p.win.left} : p.win;
   const int32_t first = blk * kRows, last = min(first + kRows, len) - 1;
-  i0 = window_lo(w, first) / kRows;
-  nblk = window_hi(w, last, len) / kRows - i0 + 1;
+  org = window_lo(w, first);
+  nblk = (window_hi(w, last, len) - org) / kRows + 1;
 }
 
 enum WaitSite { kSiteProducer = 11, kSiteT = 12, kSiteAcc = 13, kSiteEw = 14 };
@@ -211,8 +212,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.seq < 0) break;
       const int32_t start = __ldg(p.cu + it.seq);
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      int32_t i0, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
+      int32_t org, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
       const int32_t x = it.head * kD;
       if (!warp_wait(smem_u32(&S.st_empty), (item_no & 1) ^ 1, abort_flag, p.status,
                      kSiteProducer)) {
@@ -235,11 +236,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (kKeyPass) {
           // lse*log2e and Delta of the block's 128 queries; +inf / 0 past the
           // sequence end, so those columns get P = 0.
-          const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + (i0 + i) * kRows;
+          const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + org + i * kRows;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int r = lane + 32 * u;
-            const bool in = (i0 + i) * kRows + r < len;
+            const bool in = org + i * kRows + r < len;
             S.vec[s][0][r] = in ? __ldg(p.lse + base + r) * kLog2e : INFINITY;
             S.vec[s][1][r] = in ? __ldg(p.delta + base + r) : 0.f;
           }
@@ -248,9 +249,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) {
           mbar_arrive_expect_tx(smem_u32(&S.u_full[s]), 2 * kTileBytes);
           tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x,
-                      start + (i0 + i) * kRows);
+                      start + org + i * kRows);
           tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x,
-                      start + (i0 + i) * kRows);
+                      start + org + i * kRows);
         }
         if (kKeyPass) mbar_arrive(smem_u32(&S.u_full[s]));
         pending_u[s] = static_cast<int>(ph);
@@ -274,8 +275,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!read_item(item_no, it, kSiteT)) break;
       if (it.seq < 0) break;
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      int32_t i0, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
+      int32_t org, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
       if (!warp_wait(smem_u32(&S.st_full), item_no & 1, abort_flag, p.status, kSiteT)) break;
       for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_t) {
         const int s = u_no % kStages;
@@ -316,8 +317,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!read_item(item_no, it, kSiteAcc)) break;
       if (it.seq < 0) break;
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      int32_t i0, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
+      int32_t org, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
       // The previous item's accumulators must have been read by the epilogue.
       if (!warp_wait(smem_u32(&S.o_free), (item_no & 1) ^ 1, abort_flag, p.status, kSiteAcc))
         break;
@@ -358,8 +359,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.seq < 0) break;
       const int32_t start = __ldg(p.cu + it.seq);
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      int32_t i0, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, i0, nb);
+      int32_t org, nb;
+      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
       const int32_t r0 = it.blk * kRows;
       // Streaming positions this row pairs with inside the window: the queries
       // that see this key (key pass) or the keys this query sees (query pass).
@@ -394,9 +395,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           tc_fence_after();
         }
-        const int32_t col_valid = len - (i0 + i) * kRows - 64 * h;  // query pass: valid keys in this half
-        const int32_t clo = vis_lo - (i0 + i) * kRows - 64 * h;  // window, relative to this half
-        const int32_t chi = vis_hi - (i0 + i) * kRows - 64 * h;
+        const int32_t col0_pos = org + i * kRows + 64 * h;  // row position of this half's column 0
+        const int32_t col_valid = len - col0_pos;           // query pass: valid keys in this half
+        const int32_t clo = vis_lo - col0_pos, chi = vis_hi - col0_pos;  // window, same origin
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int col0 = 64 * h + 32 * c;

@@ -95,19 +95,41 @@ struct FwdParams {
 // Where a wait gave up (recorded in the status word's detail field).
 enum WaitSite { kSiteProducer = 1, kSiteMma = 2, kSiteSoftmax = 3 };
 
-// Key blocks [j0, j0 + nkv) that the real rows r0 .. min(r0 + 256, len) - 1
-// of an item can see (every block of the sequence without a window).
+// The key blocks of an item: nkv blocks of 128 keys starting at key position
+// kb0, and the blocks [lo[t], hi[t]] that query tile t uses. Without a window
+// that is the whole sequence for both tiles. With one, the blocks start at the
+// first key of the item's window band (TMA rows need no alignment) and each
+// tile uses only the blocks its own rows can see.
+struct ItemRange {
+  int32_t kb0, nkv, lo0, hi0, lo1, hi1;   // (lo0, hi0) for tile 0, (lo1, hi1) for tile 1
+  __device__ int32_t lo(int t) const { return t ? lo1 : lo0; }
+  __device__ int32_t hi(int t) const { return t ? hi1 : hi0; }
+  __device__ bool uses(int t, int32_t j) const { return j >= lo(t) && j <= hi(t); }
+};
+
 template <bool kLocal>
-__device__ __forceinline__ void item_blocks(const FwdParams& p, int32_t len, int32_t r0,
-                                            int32_t& j0, int32_t& nkv) {
+__device__ __forceinline__ ItemRange item_range(const FwdParams& p, int32_t len, int32_t r0) {
+  ItemRange ir;
   if (!kLocal) {
-    j0 = 0;
-    nkv = (len + kRows - 1) / kRows;
-    return;
+    ir.kb0 = 0;
+    ir.nkv = (len + kRows - 1) / kRows;
+    ir.lo0 = ir.lo1 = 0;
+    ir.hi0 = ir.hi1 = ir.nkv - 1;
+    return ir;
   }
+  ir.kb0 = window_lo(p.win, r0);
   const int32_t last = min(r0 + kPairRows, len) - 1;
-  j0 = window_lo(p.win, r0) / kRows;
-  nkv = window_hi(p.win, last, len) / kRows - j0 + 1;
+  ir.nkv = (window_hi(p.win, last, len) - ir.kb0) / kRows + 1;
+  ir.lo0 = 0;                        // tile 0 starts the band
+  ir.hi0 = (window_hi(p.win, min(r0 + kRows, len) - 1, len) - ir.kb0) / kRows;
+  if (r0 + kRows < len) {
+    ir.lo1 = (window_lo(p.win, r0 + kRows) - ir.kb0) / kRows;
+    ir.hi1 = ir.nkv - 1;             // tile 1 ends it
+  } else {                           // no tile 1 in this item
+    ir.lo1 = 1;
+    ir.hi1 = 0;
+  }
+  return ir;
 }
 
 __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item& it) {
@@ -150,7 +172,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(smem_u32(&S.k_full[s]), 1);
       mbar_init(smem_u32(&S.v_full[s]), 1);
       mbar_init(smem_u32(&S.k_empty[s]), 1);       // the QK issuer, after both tiles' QK
-      mbar_init(smem_u32(&S.v_empty[s]), 2);       // each PV issuer (tile 0's twice for a lone tile)
+      mbar_init(smem_u32(&S.v_empty[s]), 2);       // each PV issuer, once per block
     }
     for (int w = 0; w < kIssueWarps; ++w) mbar_init(smem_u32(&S.drain[w]), 1);
     S.abort_flag = 0;
@@ -199,8 +221,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int32_t len = __ldg(p.cu + it.seq + 1) - start;
         const int32_t r0 = it.pair * kPairRows;
         const int ntiles = (len - r0 > kRows) ? 2 : 1;
-        int32_t j0, nkv;
-        item_blocks<kLocal>(p, len, r0, j0, nkv);
+        const ItemRange ir = item_range<kLocal>(p, len, r0);
+        const int32_t nkv = ir.nkv;
         const int32_t x = it.head * kD;
         if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
                        kSiteProducer)) {
@@ -220,7 +242,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
           tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x,
-                      start + (j0 + j) * kRows);
+                      start + ir.kb0 + j * kRows);
           pending_k[s] = (int)ph;
           if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
             ok = false;
@@ -228,7 +250,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
           tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x,
-                      start + (j0 + j) * kRows);
+                      start + ir.kb0 + j * kRows);
           pending_v[s] = (int)ph;
         }
       }
@@ -261,8 +283,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
       const int32_t r0 = it.pair * kPairRows;
       const int ntiles = (len - r0 > kRows) ? 2 : 1;
-      int32_t j0, nkv;
-      item_blocks<kLocal>(p, len, r0, j0, nkv);
+      const ItemRange ir = item_range<kLocal>(p, len, r0);
+      const int32_t nkv = ir.nkv;
       if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
       for (int32_t j = 0; j < nkv && ok; ++j) {
         const uint32_t c = kv_no + j;
@@ -274,6 +296,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         const uint32_t k_addr = smem_u32(S.k[s]);
         for (int t = 0; t < ntiles; ++t) {
+          if (kLocal && !ir.uses(t, j)) continue;  // outside every window of tile t
           // The softmax must have read the previous S_t before it is overwritten.
           if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag,
                                         p.status, kSiteMma)) {
@@ -317,21 +340,26 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
       const int32_t r0 = it.pair * kPairRows;
       const int ntiles = (len - r0 > kRows) ? 2 : 1;
-      int32_t j0, nkv;
-      item_blocks<kLocal>(p, len, r0, j0, nkv);
-      if (t >= ntiles) {                           // tile 1 of a lone tile: nothing to do
-        kv_no += nkv;
-        continue;
-      }
-      // With a single tile, tile 0's warp also makes tile 1's arrival on the
-      // V release barrier.
-      const int releases = ntiles == 1 ? 2 : 1;
+      const ItemRange ir = item_range<kLocal>(p, len, r0);
+      const int32_t nkv = ir.nkv;
       for (int32_t j = 0; j < nkv; ++j) {
         const uint32_t c = kv_no + j;
         const int s = c % kStages;
+        // Both PV warps take part in every V stage phase: each waits for every
+        // block and releases it once, so the producer can never refill a stage
+        // that either warp has not yet seen (which would make a parity wait
+        // match a later phase).
         if (!warp_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
-                       kSiteMma) ||
-            !warp_wait(smem_u32(&S.p_full[t]), n_pv & 1, abort_flag, p.status, kSiteMma)) {
+                       kSiteMma)) {
+          ok = false;
+          break;
+        }
+        if (t >= ntiles || !ir.uses(t, j)) {       // this tile does not read V_j
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&S.v_empty[s]));
+          continue;
+        }
+        if (!warp_wait(smem_u32(&S.p_full[t]), n_pv & 1, abort_flag, p.status, kSiteMma)) {
           ok = false;
           break;
         }
@@ -341,11 +369,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int kk = 0; kk < kRows / 16; ++kk)
           mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
                       smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+                      (j > ir.lo(t) || kk > 0) ? 1u : 0u);
         tc_commit_warp(smem_u32(&S.pv_done[t]));
-        if (j + 1 == nkv) tc_commit_warp(smem_u32(&S.o_full[t]));
+        if (j == ir.hi(t)) tc_commit_warp(smem_u32(&S.o_full[t]));
         ++n_pv;
-        for (int r = 0; r < releases; ++r) tc_commit_warp(smem_u32(&S.v_empty[s]));
+        tc_commit_warp(smem_u32(&S.v_empty[s]));
       }
       kv_no += nkv;
     }
@@ -372,14 +400,14 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
       const int32_t r0 = it.pair * kPairRows + t * kRows;
       if (r0 >= len) continue;                   // this tile of the pair is empty
-      int32_t j0, nkv;
-      item_blocks<kLocal>(p, len, it.pair * kPairRows, j0, nkv);
+      const ItemRange ir = item_range<kLocal>(p, len, it.pair * kPairRows);
       // This row's visible key positions (local attention).
       const int32_t vis_lo = kLocal ? window_lo(p.win, r0 + row) : 0;
       const int32_t vis_hi = kLocal ? window_hi(p.win, r0 + row, len) : len - 1;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int32_t j = 0; j < nkv; ++j) {
+      for (int32_t j = ir.lo(t); j <= ir.hi(t); ++j) {
+        const bool first_blk = j == ir.lo(t);
         if (!warp_wait(smem_u32(&S.s_full[t]), s_cnt & 1, abort_flag, p.status, kSiteSoftmax)) {
           ok = false;
           break;
@@ -395,7 +423,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.s_free[t]));
-        const int32_t kb = (j0 + j) * kRows;      // key position of column 0
+        const int32_t kb = ir.kb0 + j * kRows;     // key position of column 0
         const int32_t kv_valid = len - kb;         // > 0; columns at or past it are masked
         if (kLocal) {
           // Columns outside [vis_lo, vis_hi] (which also ends before len).
@@ -461,7 +489,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         f2_split(acc[3], s6, s7);
         l = l * alpha + (((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)));
         m = m_new;
-        if (j > 0) {
+        if (!first_blk) {
           // P_t(j-1) V must have finished before P_t is overwritten or O_t rescaled.
           if (!warp_wait(smem_u32(&S.pv_done[t]), (s_cnt - 2) & 1, abort_flag, p.status,
                          kSiteSoftmax)) {
@@ -473,7 +501,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_st16(lane_base + col_p(t) + 16 * c, pk[c]);
         // O holds P(j-1) V(j-1): rescale it when some row's maximum moved.
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        if (!first_blk && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             uint32_t o[32];

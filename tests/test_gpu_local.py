@@ -140,3 +140,40 @@ def test_local64_long_documents_sampled_rows():
     check(got, ref, "bf16", "local-64 long documents")
     got_lse = lse[torch.from_numpy(hs).to(DEV), torch.from_numpy(rows).to(DEV)]
     assert float(np.abs(to64(got_lse) - ref_lse).max()) <= 2e-3
+
+
+@pytest.mark.parametrize("workload,window", [("longdoc_bf16", (64, 64)), ("longdoc_bf16", (3, 200)),
+                                             ("train_bf16", (64, 64))])
+def test_local_full_workload_pipeline_completes(workload, window):
+    """Whole workloads (many items per CTA, so the K/V rings wrap many times,
+    and single-tile items next to two-tile ones): every pipeline wait completes
+    (device status clear) and sampled rows match the oracle, forward and, for
+    the training workload, backward."""
+    wl = workloads.WORKLOADS[workload]
+    x = workloads.make_inputs(workload)
+    _, cu, n = oracle.pack_sequences(x.lengths, wl.max_seq_len)
+    q, k, v = (t.to(DEV) for t in (x.q, x.k, x.v))
+    cu_d = torch.from_numpy(cu).to(DEV)
+    b = len(x.lengths)
+    ws = torch.empty(pe.attention_workspace_bytes(torch.bfloat16, b, n, wl.num_heads, wl.head_dim,
+                                                  wl.max_seq_len, backward=True),
+                     dtype=torch.uint8, device=DEV)
+    out, lse = pe.pe_packed_attention_fwd_local(q, k, v, cu_d, wl.max_seq_len, window[0],
+                                                window[1], wl.scale, need_lse=True, workspace=ws)
+    assert pe.pe_read_device_status(ws) == 0
+    rng = np.random.default_rng(41)
+    rows = np.concatenate([rng.integers(0, n, 300), cu[:-1], cu[1:] - 1]).astype(np.int64)
+    hs = rng.integers(0, wl.num_heads, rows.shape[0]).astype(np.int64)
+    ref, _ = oracle.attention_fwd_rows(x.q, x.k, x.v, cu, wl.scale, False, rows, hs,
+                                       window=window)
+    got = out[torch.from_numpy(rows).to(DEV), torch.from_numpy(hs).to(DEV)]
+    check(got, ref, "bf16", f"{workload} local {window}")
+    if wl.backward:
+        do = x.dout.to(DEV)
+        dq, dk, dv = pe.pe_packed_attention_bwd_local(do, q, k, v, out, lse, cu_d,
+                                                      wl.max_seq_len, window[0], window[1],
+                                                      wl.scale, workspace=ws)
+        assert pe.pe_read_device_status(ws) == 0
+        rq, rk, rv = oracle.attention_bwd(x.q, x.k, x.v, x.dout, cu, wl.scale, window=window)
+        for name, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            check_grad(got, want, "bf16", f"{workload} local {name}")
