@@ -76,6 +76,11 @@ def _load():
                                                 ctypes.c_double, ctypes.c_int, i64, i64, dp, dp,
                                                 dp, ctypes.c_int]
         lib.orc_attention_bwd_local.restype = ctypes.c_int
+        lib.orc_pack_document_ids.argtypes = [i32p, i64, i64, i64p, i32p, i64p, i64p]
+        lib.orc_pack_document_ids.restype = ctypes.c_int
+        lib.orc_flatten_packed_metadata.argtypes = [i64p, i32p, i64, i64, i64, i64p, i32p, i64p,
+                                                    i64p]
+        lib.orc_flatten_packed_metadata.restype = ctypes.c_int
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = ctypes.c_int
         _lib = lib
@@ -120,6 +125,49 @@ def pack_sequences(lengths, max_seq_len: int, want_index: bool = True):
     if rc != 0:
         raise OracleError(rc)
     return flat[: n.value].copy(), cu, int(n.value)
+
+
+def pack_document_ids(ids):
+    """Indexed packing mask [B, S] (document i of a row marked i, 0 = padding)
+    -> (flat_index int64 [N], cu_seqlens int32 [D+1])."""
+    lib = _load()
+    ids = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    b, s = ids.shape
+    n, d = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib.orc_pack_document_ids(_ptr(ids, ctypes.c_int32), b, s, None, None,
+                                   ctypes.byref(n), ctypes.byref(d))
+    if rc != 0:
+        raise OracleError(rc)
+    flat = np.zeros(max(n.value, 1), dtype=np.int64)
+    cu = np.zeros(d.value + 1, dtype=np.int32)
+    rc = lib.orc_pack_document_ids(_ptr(ids, ctypes.c_int32), b, s, _ptr(flat, ctypes.c_int64),
+                                   _ptr(cu, ctypes.c_int32), ctypes.byref(n), ctypes.byref(d))
+    if rc != 0:
+        raise OracleError(rc)
+    return flat[: n.value].copy(), cu
+
+
+def flatten_packed_metadata(token_indices, row_cu_seqlens, sequence_length: int):
+    """Row-local token indices [B, S] and row-local cumulative lengths [B, M+1]
+    (both -1 padded) -> (flat_index int64 [N], cu_seqlens int32 [D+1])."""
+    lib = _load()
+    tok = np.ascontiguousarray(np.asarray(token_indices, dtype=np.int64))
+    rcu = np.ascontiguousarray(np.asarray(row_cu_seqlens, dtype=np.int32))
+    b, s = tok.shape
+    assert s == int(sequence_length) and rcu.shape[0] == b
+    n, d = ctypes.c_int64(0), ctypes.c_int64(0)
+    args = (_ptr(tok, ctypes.c_int64), _ptr(rcu, ctypes.c_int32), b, s, rcu.shape[1])
+    rc = lib.orc_flatten_packed_metadata(*args, None, None, ctypes.byref(n), ctypes.byref(d))
+    if rc != 0:
+        raise OracleError(rc)
+    flat = np.zeros(max(n.value, 1), dtype=np.int64)
+    cu = np.zeros(d.value + 1, dtype=np.int32)
+    rc = lib.orc_flatten_packed_metadata(*args, _ptr(flat, ctypes.c_int64),
+                                         _ptr(cu, ctypes.c_int32), ctypes.byref(n),
+                                         ctypes.byref(d))
+    if rc != 0:
+        raise OracleError(rc)
+    return flat[: n.value].copy(), cu
 
 
 def gather_rows(padded_rows: np.ndarray, flat_index: np.ndarray) -> np.ndarray:

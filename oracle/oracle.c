@@ -86,6 +86,92 @@ int orc_pack_sequences(const int32_t* lengths, int64_t B, int64_t S,
   return ORC_OK;
 }
 
+/* ------------------------------------------------------------------------- */
+/* Batch-major packed rows (several documents per padded row), page            */
+/* "nemo_automodel.components.models.common.packing":                         */
+/*  - is_indexed_packed_mask: an indexed packing mask marks document i of a    */
+/*    row (1-based) with i and padding with 0, e.g. [1,1,1,2,2,3,3,0,0].       */
+/*  - flatten_packed_sequence_metadata: row-local token indices [B, S] and     */
+/*    row-local cumulative lengths [B, M+1], both -1 padded, become one flat   */
+/*    token stream (indices into the padded [B, S] layout) and flat            */
+/*    cu_seqlens; inconsistent layouts, boundaries or token counts are errors. */
+/* Readings: padding is trailing in both layouts; documents are non-empty and  */
+/* numbered 1, 2, ... in order within a row; row-local boundaries start at 0,  */
+/* increase strictly and end at the row's token count; row-local token indices */
+/* lie in [0, S). Rows follow each other in the flat stream.                   */
+/* ------------------------------------------------------------------------- */
+
+/* ids: [B][S]. Outputs (nullable) flat_index [N] = i*S + j for every nonzero */
+/* ids[i][j] in row-major order, cu [D+1] with a boundary wherever a document */
+/* starts, and the totals N and D. */
+int orc_pack_document_ids(const int32_t* ids, int64_t B, int64_t S, int64_t* flat_index,
+                          int32_t* cu, int64_t* num_tokens, int64_t* num_docs) {
+  if (B < 0 || S < 1) return ORC_INVALID;
+  int64_t n = 0, d = 0;
+  for (int64_t i = 0; i < B; ++i) {
+    int32_t prev = 0;
+    for (int64_t j = 0; j < S; ++j) {
+      const int32_t id = ids[i * S + j];
+      if (id < 0) return ORC_INVALID;
+      if (id == 0) {                     /* padding: nothing may follow it */
+        prev = -1;
+        continue;
+      }
+      if (prev < 0) return ORC_INVALID;  /* a document after padding */
+      if (id == prev + 1) {              /* a new document starts here */
+        if (cu) cu[d] = (int32_t)n;
+        ++d;
+      } else if (id != prev) {
+        return ORC_INVALID;              /* skipped or repeated document number */
+      }
+      if (flat_index) flat_index[n] = i * S + j;
+      ++n;
+      if (n >= ((int64_t)1 << 31)) return ORC_OVERFLOW;
+      prev = id;
+    }
+  }
+  if (cu) cu[d] = (int32_t)n;
+  *num_tokens = n;
+  *num_docs = d;
+  return ORC_OK;
+}
+
+/* tok: [B][S] row-local token indices, -1 padded; row_cu: [B][M1] row-local  */
+/* cumulative lengths, -1 padded. Outputs as above. */
+int orc_flatten_packed_metadata(const int64_t* tok, const int32_t* row_cu, int64_t B, int64_t S,
+                                int64_t M1, int64_t* flat_index, int32_t* cu,
+                                int64_t* num_tokens, int64_t* num_docs) {
+  if (B < 0 || S < 1 || M1 < 1) return ORC_INVALID;
+  int64_t n = 0, d = 0;
+  for (int64_t i = 0; i < B; ++i) {
+    int64_t nb = 0;                       /* tokens of row i */
+    for (int64_t j = 0; j < S; ++j) {
+      const int64_t t = tok[i * S + j];
+      if (t == -1) continue;
+      if (t < 0 || t >= S || nb != j) return ORC_INVALID;  /* bad index, or padding not trailing */
+      if (flat_index) flat_index[n + nb] = i * S + t;
+      ++nb;
+    }
+    const int32_t* rc = row_cu + i * M1;
+    if (rc[0] != 0) return ORC_INVALID;
+    int64_t k = 1;
+    for (; k < M1 && rc[k] != -1; ++k) {
+      if (rc[k] <= rc[k - 1]) return ORC_INVALID;       /* empty or decreasing document */
+      if (cu) cu[d] = (int32_t)(n + rc[k - 1]);
+      ++d;
+    }
+    if (rc[k - 1] != nb) return ORC_INVALID;             /* boundaries disagree with tokens */
+    for (; k < M1; ++k)
+      if (rc[k] != -1) return ORC_INVALID;               /* padding not trailing */
+    n += nb;
+    if (n >= ((int64_t)1 << 31)) return ORC_OVERFLOW;
+  }
+  if (cu) cu[d] = (int32_t)n;
+  *num_tokens = n;
+  *num_docs = d;
+  return ORC_OK;
+}
+
 /* grid.flatten()[flat_index]: packed row t is padded row flat_index[t]. */
 void orc_gather_rows(const uint8_t* padded, const int64_t* flat_index, int64_t N,
                      int64_t row_bytes, uint8_t* packed) {

@@ -477,6 +477,109 @@ def test_local_backward_matches_finite_differences():
         np.testing.assert_allclose(g, fd, rtol=0, atol=2e-8, err_msg=name)
 
 
+# --------------------------------------------------------------------------- packed-row metadata
+# Page "nemo_automodel.components.models.common.packing": indexed packing masks
+# (document i of a row marked i, 0 = padding) and
+# flatten_packed_sequence_metadata (row-local token indices and cumulative
+# lengths, -1 padded, to one flat stream).
+
+def test_indexed_mask_worked_example(golden):
+    g = golden("indexed_packing_mask_example.txt")
+    flat, cu = oracle.pack_document_ids([g["row"]])
+    assert flat.tolist() == g["flat_index"] and cu.tolist() == g["cu_seqlens"]
+    flat2, cu2 = oracle.flatten_packed_metadata([g["row_token_indices"]], [g["row_cu_seqlens"]],
+                                                g["sequence_length"][0])
+    assert flat2.tolist() == g["flat_index"] and cu2.tolist() == g["cu_seqlens"]
+
+
+def _packed_rows(seed, b=6, s=40, max_docs=5, sparse=False):
+    """Rows built from random document lengths (numpy only): the id mask, the
+    two NeMo-style row-local layouts, and the flat outputs they stand for."""
+    rng = np.random.default_rng(seed)
+    ids = np.zeros((b, s), np.int32)
+    tok = np.full((b, s), -1, np.int64)
+    rcu = np.full((b, max_docs + 1), -1, np.int32)
+    flat, cu, total = [], [0], 0
+    for i in range(b):
+        docs = []
+        room = s
+        for _ in range(int(rng.integers(0, max_docs + 1))):
+            if room == 0:
+                break
+            docs.append(int(rng.integers(1, min(room, 12) + 1)))
+            room -= docs[-1]
+        n = sum(docs)
+        ids[i, :n] = np.repeat(np.arange(1, len(docs) + 1), docs)
+        # Row-local positions: the first n positions, or (sparse) n sorted distinct ones.
+        pos = np.sort(rng.choice(s, n, replace=False)) if sparse else np.arange(n)
+        tok[i, :n] = pos
+        rcu[i, :len(docs) + 1] = np.concatenate([[0], np.cumsum(docs)])
+        flat.extend((i * s + pos).tolist())
+        cu.extend((total + np.cumsum(docs)).tolist())
+        total += n
+    return ids, tok, rcu, np.array(flat, np.int64), np.array(cu, np.int32)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_packed_rows_match_independent_construction(seed):
+    ids, tok, rcu, flat, cu = _packed_rows(seed)
+    f1, c1 = oracle.pack_document_ids(ids)
+    np.testing.assert_array_equal(f1, flat)
+    np.testing.assert_array_equal(c1, cu)
+    f2, c2 = oracle.flatten_packed_metadata(tok, rcu, ids.shape[1])
+    np.testing.assert_array_equal(f2, flat)
+    np.testing.assert_array_equal(c2, cu)
+    # The row-local token indices need not be the first positions of a row.
+    _, tok_s, rcu_s, flat_s, cu_s = _packed_rows(seed, sparse=True)
+    f3, c3 = oracle.flatten_packed_metadata(tok_s, rcu_s, ids.shape[1])
+    np.testing.assert_array_equal(f3, flat_s)
+    np.testing.assert_array_equal(c3, cu_s)
+
+
+def test_one_document_per_row_is_pack_sequences():
+    lengths = np.array([5, 1, 9, 3], np.int32)
+    s = 9
+    ids = (np.arange(s)[None, :] < lengths[:, None]).astype(np.int32)
+    flat, cu = oracle.pack_document_ids(ids)
+    flat_p, cu_p, _ = oracle.pack_sequences(lengths, s)
+    np.testing.assert_array_equal(flat, flat_p)
+    np.testing.assert_array_equal(cu, cu_p)
+
+
+@pytest.mark.parametrize("row", [
+    [1, 1, 3, 0],     # document 2 skipped
+    [1, 0, 1, 0],     # a document after padding
+    [2, 2, 0, 0],     # numbering does not start at 1
+    [1, 2, 1, 0],     # document 1 split in two
+    [1, -1, 0, 0],    # negative id
+    [0, 1, 1, 0],     # padding before the first document
+])
+def test_indexed_mask_rejects_malformed_rows(row):
+    with pytest.raises(OracleError):
+        oracle.pack_document_ids([row])
+
+
+@pytest.mark.parametrize("tok,rcu", [
+    ([0, 1, 2, -1], [1, 3, -1]),      # boundaries do not start at 0
+    ([0, 1, 2, -1], [0, 2, 2, 3]),    # an empty document
+    ([0, 1, 2, -1], [0, 2, -1, -1]),  # boundaries end before the tokens do
+    ([0, 1, 2, -1], [0, 3, 4, -1]),   # boundaries end after them
+    ([0, -1, 2, -1], [0, 2, -1, -1]), # token padding not trailing
+    ([0, 1, 2, -1], [0, -1, 3, -1]),  # boundary padding not trailing
+    ([0, 1, 4, -1], [0, 3, -1, -1]),  # index outside the row
+])
+def test_flatten_rejects_inconsistent_layouts(tok, rcu):
+    with pytest.raises(OracleError):
+        oracle.flatten_packed_metadata([tok], [rcu], 4)
+
+
+def test_empty_rows_and_batch():
+    flat, cu = oracle.pack_document_ids(np.zeros((3, 4), np.int32))
+    assert flat.size == 0 and cu.tolist() == [0]
+    flat, cu = oracle.flatten_packed_metadata(np.full((2, 3), -1), [[0, -1], [0, -1]], 3)
+    assert flat.size == 0 and cu.tolist() == [0]
+
+
 # --------------------------------------------------------------------------- input recipes
 
 def test_workload_recipes():
