@@ -51,7 +51,8 @@ typedef enum pe_dtype { PE_BF16 = 0, PE_FP32 = 1 } pe_dtype;
 const char* pe_status_string(int status);
 
 /* Version of this ABI (incremented when an entry point is added or changed;
- * 2 added pe_packed_attention_fwd_local and pe_packed_attention_bwd_local). */
+ * 2 added pe_packed_attention_fwd_local, pe_packed_attention_bwd_local,
+ * pe_rows_workspace_size, pe_pack_document_ids, pe_flatten_packed_metadata). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -107,6 +108,45 @@ pe_status pe_gather_packed(const void* padded, const int64_t* flat_index, int64_
 pe_status pe_scatter_padded(const void* packed, const int32_t* cu_seqlens, int32_t num_sequences,
                             int32_t max_seq_len, int64_t row_bytes, void* padded,
                             pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Packed rows: padded [B, S] layouts that hold several documents per row
+ * (page "nemo_automodel.components.models.common.packing"), turned into the
+ * flat_index / cu_seqlens layout that the gather, scatter and attention calls
+ * consume. Documents follow each other row by row; flat_index holds indices
+ * into the padded [B, S] layout (row * S + position).
+ *
+ * pe_pack_document_ids: an indexed packing mask document_ids [B, S] int32
+ *   (function is_indexed_packed_mask: document i of a row, 1-based, marked i;
+ *   padding 0), e.g. the row [1,1,1,2,2,3,3,0,0] gives flat_index 0..6 and
+ *   cu_seqlens [0,3,5,7].
+ * pe_flatten_packed_metadata: function flatten_packed_sequence_metadata's
+ *   inputs, row-local token indices token_indices [B, S] int64 and row-local
+ *   cumulative lengths row_cu_seqlens [B, M1] int32, both -1 padded.
+ * Readings where the page is silent: padding is trailing in every row;
+ * documents are non-empty and numbered 1, 2, ... in order within a row;
+ * row-local boundaries start at 0, increase strictly and end at the row's
+ * token count; token indices lie in [0, S). Any other layout returns
+ * PE_ERR_INVALID_ARG (nothing is written to the outputs then); a token count of
+ * 2^31 or more returns PE_ERR_OVERFLOW.
+ * Outputs (device, caller-owned): flat_index with room for B*S entries,
+ * cu_seqlens with room for B*S + 1 (document ids) or B*(M1-1) + 1 (row
+ * boundaries) entries; *num_tokens and *num_documents are written on the
+ * host: each call reads 16 bytes back once and synchronizes the stream.
+ * Workspace: pe_rows_workspace_size(B) bytes, 16-byte aligned, device.
+ * ------------------------------------------------------------------------ */
+size_t pe_rows_workspace_size(int32_t num_rows);
+pe_status pe_pack_document_ids(const int32_t* document_ids, int32_t num_rows,
+                               int32_t sequence_length, int64_t* flat_index,
+                               int32_t* cu_seqlens, int64_t* num_tokens,
+                               int32_t* num_documents, void* workspace, size_t workspace_bytes,
+                               pe_stream_t stream);
+pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t* row_cu_seqlens,
+                                     int32_t num_rows, int32_t sequence_length,
+                                     int32_t row_cu_columns, int64_t* flat_index,
+                                     int32_t* cu_seqlens, int64_t* num_tokens,
+                                     int32_t* num_documents, void* workspace,
+                                     size_t workspace_bytes, pe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Packed attention forward (function packed_attention and the custom op

@@ -12,6 +12,8 @@ from .binding import (  # noqa: F401
     load_library,
     pe_attention_kernel,
     pe_gather_packed,
+    pe_flatten_packed_metadata,
+    pe_pack_document_ids,
     pe_pack_sequences,
     pe_packed_attention_bwd,
     pe_packed_attention_bwd_local,

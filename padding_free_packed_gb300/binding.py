@@ -25,6 +25,7 @@ EXPORTED = (
     "pe_gather_packed", "pe_scatter_padded", "pe_attention_workspace_size",
     "pe_packed_attention_fwd", "pe_packed_attention_bwd", "pe_packed_attention_fwd_local",
     "pe_packed_attention_bwd_local", "pe_read_device_status", "pe_attention_kernel",
+    "pe_rows_workspace_size", "pe_pack_document_ids", "pe_flatten_packed_metadata",
 )
 
 _lib = None
@@ -77,6 +78,14 @@ def load_library(path: str = LIB_PATH):
                                                   vp, c.c_float, i32, i32, c.c_int, vp, vp, vp,
                                                   vp, vp, vp, vp, sz, vp]
     lib.pe_packed_attention_bwd_local.restype = c.c_int
+    lib.pe_rows_workspace_size.argtypes = [i32]
+    lib.pe_rows_workspace_size.restype = sz
+    lib.pe_pack_document_ids.argtypes = [vp, i32, i32, vp, vp, c.POINTER(i64), c.POINTER(i32),
+                                         vp, sz, vp]
+    lib.pe_pack_document_ids.restype = c.c_int
+    lib.pe_flatten_packed_metadata.argtypes = [vp, vp, i32, i32, i32, vp, vp, c.POINTER(i64),
+                                               c.POINTER(i32), vp, sz, vp]
+    lib.pe_flatten_packed_metadata.restype = c.c_int
     lib.pe_attention_kernel.argtypes = [c.c_int, i32, c.c_int, c.c_int]
     lib.pe_attention_kernel.restype = c.c_char_p
     lib.pe_read_device_status.argtypes = [vp, vp]
@@ -131,6 +140,45 @@ def pe_pack_sequences(lengths: torch.Tensor, max_seq_len: int):
            lib.pe_pack_sequences(_ptr(lengths), b, int(max_seq_len), _ptr(flat), _ptr(cu),
                                  ctypes.byref(n), _ptr(ws), ws.numel(), _stream(dev)))
     return flat[: n.value], cu, int(n.value)
+
+
+def pe_pack_document_ids(document_ids: torch.Tensor):
+    """Indexed packing mask [B, S] (document i of a row marked i, 0 = padding)
+    -> (flat_index int64 [N] into the [B, S] layout, cu_seqlens int32 [D+1], N)."""
+    lib = load_library()
+    ids = _cuda(document_ids, "document_ids").to(torch.int32)
+    b, s = (int(x) for x in ids.shape)
+    dev = ids.device
+    flat = torch.empty(max(b * s, 1), dtype=torch.int64, device=dev)
+    cu = torch.empty(b * s + 1, dtype=torch.int32, device=dev)
+    ws = _workspace(lib.pe_rows_workspace_size(b), dev)
+    n, d = ctypes.c_int64(0), ctypes.c_int32(0)
+    _check("pe_pack_document_ids",
+           lib.pe_pack_document_ids(_ptr(ids), b, s, _ptr(flat), _ptr(cu), ctypes.byref(n),
+                                    ctypes.byref(d), _ptr(ws), ws.numel(), _stream(dev)))
+    return flat[: n.value], cu[: d.value + 1], int(n.value)
+
+
+def pe_flatten_packed_metadata(token_indices: torch.Tensor, row_cu_seqlens: torch.Tensor):
+    """Row-local token indices [B, S] and row-local cumulative lengths [B, M+1]
+    (both -1 padded) -> (flat_index int64 [N], cu_seqlens int32 [D+1], N)."""
+    lib = load_library()
+    tok = _cuda(token_indices, "token_indices").to(torch.int64)
+    rcu = _cuda(row_cu_seqlens, "row_cu_seqlens").to(torch.int32)
+    b, s = (int(x) for x in tok.shape)
+    m1 = int(rcu.shape[1])
+    if int(rcu.shape[0]) != b:
+        raise ValueError("token_indices and row_cu_seqlens disagree on the number of rows")
+    dev = tok.device
+    flat = torch.empty(max(b * s, 1), dtype=torch.int64, device=dev)
+    cu = torch.empty(b * max(m1 - 1, 0) + 1, dtype=torch.int32, device=dev)
+    ws = _workspace(lib.pe_rows_workspace_size(b), dev)
+    n, d = ctypes.c_int64(0), ctypes.c_int32(0)
+    _check("pe_flatten_packed_metadata",
+           lib.pe_flatten_packed_metadata(_ptr(tok), _ptr(rcu), b, s, m1, _ptr(flat), _ptr(cu),
+                                          ctypes.byref(n), ctypes.byref(d), _ptr(ws), ws.numel(),
+                                          _stream(dev)))
+    return flat[: n.value], cu[: d.value + 1], int(n.value)
 
 
 def pe_gather_packed(padded: torch.Tensor, flat_index: torch.Tensor, num_tokens: int | None = None):
