@@ -173,7 +173,14 @@ def run_ours(args, rank, world):
     wl = workloads.WORKLOADS[args.workload]
     # Weak scaling: every rank draws its own batch of the same workload.
     train = wl.backward
-    if args.packed:
+    rows_layout = args.layout == "rows"
+    if rows_layout:
+        # Documents packed several to a padded row (an indexed packing mask).
+        drawn = workloads.make_packed_row_inputs(args.workload, args.row_len, seed=args.seed + rank,
+                                                 with_dout=train, max_sequences=args.sequences)
+        lengths, row_ids = drawn[0], drawn[1]
+        host_grids = list(drawn[2:])
+    elif args.packed:
         # Already-packed inputs (a pipeline that collates without padding):
         # the step is the attention forward (and backward) alone.
         lengths = workloads.draw_lengths(args.workload, np.random.default_rng(args.seed + rank))
@@ -201,10 +208,14 @@ def run_ours(args, rank, world):
     kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token)
     bwd_kernel = pe.pe_attention_kernel(wl.torch_dtype, d, backward=True) if train else None
 
-    lengths_d = torch.from_numpy(lengths).to(dev)
+    # The per-step layout metadata: lengths, or the packed rows' mask.
+    meta_host = row_ids if rows_layout else lengths
+    lengths_d = torch.from_numpy(meta_host).to(dev)
     dev_grids = [t.to(dev) for t in host_grids]
-    og = torch.empty_like(dev_grids[0])
-    grad_grids = [torch.empty_like(dev_grids[0]) for _ in range(3)] if train else None
+    og = (torch.empty((n_tokens, h, d), dtype=dev_grids[0].dtype, device=dev) if rows_layout
+          else torch.empty_like(dev_grids[0]))
+    grad_grids = ([torch.empty_like(og) for _ in range(3)] if rows_layout else
+                  [torch.empty_like(dev_grids[0]) for _ in range(3)]) if train else None
     packed_cu = pe.pe_pack_sequences(lengths_d, s)[1] if args.packed else None
     q_first = (dev_grids[0][packed_cu[:-1].long()].contiguous()
                if args.packed and args.first_token else None)
@@ -242,13 +253,16 @@ def run_ours(args, rank, world):
                 out, _ = timed(record, fwd_events, lambda: attention_fwd(
                     q_first, k, v, cu, s, wl.scale, query_is_first_token=True))
                 return n_tokens
+        elif rows_layout:
+            flat, cu, n = pe.pe_pack_document_ids(lengths_t)
+            q, k, v = (pe.pe_gather_packed(g, flat, n) for g in grids[:3])
         else:
             flat, cu, n = pe.pe_pack_sequences(lengths_t, s)
             q, k, v = (pe.pe_gather_packed(g, flat, n) for g in grids[:3])
         out, lse = timed(record, fwd_events,
                          lambda: attention_fwd(q, k, v, cu, s, wl.scale, need_lse=train))
-        if args.packed:
-            og.copy_(out)
+        if args.packed or rows_layout:
+            og.copy_(out)          # packed rows: the output stays packed (a THD consumer)
         else:
             pe.pe_scatter_padded(out, cu, s, out=og)
         if train:
@@ -256,7 +270,7 @@ def run_ours(args, rank, world):
             grads = timed(record, bwd_events,
                           lambda: attention_bwd(do, q, k, v, out, lse, cu, s, wl.scale))
             for g, grid in zip(grads, grad_grids):
-                if args.packed:
+                if args.packed or rows_layout:
                     grid.copy_(g)
                 else:
                     pe.pe_scatter_padded(g, cu, s, out=grid)
@@ -267,6 +281,8 @@ def run_ours(args, rank, world):
     # and 3 scatters. Packed steps: plan+attention (+ the 5 backward launches).
     if args.packed:
         launches_per_step = 2 + (5 if train else 0)
+    elif rows_layout:   # mask count, scan, fill, 3 gathers, plan + attention (+ dO gather, backward)
+        launches_per_step = 3 + 3 + 2 + ((1 + 5) if train else 0)
     else:
         launches_per_step = 2 + 3 + 2 + 1 + ((1 + 5 + 3) if train else 0)
 
@@ -299,7 +315,7 @@ def run_ours(args, rank, world):
     e2e = None
     if not args.no_e2e:
         host_in = [t.pin_memory() for t in host_grids]
-        hlen = torch.from_numpy(lengths).pin_memory()
+        hlen = torch.from_numpy(meta_host).pin_memory()
         dev_in = [torch.empty_like(t, device=dev) for t in host_in]
         dlen = torch.empty_like(lengths_d)
         results = [og] + (grad_grids if train else [])
@@ -371,7 +387,13 @@ def run_ours(args, rank, world):
                    "attention": (f"local window ({window[0]}, {window[1]})" if window
                                  else "full") + (", first-token query" if args.first_token
                                                  else ""),
-                   "step": (("tile plan + attention forward + backward on packed inputs"
+                   "layout": (f"documents packed into rows of {args.row_len} (indexed packing "
+                              "mask)" if rows_layout else
+                              "packed" if args.packed else "one sequence per padded row"),
+                   "step": ("mask -> flat_index/cu_seqlens + gather q,k,v + tile plan + attention "
+                            "forward" + (" + dO gather + backward" if train else "")
+                            + " (outputs stay packed)") if rows_layout else
+                           (("tile plan + attention forward + backward on packed inputs"
                              if train else "tile plan + attention forward on packed inputs")
                             if args.packed else
                             ("pack + gather q,k,v,dO + tile plan + attention forward + scatter "
@@ -492,6 +514,10 @@ def main():
                     help="inputs already packed: time the attention calls alone")
     ap.add_argument("--first-token", action="store_true",
                     help="with --packed: one query per sequence (its first token)")
+    ap.add_argument("--layout", choices=["padded", "rows"], default="padded",
+                    help="rows: documents packed several to a row of --row-len tokens, with an "
+                         "indexed packing mask (document i of a row marked i)")
+    ap.add_argument("--row-len", type=int, default=16384)
     ap.add_argument("--window", type=int, nargs=2, metavar=("LEFT", "RIGHT"), default=None,
                     help="local attention: query at position r sees keys r-LEFT .. r+RIGHT "
                          "(negative = unbounded); e.g. 64 64 for ModernBERT's local layers")

@@ -13,9 +13,11 @@
 // increase strictly and end at the row's token count; row-local token indices
 // lie in [0, S). Rows follow each other in the flat stream.
 //
-// Three kernels and one host read, like pack_sequences: a per-row validating
-// count (one CTA per row), a single-CTA scan of the per-row token and document
-// counts, and a per-row fill; the host then copies back 16 bytes.
+// Three kernels and one host read, like pack_sequences: a validating count
+// over (row, chunk of 2048 positions) pairs that adds each chunk's tokens and
+// document starts into its row's totals (integer atomics: exact in any order),
+// a single-CTA scan of the per-row totals, and a fill over the same chunks;
+// the host then copies back 16 bytes.
 #include "pe_common.cuh"
 
 namespace pe {
@@ -24,6 +26,7 @@ namespace {
 
 constexpr int kRowThreads = 256;
 constexpr int kScanThreads = 1024;
+constexpr int32_t kChunk = 2048;   // row positions per CTA work item
 
 struct RowsResult {
   long long num_tokens;
@@ -93,11 +96,14 @@ __device__ __forceinline__ void block_sum2(int& a, int& b, int* sh) {
 __global__ void __launch_bounds__(kRowThreads)
 doc_ids_count_kernel(const int32_t* __restrict__ ids, int32_t B, int32_t S, RowsWorkspace w) {
   __shared__ int sh[64];
-  for (int64_t b = blockIdx.x; b < B; b += gridDim.x) {
+  const int32_t chunks = (S + kChunk - 1) / kChunk;
+  for (int64_t item = blockIdx.x; item < (int64_t)B * chunks; item += gridDim.x) {
+    const int64_t b = item / chunks;
+    const int32_t j0 = (int32_t)(item - b * chunks) * kChunk, j1 = min(j0 + kChunk, S);
     const int32_t* row = ids + b * (int64_t)S;
     int tokens = 0, starts = 0;
     bool bad = false;
-    for (int32_t j = threadIdx.x; j < S; j += kRowThreads) {
+    for (int32_t j = j0 + threadIdx.x; j < j1; j += kRowThreads) {
       const int32_t id = __ldg(row + j);
       const int32_t left = j > 0 ? __ldg(row + j - 1) : 0;
       if (id < 0) bad = true;
@@ -118,31 +124,37 @@ doc_ids_count_kernel(const int32_t* __restrict__ ids, int32_t B, int32_t S, Rows
     if (bad) flag_invalid(w.result);
     block_sum2(tokens, starts, sh);
     if (threadIdx.x == 0) {
-      w.n[b] = tokens;
-      w.d[b] = starts;
+      atomicAdd(w.n + b, tokens);
+      atomicAdd(w.d + b, starts);
     }
   }
 }
 
 // Row-local token indices and cumulative lengths (-1 padded): per row, counts
 // the tokens and documents and checks the layout rules.
+// The check that a row's last boundary equals its token count needs the row
+// total, so it runs in the scan.
 __global__ void __launch_bounds__(kRowThreads)
 nemo_rows_count_kernel(const int64_t* __restrict__ tok, const int32_t* __restrict__ rcu,
                        int32_t B, int32_t S, int32_t M1, RowsWorkspace w) {
   __shared__ int sh[64];
-  for (int64_t b = blockIdx.x; b < B; b += gridDim.x) {
+  const int32_t chunks = (S + kChunk - 1) / kChunk;
+  for (int64_t item = blockIdx.x; item < (int64_t)B * chunks; item += gridDim.x) {
+    const int64_t b = item / chunks;
+    const int32_t chunk = (int32_t)(item - b * chunks);
+    const int32_t j0 = chunk * kChunk, j1 = min(j0 + kChunk, S);
     const int64_t* trow = tok + b * (int64_t)S;
     const int32_t* crow = rcu + b * (int64_t)M1;
     int tokens = 0, bounds = 0;
     bool bad = false;
-    for (int32_t j = threadIdx.x; j < S; j += kRowThreads) {
+    for (int32_t j = j0 + threadIdx.x; j < j1; j += kRowThreads) {
       const int64_t t = __ldg(trow + j);
       if (t == -1) continue;
       ++tokens;
       bad |= t < 0 || t >= S;
       bad |= j > 0 && __ldg(trow + j - 1) == -1;   // padding not trailing
     }
-    for (int32_t k = threadIdx.x; k < M1; k += kRowThreads) {
+    for (int32_t k = threadIdx.x; chunk == 0 && k < M1; k += kRowThreads) {  // boundaries once per row
       const int32_t c = __ldg(crow + k);
       if (k == 0) {
         bad |= c != 0;
@@ -153,13 +165,11 @@ nemo_rows_count_kernel(const int64_t* __restrict__ tok, const int32_t* __restric
       const int32_t prev = __ldg(crow + k - 1);
       bad |= prev == -1 || c <= prev;              // padding not trailing, or an empty document
     }
-    block_sum2(tokens, bounds, sh);
-    // The last boundary must equal the row's token count.
-    if (threadIdx.x == 0 && __ldg(crow + bounds) != tokens) bad = true;
     if (bad) flag_invalid(w.result);
+    block_sum2(tokens, bounds, sh);
     if (threadIdx.x == 0) {
-      w.n[b] = tokens;
-      w.d[b] = bounds;
+      atomicAdd(w.n + b, tokens);
+      atomicAdd(w.d + b, bounds);
     }
   }
 }
@@ -192,13 +202,18 @@ __device__ __forceinline__ long long scan1024(long long x, long long* warp_sums,
 }
 
 // Exclusive prefixes of the per-row counts; totals and the closing boundary.
+// With row-local boundaries (rcu non-null) it also checks that each row's last
+// boundary equals the row's token count.
 __global__ void __launch_bounds__(kScanThreads)
-rows_scan_kernel(int32_t B, RowsWorkspace w, int32_t* __restrict__ cu_seqlens) {
+rows_scan_kernel(int32_t B, RowsWorkspace w, const int32_t* __restrict__ rcu, int32_t M1,
+                 int32_t* __restrict__ cu_seqlens) {
   __shared__ long long warp_sums[32];
   long long carry_n = 0, carry_d = 0;
   for (int64_t base = 0; base < B; base += kScanThreads) {
     const int64_t b = base + threadIdx.x;
     const long long n = b < B ? w.n[b] : 0, d = b < B ? w.d[b] : 0;
+    // d < M1 always: it counts boundary entries after the first of M1.
+    if (rcu && b < B && __ldg(rcu + b * (int64_t)M1 + d) != n) flag_invalid(w.result);
     long long tn, td;
     const long long in = scan1024(n, warp_sums, tn);
     const long long id = scan1024(d, warp_sums, td);
@@ -209,6 +224,7 @@ rows_scan_kernel(int32_t B, RowsWorkspace w, int32_t* __restrict__ cu_seqlens) {
     carry_n += tn;
     carry_d += td;
   }
+  __syncthreads();   // every row's check has flagged before the status is read
   if (threadIdx.x == 0) {
     RowsResult* r = w.result;
     if (r->status == PE_OK && carry_n >= (1LL << 31)) r->status = PE_ERR_OVERFLOW;
@@ -222,11 +238,14 @@ __global__ void __launch_bounds__(kRowThreads)
 doc_ids_fill_kernel(const int32_t* __restrict__ ids, int32_t B, int32_t S, RowsWorkspace w,
                     int64_t* __restrict__ flat_index, int32_t* __restrict__ cu_seqlens) {
   if (w.result->status != PE_OK) return;
-  for (int64_t b = blockIdx.x; b < B; b += gridDim.x) {
+  const int32_t chunks = (S + kChunk - 1) / kChunk;
+  for (int64_t item = blockIdx.x; item < (int64_t)B * chunks; item += gridDim.x) {
+    const int64_t b = item / chunks;
+    const int32_t j0 = (int32_t)(item - b * chunks) * kChunk;
     const int32_t* row = ids + b * (int64_t)S;
-    const int32_t n = w.n[b];
+    const int32_t n = w.n[b], j1 = min(j0 + kChunk, n);
     const int64_t t0 = w.tok_off[b], d0 = w.doc_off[b];
-    for (int32_t j = threadIdx.x; j < n; j += kRowThreads) {   // tokens are the first n positions
+    for (int32_t j = j0 + threadIdx.x; j < j1; j += kRowThreads) {  // tokens: the first n positions
       flat_index[t0 + j] = b * (int64_t)S + j;
       const int32_t id = __ldg(row + j);
       if (j == 0 || __ldg(row + j - 1) != id) cu_seqlens[d0 + id - 1] = (int32_t)(t0 + j);
@@ -239,20 +258,34 @@ nemo_rows_fill_kernel(const int64_t* __restrict__ tok, const int32_t* __restrict
                       int32_t B, int32_t S, int32_t M1, RowsWorkspace w,
                       int64_t* __restrict__ flat_index, int32_t* __restrict__ cu_seqlens) {
   if (w.result->status != PE_OK) return;
-  for (int64_t b = blockIdx.x; b < B; b += gridDim.x) {
+  const int32_t chunks = (S + kChunk - 1) / kChunk;
+  for (int64_t item = blockIdx.x; item < (int64_t)B * chunks; item += gridDim.x) {
+    const int64_t b = item / chunks;
+    const int32_t chunk = (int32_t)(item - b * chunks);
     const int32_t n = w.n[b], d = w.d[b];
     const int64_t t0 = w.tok_off[b], d0 = w.doc_off[b];
-    for (int32_t i = threadIdx.x; i < n; i += kRowThreads)
+    for (int32_t i = chunk * kChunk + threadIdx.x; i < min(chunk * kChunk + kChunk, n);
+         i += kRowThreads)
       flat_index[t0 + i] = b * (int64_t)S + __ldg(tok + b * (int64_t)S + i);
-    for (int32_t k = threadIdx.x; k < d; k += kRowThreads)
+    for (int32_t k = threadIdx.x; chunk == 0 && k < d; k += kRowThreads)
       cu_seqlens[d0 + k] = (int32_t)(t0 + __ldg(rcu + b * (int64_t)M1 + k));
   }
 }
 
 // Launch sizes and the host read shared by both entry points.
-unsigned row_blocks(int32_t B) {
+unsigned row_blocks(int32_t B, int32_t S) {
+  const int64_t items = (int64_t)B * ((S + kChunk - 1) / kChunk);
   const int64_t cap = (int64_t)device_sm_count() * 8;
-  return (unsigned)(B < cap ? B : cap);
+  return (unsigned)(items < cap ? items : cap);
+}
+
+// Zeroes the result word and the per-row totals the count kernels add into.
+pe_status clear_counts(const RowsWorkspace& w, int32_t B, cudaStream_t stream) {
+  PE_CUDA_TRY(cudaMemsetAsync(w.result, 0, sizeof(RowsResult), stream));
+  if (B > 0)
+    PE_CUDA_TRY(cudaMemsetAsync(w.n, 0, reinterpret_cast<char*>(w.tok_off) -
+                                            reinterpret_cast<char*>(w.n), stream));
+  return PE_OK;
 }
 
 pe_status read_result(const RowsWorkspace& w, int64_t* num_tokens, int32_t* num_documents,
@@ -296,15 +329,15 @@ extern "C" pe_status pe_pack_document_ids(const int32_t* document_ids, int32_t B
   PE_TRY(check_rows_args(B, S, document_ids, flat_index, cu_seqlens, num_tokens, num_documents,
                          workspace, workspace_bytes));
   const RowsWorkspace w = rows_ws_view(workspace, B);
-  PE_CUDA_TRY(cudaMemsetAsync(w.result, 0, sizeof(RowsResult), stream));
+  PE_TRY(clear_counts(w, B, stream));
   if (B > 0) {
-    doc_ids_count_kernel<<<row_blocks(B), kRowThreads, 0, stream>>>(document_ids, B, S, w);
+    doc_ids_count_kernel<<<row_blocks(B, S), kRowThreads, 0, stream>>>(document_ids, B, S, w);
     PE_CUDA_TRY(cudaGetLastError());
   }
-  rows_scan_kernel<<<1, kScanThreads, 0, stream>>>(B, w, cu_seqlens);
+  rows_scan_kernel<<<1, kScanThreads, 0, stream>>>(B, w, nullptr, 0, cu_seqlens);
   PE_CUDA_TRY(cudaGetLastError());
   if (B > 0) {
-    doc_ids_fill_kernel<<<row_blocks(B), kRowThreads, 0, stream>>>(document_ids, B, S, w,
+    doc_ids_fill_kernel<<<row_blocks(B, S), kRowThreads, 0, stream>>>(document_ids, B, S, w,
                                                                    flat_index, cu_seqlens);
     PE_CUDA_TRY(cudaGetLastError());
   }
@@ -322,16 +355,16 @@ extern "C" pe_status pe_flatten_packed_metadata(const int64_t* token_indices,
   PE_TRY(check_rows_args(B, S, token_indices, flat_index, cu_seqlens, num_tokens, num_documents,
                          workspace, workspace_bytes));
   const RowsWorkspace w = rows_ws_view(workspace, B);
-  PE_CUDA_TRY(cudaMemsetAsync(w.result, 0, sizeof(RowsResult), stream));
+  PE_TRY(clear_counts(w, B, stream));
   if (B > 0) {
-    nemo_rows_count_kernel<<<row_blocks(B), kRowThreads, 0, stream>>>(token_indices,
+    nemo_rows_count_kernel<<<row_blocks(B, S), kRowThreads, 0, stream>>>(token_indices,
                                                                       row_cu_seqlens, B, S, M1, w);
     PE_CUDA_TRY(cudaGetLastError());
   }
-  rows_scan_kernel<<<1, kScanThreads, 0, stream>>>(B, w, cu_seqlens);
+  rows_scan_kernel<<<1, kScanThreads, 0, stream>>>(B, w, row_cu_seqlens, M1, cu_seqlens);
   PE_CUDA_TRY(cudaGetLastError());
   if (B > 0) {
-    nemo_rows_fill_kernel<<<row_blocks(B), kRowThreads, 0, stream>>>(
+    nemo_rows_fill_kernel<<<row_blocks(B, S), kRowThreads, 0, stream>>>(
         token_indices, row_cu_seqlens, B, S, M1, w, flat_index, cu_seqlens);
     PE_CUDA_TRY(cudaGetLastError());
   }

@@ -173,3 +173,38 @@ def make_padded_inputs(name: str, seed: int = 0, max_sequences: int | None = Non
         x = torch.from_numpy(rng.standard_normal(shape, dtype=np.float32))
         grids.append(x.to(wl.torch_dtype) if wl.torch_dtype != torch.float32 else x)
     return (lengths, *grids)
+
+
+def make_packed_row_inputs(name: str, row_len: int, seed: int = 0, with_dout: bool = False,
+                           max_sequences: int | None = None) -> tuple:
+    """The workload's documents packed in order into padded rows of ``row_len``
+    tokens, as a packing collater lays them out: a document goes to the current
+    row if it fits, else it starts a new row. Returns (document lengths, the
+    indexed packing mask ``[R, row_len]`` int32 (document i of a row marked i,
+    0 = padding), q, k, v grids ``[R, row_len, H, d]``, plus dO when
+    ``with_dout``). Lengths are the workload's first draw; grid values are
+    fresh N(0, 1) draws in float32, pad positions included."""
+    wl = WORKLOADS[name]
+    rng = np.random.default_rng(seed)
+    lengths = draw_lengths(name, rng)
+    if max_sequences is not None:
+        lengths = np.ascontiguousarray(lengths[:max_sequences])
+    if int(lengths.max()) > row_len:
+        raise ValueError(f"a document of {int(lengths.max())} tokens does not fit a row of {row_len}")
+    rows, fill = [[]], 0
+    for length in lengths.tolist():
+        if fill + length > row_len:
+            rows.append([])
+            fill = 0
+        rows[-1].append(length)
+        fill += length
+    ids = np.zeros((len(rows), row_len), np.int32)
+    for r, docs in enumerate(rows):
+        n = sum(docs)
+        ids[r, :n] = np.repeat(np.arange(1, len(docs) + 1), docs)
+    shape = (len(rows), row_len, wl.num_heads, wl.head_dim)
+    grids = []
+    for _ in range(4 if with_dout else 3):
+        x = torch.from_numpy(rng.standard_normal(shape, dtype=np.float32))
+        grids.append(x.to(wl.torch_dtype) if wl.torch_dtype != torch.float32 else x)
+    return (lengths, ids, *grids)

@@ -592,3 +592,12 @@ def test_workload_recipes():
         assert lengths.min() >= 1 and lengths.max() <= workloads.WORKLOADS[name].max_seq_len
     x = workloads.make_inputs("tiny_fp32")
     assert x.q.dtype == torch.float32 and tuple(x.q.shape) == (91, 2, 8)
+
+
+def test_packed_row_recipe_keeps_the_documents_in_order():
+    """The packed-rows input recipe lays the workload's documents out in order:
+    the oracle's conversion of its mask gives back exactly their lengths."""
+    lengths, ids, q, _, _ = workloads.make_packed_row_inputs("contrastive_bf16", 2048)
+    _, cu = oracle.pack_document_ids(ids)
+    np.testing.assert_array_equal(np.diff(cu), lengths)
+    assert q.shape[:2] == ids.shape and ids.shape[1] == 2048
