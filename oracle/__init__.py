@@ -81,6 +81,14 @@ def _load():
         lib.orc_flatten_packed_metadata.argtypes = [i64p, i32p, i64, i64, i64, i64p, i32p, i64p,
                                                     i64p]
         lib.orc_flatten_packed_metadata.restype = ctypes.c_int
+        lib.orc_packed_positions.argtypes = [i32p, i64, i64p]
+        lib.orc_packed_positions.restype = None
+        lib.orc_rope.argtypes = [dp, i64p, i64, i64, i64, ctypes.c_double]
+        lib.orc_rope.restype = None
+        lib.orc_layernorm.argtypes = [dp, dp, dp, dp, i64, i64, ctypes.c_double, dp, dp]
+        lib.orc_layernorm.restype = None
+        lib.orc_geglu.argtypes = [dp, i64, i64, dp]
+        lib.orc_geglu.restype = None
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = ctypes.c_int
         _lib = lib
@@ -271,3 +279,51 @@ def attention_bwd(q, k, v, dout, cu_seqlens, scale: float, first_token: bool = F
     if rc != 0:
         raise OracleError(rc)
     return dq, dk, dv
+
+
+# --------------------------------------------------------------------------- layer tail
+
+def packed_positions(cu_seqlens) -> np.ndarray:
+    """Position of every token inside its own sequence (int64 [N])."""
+    lib = _load()
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    pos = np.zeros(int(cu[-1]), dtype=np.int64)
+    lib.orc_packed_positions(_ptr(cu, ctypes.c_int32), int(cu.shape[0]) - 1,
+                             _ptr(pos, ctypes.c_int64))
+    return pos
+
+
+def rope(x, positions, theta: float) -> np.ndarray:
+    """Split-half rotary embedding of x [N, H, D] at the given positions (fp64 copy)."""
+    lib = _load()
+    y = _f64(x).copy()
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    n, h, d = y.shape
+    lib.orc_rope(_ptr(y, ctypes.c_double), _ptr(pos, ctypes.c_int64), n, h, d, float(theta))
+    return y
+
+
+def layernorm(x, weight, bias=None, eps: float = 1e-5, residual=None):
+    """LayerNorm over the last dim of x [N, C] (of x + residual when given).
+    Returns y, plus h = x + residual when a residual is given."""
+    lib = _load()
+    xx = _f64(x)
+    n, c = xx.shape
+    w = _f64(weight)
+    b = None if bias is None else _f64(bias)
+    r = None if residual is None else _f64(residual)
+    y = np.zeros_like(xx)
+    h = np.zeros_like(xx) if residual is not None else None
+    dp = lambda a: None if a is None else _ptr(a, ctypes.c_double)
+    lib.orc_layernorm(dp(xx), dp(r), dp(w), dp(b), n, c, float(eps), dp(y), dp(h))
+    return (y, h) if residual is not None else y
+
+
+def geglu(x) -> np.ndarray:
+    """gelu(x[:, :F]) * x[:, F:] for x [N, 2F], exact GELU."""
+    lib = _load()
+    xx = _f64(x)
+    n, f2 = xx.shape
+    y = np.zeros((n, f2 // 2), dtype=np.float64)
+    lib.orc_geglu(_ptr(xx, ctypes.c_double), n, f2 // 2, _ptr(y, ctypes.c_double))
+    return y

@@ -518,6 +518,75 @@ int orc_attention_bwd(const double* q, const double* k, const double* v, const d
                                  dv, nthreads);
 }
 
+/* ------------------------------------------------------------------------- */
+/* The packed encoder layer tail (page "packed-encoders 0.1.0": fused          */
+/* LayerNorm / residual-LayerNorm / RoPE / GeGLU kernels on the flat token     */
+/* buffer, with position ids that restart at every sequence - section "Fully  */
+/* packed execution": position_ids = cat(arange(L_i))). The pages name the     */
+/* operations and ModernBERT's split-half RoPE convention; the formulas are    */
+/* ModernBERT's:                                                               */
+/*   RoPE: for head_dim D and i < D/2, with a = pos * theta^(-2i/D),          */
+/*         out[i] = x[i] cos a - x[i+D/2] sin a, out[i+D/2] = x[i+D/2] cos a + */
+/*         x[i] sin a;                                                        */
+/*   LayerNorm: y = (h - mean(h)) / sqrt(var(h) + eps) * w (+ b), biased var;  */
+/*   residual-LayerNorm: h = x + residual (also returned), then LayerNorm;     */
+/*   GeGLU: y[f] = gelu(x[f]) * x[F + f] with the exact (erf) GELU.            */
+/* ------------------------------------------------------------------------- */
+
+/* pos[t] = t - cu[i] for the sequence i holding token t. */
+void orc_packed_positions(const int32_t* cu, int64_t B, int64_t* pos) {
+  for (int64_t i = 0; i < B; ++i)
+    for (int64_t t = cu[i]; t < cu[i + 1]; ++t) pos[t] = t - cu[i];
+}
+
+/* x: [N][H][D], rotated in place. */
+void orc_rope(double* x, const int64_t* pos, int64_t N, int64_t H, int64_t D, double theta) {
+  const int64_t half = D / 2;
+  for (int64_t t = 0; t < N; ++t)
+    for (int64_t h = 0; h < H; ++h) {
+      double* v = x + (t * H + h) * D;
+      for (int64_t i = 0; i < half; ++i) {
+        const double a = (double)pos[t] * pow(theta, -2.0 * (double)i / (double)D);
+        const double c = cos(a), s = sin(a);
+        const double x1 = v[i], x2 = v[i + half];
+        v[i] = x1 * c - x2 * s;
+        v[i + half] = x2 * c + x1 * s;
+      }
+    }
+}
+
+/* x, residual (nullable), y, residual_out (nullable): [N][C]; w [C]; b [C] nullable. */
+void orc_layernorm(const double* x, const double* residual, const double* w, const double* b,
+                   int64_t N, int64_t C, double eps, double* y, double* residual_out) {
+  for (int64_t t = 0; t < N; ++t) {
+    const double* xr = x + t * C;
+    double mean = 0.0;
+    for (int64_t c = 0; c < C; ++c) mean += xr[c] + (residual ? residual[t * C + c] : 0.0);
+    mean /= (double)C;
+    double var = 0.0;
+    for (int64_t c = 0; c < C; ++c) {
+      const double d = xr[c] + (residual ? residual[t * C + c] : 0.0) - mean;
+      var += d * d;
+    }
+    var /= (double)C;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int64_t c = 0; c < C; ++c) {
+      const double h = xr[c] + (residual ? residual[t * C + c] : 0.0);
+      if (residual_out) residual_out[t * C + c] = h;
+      y[t * C + c] = (h - mean) * rstd * w[c] + (b ? b[c] : 0.0);
+    }
+  }
+}
+
+/* x: [N][2F] -> y: [N][F]. */
+void orc_geglu(const double* x, int64_t N, int64_t F, double* y) {
+  for (int64_t t = 0; t < N; ++t)
+    for (int64_t f = 0; f < F; ++f) {
+      const double a = x[t * 2 * F + f], g = x[t * 2 * F + F + f];
+      y[t * F + f] = 0.5 * a * (1.0 + erf(a / sqrt(2.0))) * g;
+    }
+}
+
 int orc_hardware_threads(void) {
   long n = sysconf(_SC_NPROCESSORS_ONLN);
   return n > 0 ? (int)n : 1;

@@ -580,6 +580,77 @@ def test_empty_rows_and_batch():
     assert flat.size == 0 and cu.tolist() == [0]
 
 
+# --------------------------------------------------------------------------- layer tail
+# Page "packed-encoders 0.1.0": fused LayerNorm / residual-LayerNorm / RoPE
+# (split-half convention) / GeGLU on the flat token buffer, with position ids
+# restarting at every sequence.
+
+def test_packed_positions_worked_example(golden):
+    g = golden("packed_position_ids_example.txt")
+    _, cu, _ = oracle.pack_sequences(g["lengths"], max(g["lengths"]))
+    assert cu.tolist() == g["cu_seqlens"]
+    assert oracle.packed_positions(cu).tolist() == g["position_ids"]
+
+
+def test_rope_is_a_complex_rotation_of_split_halves():
+    """Pairs (i, i + D/2) as complex numbers x_i + j x_{i+D/2}, multiplied by
+    exp(j * pos * theta^(-2i/D))."""
+    rng = np.random.default_rng(101)
+    n, h, d, theta = 37, 3, 16, 10000.0
+    x = rng.standard_normal((n, h, d))
+    pos = rng.integers(0, 9000, n)
+    got = oracle.rope(x, pos, theta)
+    angle = pos[:, None] * theta ** (-np.arange(0, d, 2) / d)            # [n, d/2]
+    z = (x[..., : d // 2] + 1j * x[..., d // 2:]) * np.exp(1j * angle)[:, None, :]
+    np.testing.assert_allclose(got[..., : d // 2], z.real, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(got[..., d // 2:], z.imag, rtol=0, atol=1e-10)
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(102)
+    n, h, d = 9, 2, 8
+    x = rng.standard_normal((n, h, d))
+    # Position 0 is the identity; every pair keeps its norm.
+    np.testing.assert_allclose(oracle.rope(x, np.zeros(n, np.int64), 500.0), x, atol=1e-15)
+    y = oracle.rope(x, np.arange(n) * 7, 500.0)
+    np.testing.assert_allclose(x[..., :4] ** 2 + x[..., 4:] ** 2, y[..., :4] ** 2 + y[..., 4:] ** 2,
+                               rtol=1e-12)
+    # Scores depend only on the position difference.
+    q, k = rng.standard_normal((1, 1, d)), rng.standard_normal((1, 1, d))
+    def score(m, p):
+        return float(np.sum(oracle.rope(q, [m], 500.0) * oracle.rope(k, [p], 500.0)))
+    assert abs(score(11, 4) - score(31, 24)) < 1e-10
+
+
+@pytest.mark.parametrize("with_bias", [True, False])
+@pytest.mark.parametrize("with_residual", [True, False])
+def test_layernorm_matches_torch(with_bias, with_residual):
+    rng = np.random.default_rng(103)
+    n, c, eps = 13, 48, 1e-5
+    x = rng.standard_normal((n, c)) * 3 + 1
+    r = rng.standard_normal((n, c)) if with_residual else None
+    w = rng.standard_normal(c)
+    b = rng.standard_normal(c) if with_bias else None
+    got = oracle.layernorm(x, w, b, eps, residual=r)
+    h = x + r if with_residual else x
+    ref = F.layer_norm(torch.from_numpy(h), (c,), torch.from_numpy(w),
+                       None if b is None else torch.from_numpy(b), eps).numpy()
+    if with_residual:
+        got, got_h = got
+        np.testing.assert_array_equal(got_h, h)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_geglu_matches_torch_exact_gelu():
+    rng = np.random.default_rng(104)
+    x = rng.standard_normal((11, 2 * 24)) * 4
+    got = oracle.geglu(x)
+    t = torch.from_numpy(x)
+    ref = (F.gelu(t[:, :24], approximate="none") * t[:, 24:]).numpy()
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+    assert oracle.geglu(np.array([[0.0, 5.0]]))[0, 0] == 0.0
+
+
 # --------------------------------------------------------------------------- input recipes
 
 def test_workload_recipes():
