@@ -52,7 +52,8 @@ const char* pe_status_string(int status);
 
 /* Version of this ABI (incremented when an entry point is added or changed;
  * 2 added pe_packed_attention_fwd_local, pe_packed_attention_bwd_local,
- * pe_rows_workspace_size, pe_pack_document_ids, pe_flatten_packed_metadata). */
+ * pe_rows_workspace_size, pe_pack_document_ids, pe_flatten_packed_metadata,
+ * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -242,6 +243,45 @@ pe_status pe_packed_attention_bwd_local(pe_dtype dtype, int32_t num_sequences,
                                         const float* lse, const void* dout, void* dq, void* dk,
                                         void* dv, void* workspace, size_t workspace_bytes,
                                         pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * The packed encoder layer tail (page "packed-encoders 0.1.0": fused
+ * LayerNorm / residual-LayerNorm / RoPE / GeGLU kernels on the flat token
+ * buffer, the token count a runtime grid dimension; position ids restart at
+ * every sequence, section "Fully packed execution"). Formulas as in
+ * ModernBERT. Every call is asynchronous on `stream`, allocates nothing and
+ * reads nothing back, so a layer tail can be captured in a CUDA graph. Tensors
+ * are contiguous device memory in the I/O dtype (bf16 or fp32); arithmetic is
+ * fp32.
+ *
+ * pe_packed_positions: positions[t] = t - cu_seqlens[i] for the sequence i
+ *   holding token t (int32 [num_tokens]); the README's lengths 5, 3, 8 give
+ *   0 1 2 3 4 0 1 2 0 1 2 3 4 5 6 7.
+ * pe_rope_packed: split-half rotary embedding in place on q [N, q_heads, D]
+ *   and k [N, k_heads, D] (k may be NULL): for i < D/2 and
+ *   a = positions[t] * theta^(-2i/D), (x[i], x[i+D/2]) becomes
+ *   (x[i] cos a - x[i+D/2] sin a, x[i+D/2] cos a + x[i] sin a). D even,
+ *   theta > 1 (ModernBERT: 160000 for global layers, 10000 for local ones).
+ *   Angles are reduced modulo 2 pi in double precision.
+ * pe_layernorm: y = (h - mean(h)) / sqrt(var(h) + eps) * weight (+ bias) per
+ *   row of C channels, biased variance, bias nullable; h = x, or with a
+ *   residual h = x + residual rounded to the I/O dtype, written to
+ *   residual_out when that is non-NULL.
+ * pe_geglu: y [N, F] = gelu(x[:, :F]) * x[:, F:] for x [N, 2F], exact (erf)
+ *   GELU.
+ * Errors: PE_ERR_INVALID_ARG for negative sizes, NULL required pointers, odd
+ * D, theta <= 1 or eps <= 0; PE_ERR_UNSUPPORTED for other dtypes or devices.
+ * ------------------------------------------------------------------------ */
+pe_status pe_packed_positions(const int32_t* cu_seqlens, int32_t num_sequences,
+                              int64_t num_tokens, int32_t* positions, pe_stream_t stream);
+pe_status pe_rope_packed(pe_dtype dtype, void* q, int32_t q_heads, void* k, int32_t k_heads,
+                         const int32_t* positions, int64_t num_tokens, int32_t head_dim,
+                         double theta, pe_stream_t stream);
+pe_status pe_layernorm(pe_dtype dtype, const void* x, const void* residual, const void* weight,
+                       const void* bias, int64_t num_tokens, int32_t channels, float eps, void* y,
+                       void* residual_out, pe_stream_t stream);
+pe_status pe_geglu(pe_dtype dtype, const void* x, int64_t num_tokens, int32_t features, void* y,
+                   pe_stream_t stream);
 
 /* Name of the kernel family that pe_packed_attention_fwd (backward = 0) or
  * pe_packed_attention_bwd (backward = 1) runs for these arguments on an sm_103a

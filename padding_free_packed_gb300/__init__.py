@@ -13,12 +13,16 @@ from .binding import (  # noqa: F401
     pe_attention_kernel,
     pe_gather_packed,
     pe_flatten_packed_metadata,
+    pe_geglu,
+    pe_layernorm,
     pe_pack_document_ids,
     pe_pack_sequences,
+    pe_packed_positions,
     pe_packed_attention_bwd,
     pe_packed_attention_bwd_local,
     pe_packed_attention_fwd,
     pe_packed_attention_fwd_local,
     pe_read_device_status,
+    pe_rope_packed,
     pe_scatter_padded,
 )

@@ -26,6 +26,7 @@ EXPORTED = (
     "pe_packed_attention_fwd", "pe_packed_attention_bwd", "pe_packed_attention_fwd_local",
     "pe_packed_attention_bwd_local", "pe_read_device_status", "pe_attention_kernel",
     "pe_rows_workspace_size", "pe_pack_document_ids", "pe_flatten_packed_metadata",
+    "pe_packed_positions", "pe_rope_packed", "pe_layernorm", "pe_geglu",
 )
 
 _lib = None
@@ -86,6 +87,14 @@ def load_library(path: str = LIB_PATH):
     lib.pe_flatten_packed_metadata.argtypes = [vp, vp, i32, i32, i32, vp, vp, c.POINTER(i64),
                                                c.POINTER(i32), vp, sz, vp]
     lib.pe_flatten_packed_metadata.restype = c.c_int
+    lib.pe_packed_positions.argtypes = [vp, i32, i64, vp, vp]
+    lib.pe_packed_positions.restype = c.c_int
+    lib.pe_rope_packed.argtypes = [c.c_int, vp, i32, vp, i32, vp, i64, i32, c.c_double, vp]
+    lib.pe_rope_packed.restype = c.c_int
+    lib.pe_layernorm.argtypes = [c.c_int, vp, vp, vp, vp, i64, i32, c.c_float, vp, vp, vp]
+    lib.pe_layernorm.restype = c.c_int
+    lib.pe_geglu.argtypes = [c.c_int, vp, i64, i32, vp, vp]
+    lib.pe_geglu.restype = c.c_int
     lib.pe_attention_kernel.argtypes = [c.c_int, i32, c.c_int, c.c_int]
     lib.pe_attention_kernel.restype = c.c_char_p
     lib.pe_read_device_status.argtypes = [vp, vp]
@@ -325,3 +334,60 @@ def pe_read_device_status(workspace: torch.Tensor) -> int:
     """Device-side status left in an attention workspace (0 = every wait completed)."""
     lib = load_library()
     return int(lib.pe_read_device_status(_ptr(workspace), _stream(workspace.device)))
+
+
+# --------------------------------------------------------------------------- layer tail
+
+def pe_packed_positions(cu_seqlens: torch.Tensor, num_tokens: int, out=None) -> torch.Tensor:
+    """Position of every token inside its own sequence (int32 [num_tokens])."""
+    lib = load_library()
+    cu = _cuda(cu_seqlens, "cu_seqlens")
+    if out is None:
+        out = torch.empty(int(num_tokens), dtype=torch.int32, device=cu.device)
+    _check("pe_packed_positions",
+           lib.pe_packed_positions(_ptr(cu), int(cu.numel()) - 1, int(num_tokens), _ptr(out),
+                                   _stream(cu.device)))
+    return out
+
+
+def pe_rope_packed(q: torch.Tensor, k: torch.Tensor | None, positions: torch.Tensor,
+                   theta: float) -> None:
+    """Split-half rotary embedding, in place, on q [N, Hq, D] and k [N, Hk, D]."""
+    lib = load_library()
+    if not (q.is_cuda and q.is_contiguous()) or (k is not None and not k.is_contiguous()):
+        raise ValueError("q and k must be contiguous CUDA tensors (rotated in place)")
+    positions = _cuda(positions, "positions").to(torch.int32)
+    n, hq, d = q.shape
+    hk = 0 if k is None else int(k.shape[1])
+    _check("pe_rope_packed",
+           lib.pe_rope_packed(_dtype_code(q.dtype), _ptr(q), hq, _ptr(k), hk, _ptr(positions), n,
+                              d, float(theta), _stream(q.device)))
+
+
+def pe_layernorm(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None = None,
+                 eps: float = 1e-5, residual: torch.Tensor | None = None, out=None):
+    """LayerNorm over the last dim of x [N, C]; with a residual, of h = x + residual
+    (rounded to x's dtype), returning (y, h). Otherwise returns y."""
+    lib = load_library()
+    x = _cuda(x, "x")
+    n, c = x.shape
+    weight = _cuda(weight, "weight").to(x.dtype)
+    bias = None if bias is None else _cuda(bias, "bias").to(x.dtype)
+    residual = None if residual is None else _cuda(residual, "residual")
+    y = torch.empty_like(x) if out is None else out
+    h = torch.empty_like(x) if residual is not None else None
+    _check("pe_layernorm",
+           lib.pe_layernorm(_dtype_code(x.dtype), _ptr(x), _ptr(residual), _ptr(weight),
+                            _ptr(bias), n, c, float(eps), _ptr(y), _ptr(h), _stream(x.device)))
+    return (y, h) if residual is not None else y
+
+
+def pe_geglu(x: torch.Tensor, out=None) -> torch.Tensor:
+    """gelu(x[:, :F]) * x[:, F:] for x [N, 2F] (exact GELU)."""
+    lib = load_library()
+    x = _cuda(x, "x")
+    n, f2 = x.shape
+    y = torch.empty((n, f2 // 2), dtype=x.dtype, device=x.device) if out is None else out
+    _check("pe_geglu", lib.pe_geglu(_dtype_code(x.dtype), _ptr(x), n, f2 // 2, _ptr(y),
+                                    _stream(x.device)))
+    return y

@@ -1,0 +1,251 @@
+// The packed encoder layer tail on the flat [N, ...] token buffer (page
+// "packed-encoders 0.1.0": fused LayerNorm / residual-LayerNorm / RoPE / GeGLU
+// kernels whose token count is a runtime grid dimension; position ids restart
+// at every sequence, section "Fully packed execution"). The formulas are
+// ModernBERT's:
+//   RoPE (split-half): for i < D/2 and a = pos * theta^(-2i/D),
+//     out[i] = x[i] cos a - x[i+D/2] sin a, out[i+D/2] = x[i+D/2] cos a + x[i] sin a;
+//   LayerNorm: y = (h - mean) / sqrt(var + eps) * w (+ b), biased variance;
+//     residual-LayerNorm: h = x + residual, stored (rounded to the I/O type)
+//     and normalised as stored;
+//   GeGLU: y[f] = gelu(x[f]) * x[F + f], exact (erf) GELU.
+// Every call is asynchronous on its stream, allocates nothing and reads
+// nothing back, so a whole layer tail can be captured in a CUDA graph. All
+// are bandwidth kernels: each element is read once from HBM and written once.
+#include <math.h>
+
+#include "pe_common.cuh"
+
+namespace pe {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// pos[cu_i + j] = j: one block per sequence (grid-stride).
+__global__ void packed_positions_kernel(const int32_t* __restrict__ cu, int32_t B,
+                                        int32_t* __restrict__ pos) {
+  for (int64_t i = blockIdx.x; i < B; i += gridDim.x) {
+    const int32_t start = __ldg(cu + i), len = __ldg(cu + i + 1) - start;
+    for (int32_t j = threadIdx.x; j < len; j += blockDim.x) pos[start + j] = j;
+  }
+}
+
+// One warp per token; lane i handles the frequency pairs i, i + 32, ... of
+// every head of q and of k. The angle pos * theta^(-2i/D) is reduced modulo
+// 2 pi in double precision (once per token and frequency, shared by all heads
+// and both tensors), so the fp32 sine and cosine keep full accuracy at long
+// positions; an fp32 product alone would be off by ~pos * 2^-24 radians.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+rope_kernel(T* __restrict__ q, int32_t hq, T* __restrict__ k, int32_t hk,
+            const int32_t* __restrict__ pos, int64_t N, int32_t D, double log2_theta) {
+  const int lane = threadIdx.x & 31;
+  const int32_t half = D / 2;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  constexpr double kTwoPi = 6.283185307179586476925;
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < N;
+       t += warps) {
+    const double p = (double)__ldg(pos + t);
+    for (int32_t i = lane; i < half; i += 32) {
+      const double a = p * exp2(-2.0 * (double)i / (double)D * log2_theta);
+      const float r = (float)(a - kTwoPi * rint(a / kTwoPi));
+      float s, c;
+      sincosf(r, &s, &c);
+      for (int32_t h = 0; h < hq; ++h) {
+        T* v = q + (t * hq + h) * D;
+        const float x1 = to_f32(v[i]), x2 = to_f32(v[i + half]);
+        v[i] = from_f32<T>(x1 * c - x2 * s);
+        v[i + half] = from_f32<T>(x2 * c + x1 * s);
+      }
+      for (int32_t h = 0; h < hk; ++h) {
+        T* v = k + (t * hk + h) * D;
+        const float x1 = to_f32(v[i]), x2 = to_f32(v[i + half]);
+        v[i] = from_f32<T>(x1 * c - x2 * s);
+        v[i + half] = from_f32<T>(x2 * c + x1 * s);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// One warp per row of C channels. h = x (+ residual, rounded to T); the mean,
+// then the variance as the mean of squared deviations, then the output - three
+// passes over the row, of which only the first reaches HBM.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+layernorm_kernel(const T* __restrict__ x, const T* __restrict__ res, const T* __restrict__ w,
+                 const T* __restrict__ b, int64_t N, int32_t C, float eps, T* __restrict__ y,
+                 T* __restrict__ res_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < N;
+       t += warps) {
+    const T* xr = x + t * C;
+    const T* rr = res ? res + t * C : nullptr;
+    auto h_at = [&](int32_t c) -> float {
+      if (!rr) return to_f32(xr[c]);
+      return to_f32(from_f32<T>(to_f32(xr[c]) + to_f32(rr[c])));  // as stored in res_out
+    };
+    float sum = 0.f;
+    for (int32_t c = lane; c < C; c += 32) {
+      const float h = h_at(c);
+      if (res_out) res_out[t * C + c] = from_f32<T>(h);
+      sum += h;
+    }
+    const float mean = warp_sum(sum) / (float)C;
+    float sq = 0.f;
+    for (int32_t c = lane; c < C; c += 32) {
+      const float d = h_at(c) - mean;
+      sq = fmaf(d, d, sq);
+    }
+    const float rstd = rsqrtf(warp_sum(sq) / (float)C + eps);
+    for (int32_t c = lane; c < C; c += 32) {
+      const float v = (h_at(c) - mean) * rstd * to_f32(w[c]) + (b ? to_f32(b[c]) : 0.f);
+      y[t * C + c] = from_f32<T>(v);
+    }
+  }
+}
+
+__device__ __forceinline__ float gelu_exact(float a) {
+  return 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
+}
+
+// y[t, f] = gelu(x[t, f]) * x[t, F + f]; V consecutive features per thread
+// (16-byte vectors when the row and pointers allow it, else V = 1).
+template <typename T, int V>
+__global__ void __launch_bounds__(kThreads)
+geglu_kernel(const T* __restrict__ x, int64_t N, int32_t F, T* __restrict__ y) {
+  const int64_t per_row = F / V;
+  const int64_t total = N * per_row;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = e / per_row;
+    const int32_t f = (int32_t)(e - t * per_row) * V;
+    const T* a = x + t * 2 * F + f;
+    const T* g = a + F;
+    T out[V];
+    if constexpr (V > 1) {
+      uint4 av = *reinterpret_cast<const uint4*>(a), gv = *reinterpret_cast<const uint4*>(g);
+      const T* ae = reinterpret_cast<const T*>(&av);
+      const T* ge = reinterpret_cast<const T*>(&gv);
+#pragma unroll
+      for (int u = 0; u < V; ++u) out[u] = from_f32<T>(gelu_exact(to_f32(ae[u])) * to_f32(ge[u]));
+      *reinterpret_cast<uint4*>(y + t * F + f) = *reinterpret_cast<const uint4*>(out);
+    } else {
+      y[t * F + f] = from_f32<T>(gelu_exact(to_f32(a[0])) * to_f32(g[0]));
+    }
+  }
+}
+
+unsigned grid_for(int64_t units_per_block_work, int64_t units) {
+  int64_t blocks = ceil_div(units, units_per_block_work);
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  return (unsigned)(blocks > 0 ? blocks : 1);
+}
+
+template <typename T>
+pe_status launch_rope(void* q, int32_t hq, void* k, int32_t hk, const int32_t* pos, int64_t N,
+                      int32_t D, double theta, cudaStream_t stream) {
+  rope_kernel<T><<<grid_for(kThreads / 32, N), kThreads, 0, stream>>>(
+      static_cast<T*>(q), hq, static_cast<T*>(k), hk, pos, N, D, log2(theta));
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+template <typename T>
+pe_status launch_layernorm(const void* x, const void* res, const void* w, const void* b,
+                           int64_t N, int32_t C, float eps, void* y, void* res_out,
+                           cudaStream_t stream) {
+  layernorm_kernel<T><<<grid_for(kThreads / 32, N), kThreads, 0, stream>>>(
+      static_cast<const T*>(x), static_cast<const T*>(res), static_cast<const T*>(w),
+      static_cast<const T*>(b), N, C, eps, static_cast<T*>(y), static_cast<T*>(res_out));
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+template <typename T>
+pe_status launch_geglu(const void* x, int64_t N, int32_t F, void* y, cudaStream_t stream) {
+  constexpr int V = 16 / sizeof(T);
+  if (F % V == 0 && aligned(x, 16) && aligned(y, 16)) {
+    geglu_kernel<T, V><<<grid_for(kThreads, N * (F / V)), kThreads, 0, stream>>>(
+        static_cast<const T*>(x), N, F, static_cast<T*>(y));
+  } else {
+    geglu_kernel<T, 1><<<grid_for(kThreads, N * F), kThreads, 0, stream>>>(
+        static_cast<const T*>(x), N, F, static_cast<T*>(y));
+  }
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+bool dtype_ok(pe_dtype d) { return d == PE_BF16 || d == PE_FP32; }
+
+}  // namespace
+
+}  // namespace pe
+
+using namespace pe;
+
+extern "C" pe_status pe_packed_positions(const int32_t* cu_seqlens, int32_t B, int64_t N,
+                                         int32_t* positions, pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (B < 0 || N < 0 || N >= (1LL << 31)) return PE_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return PE_OK;
+  if (!cu_seqlens || !positions) return PE_ERR_INVALID_ARG;
+  if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  packed_positions_kernel<<<(unsigned)(B < cap ? B : cap), kThreads, 0, stream>>>(cu_seqlens, B,
+                                                                                 positions);
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+extern "C" pe_status pe_rope_packed(pe_dtype dtype, void* q, int32_t q_heads, void* k,
+                                    int32_t k_heads, const int32_t* positions, int64_t N,
+                                    int32_t head_dim, double theta, pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!dtype_ok(dtype)) return PE_ERR_UNSUPPORTED;
+  if (N < 0 || q_heads < 0 || k_heads < 0 || head_dim < 2 || head_dim % 2 != 0 ||
+      !(theta > 1.0) || !isfinite(theta))
+    return PE_ERR_INVALID_ARG;
+  if (!k) k_heads = 0;
+  if (N == 0 || (q_heads == 0 && k_heads == 0)) return PE_OK;
+  if (!positions || (q_heads > 0 && !q)) return PE_ERR_INVALID_ARG;
+  if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  if (dtype == PE_FP32)
+    return launch_rope<float>(q, q_heads, k, k_heads, positions, N, head_dim, theta, stream);
+  return launch_rope<__nv_bfloat16>(q, q_heads, k, k_heads, positions, N, head_dim, theta, stream);
+}
+
+extern "C" pe_status pe_layernorm(pe_dtype dtype, const void* x, const void* residual,
+                                  const void* weight, const void* bias, int64_t N, int32_t C,
+                                  float eps, void* y, void* residual_out, pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!dtype_ok(dtype)) return PE_ERR_UNSUPPORTED;
+  if (N < 0 || C < 1 || !(eps > 0.f) || !isfinite(eps)) return PE_ERR_INVALID_ARG;
+  if (N == 0) return PE_OK;
+  if (!x || !weight || !y || (residual_out && !residual)) return PE_ERR_INVALID_ARG;
+  if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  if (dtype == PE_FP32)
+    return launch_layernorm<float>(x, residual, weight, bias, N, C, eps, y, residual_out, stream);
+  return launch_layernorm<__nv_bfloat16>(x, residual, weight, bias, N, C, eps, y, residual_out,
+                                         stream);
+}
+
+extern "C" pe_status pe_geglu(pe_dtype dtype, const void* x, int64_t N, int32_t F, void* y,
+                              pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!dtype_ok(dtype)) return PE_ERR_UNSUPPORTED;
+  if (N < 0 || F < 1) return PE_ERR_INVALID_ARG;
+  if (N == 0) return PE_OK;
+  if (!x || !y) return PE_ERR_INVALID_ARG;
+  if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
+  if (dtype == PE_FP32) return launch_geglu<float>(x, N, F, y, stream);
+  return launch_geglu<__nv_bfloat16>(x, N, F, y, stream);
+}
