@@ -426,6 +426,97 @@ def run_ours(args, rank, world):
     return line
 
 
+# --------------------------------------------------------------------------- layer tail
+
+# ModernBERT's feed-forward width for its hidden sizes (base, large).
+FFN_WIDTH = {768: 1152, 1024: 2624}
+
+
+def run_tail(args, rank, world):
+    """The packed encoder layer tail on a workload's packed tokens: positions,
+    RoPE on q and k, residual-LayerNorm on [N, H*d], GeGLU on [N, 2F] - all
+    bandwidth kernels, reported as algorithmic bytes per second."""
+    import torch
+
+    import padding_free_packed_gb300 as pe
+    from padding_free_packed_gb300 import workloads
+
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pe.load_library()
+    wl = workloads.WORKLOADS[args.workload]
+    lengths = workloads.draw_lengths(args.workload, np.random.default_rng(args.seed + rank))
+    n, h, d = int(lengths.sum()), wl.num_heads, wl.head_dim
+    c = h * d
+    f = FFN_WIDTH.get(c, 3 * c // 2)
+    dt = wl.torch_dtype
+    e = torch.empty((), dtype=dt).element_size()
+    gen = torch.Generator(device=dev).manual_seed(args.seed + rank)
+    mk = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(dt)
+    cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).to(dev)
+    q, k, x, resid, mlp_in = mk(n, h, d), mk(n, h, d), mk(n, c), mk(n, c), mk(n, 2 * f)
+    w = torch.ones(c, dtype=dt, device=dev)
+    b = len(lengths)
+    algo = {"positions": 4 * n + 4 * (b + 1),
+            "rope": 2 * 2 * n * c * e + 4 * n,
+            "layernorm": 4 * n * c * e + c * e,
+            "geglu": 3 * n * f * e}
+    stream = torch.cuda.current_stream(dev)
+    events = {key: [] for key in algo}
+
+    def timed(record, key, fn):
+        if not record:
+            return fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        out = fn()
+        e1.record(stream)
+        events[key].append((e0, e1))
+        return out
+
+    def step(record):
+        pos = timed(record, "positions", lambda: pe.pe_packed_positions(cu, n))
+        timed(record, "rope", lambda: pe.pe_rope_packed(q, k, pos, 160000.0))
+        timed(record, "layernorm", lambda: pe.pe_layernorm(x, w, None, 1e-5, residual=resid))
+        timed(record, "geglu", lambda: pe.pe_geglu(mlp_in))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / args.steps
+    per = {key: sum(a.elapsed_time(b) for a, b in ev) / len(ev) for key, ev in events.items()}
+    gbs = {key: algo[key] / (per[key] * 1e-3) / 1e9 for key in algo}
+    peaks, peaks_src = load_peaks()
+    dom = max(per, key=per.get)
+    total = sum(algo.values())
+    return {
+        "metric": "packed encoder layer tail HBM throughput", "value": world * total / (ms * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": args.workload, "num_tokens": n, "hidden": c, "heads": h,
+                   "head_dim": d, "ffn_width": f,
+                   "step": "positions + RoPE(q, k) + residual-LayerNorm + GeGLU",
+                   "bytes_per_step": total,
+                   "l2": "inputs larger than L2, no flush" if n * 2 * f * e > 129e6 else
+                         "inputs smaller than L2"},
+        "kernels": {key: {"ms": per[key], "gb_s": gbs[key], "bytes": algo[key]} for key in algo},
+        "roofline": {"bound": "hbm", "achieved": gbs[dom], "peak": float(peaks["hbm_gbs"]),
+                     "unit": "GB/s", "frac": gbs[dom] / float(peaks["hbm_gbs"]), "traffic": None,
+                     "peak_source": f"copy bandwidth, {peaks_src}", "kernel": dom},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 # --------------------------------------------------------------------------- oracle arms
 
 def _oracle_sample(workload: str, rows: int, seed: int, window=None):
@@ -521,6 +612,9 @@ def main():
     ap.add_argument("--window", type=int, nargs=2, metavar=("LEFT", "RIGHT"), default=None,
                     help="local attention: query at position r sees keys r-LEFT .. r+RIGHT "
                          "(negative = unbounded); e.g. 64 64 for ModernBERT's local layers")
+    ap.add_argument("--tail", action="store_true",
+                    help="time the packed encoder layer tail (positions, RoPE, residual-"
+                         "LayerNorm, GeGLU) on the workload's packed tokens instead")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=98304,
@@ -543,7 +637,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    line = run_ours(args, rank, world)
+    line = run_tail(args, rank, world) if args.tail else run_ours(args, rank, world)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

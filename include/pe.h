@@ -260,7 +260,7 @@ pe_status pe_packed_attention_bwd_local(pe_dtype dtype, int32_t num_sequences,
  * pe_rope_packed: split-half rotary embedding in place on q [N, q_heads, D]
  *   and k [N, k_heads, D] (k may be NULL): for i < D/2 and
  *   a = positions[t] * theta^(-2i/D), (x[i], x[i+D/2]) becomes
- *   (x[i] cos a - x[i+D/2] sin a, x[i+D/2] cos a + x[i] sin a). D even,
+ *   (x[i] cos a - x[i+D/2] sin a, x[i+D/2] cos a + x[i] sin a). D even, <= 256,
  *   theta > 1 (ModernBERT: 160000 for global layers, 10000 for local ones).
  *   Angles are reduced modulo 2 pi in double precision.
  * pe_layernorm: y = (h - mean(h)) / sqrt(var(h) + eps) * weight (+ bias) per

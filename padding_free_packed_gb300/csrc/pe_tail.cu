@@ -31,40 +31,82 @@ __global__ void packed_positions_kernel(const int32_t* __restrict__ cu, int32_t 
   }
 }
 
-// One warp per token; lane i handles the frequency pairs i, i + 32, ... of
-// every head of q and of k. The angle pos * theta^(-2i/D) is reduced modulo
-// 2 pi in double precision (once per token and frequency, shared by all heads
-// and both tensors), so the fp32 sine and cosine keep full accuracy at long
-// positions; an fp32 product alone would be off by ~pos * 2^-24 radians.
-template <typename T>
+// Vectors of V elements, moved as 16 bytes when V * sizeof(T) == 16.
+template <typename T, int V>
+struct Vec {
+  T e[V];
+};
+
+template <typename T, int V>
+__device__ __forceinline__ Vec<T, V> load_vec(const T* p) {
+  Vec<T, V> v;
+  if constexpr (V * sizeof(T) == 16) {
+    *reinterpret_cast<uint4*>(v.e) = *reinterpret_cast<const uint4*>(p);
+  } else {
+#pragma unroll
+    for (int u = 0; u < V; ++u) v.e[u] = p[u];
+  }
+  return v;
+}
+
+template <typename T, int V>
+__device__ __forceinline__ void store_vec(T* p, const Vec<T, V>& v) {
+  if constexpr (V * sizeof(T) == 16) {
+    *reinterpret_cast<uint4*>(p) = *reinterpret_cast<const uint4*>(v.e);
+  } else {
+#pragma unroll
+    for (int u = 0; u < V; ++u) p[u] = v.e[u];
+  }
+}
+
+// One warp per token. The angle pos * theta^(-2i/D) of each frequency i is
+// reduced modulo 2 pi in double precision once per token (lane i), shared by
+// all heads of q and k through a per-warp table of cosines and sines, so the
+// fp32 sine and cosine keep full accuracy at long positions (an fp32 product
+// alone would be off by ~pos * 2^-24 radians). The frequencies in turns per
+// position, theta^(-2i/D) / (2 pi), come from the host in double precision.
+// Lanes then move V consecutive pairs of one head at a time (16-byte vectors
+// from both halves of the row when the half-width allows it, else V = 1).
+constexpr int kMaxHalf = 128;         // head_dim <= 256
+
+struct RopeTurns {
+  double t[kMaxHalf];
+};
+
+template <typename T, int V>
 __global__ void __launch_bounds__(kThreads)
 rope_kernel(T* __restrict__ q, int32_t hq, T* __restrict__ k, int32_t hk,
-            const int32_t* __restrict__ pos, int64_t N, int32_t D, double log2_theta) {
-  const int lane = threadIdx.x & 31;
-  const int32_t half = D / 2;
+            const int32_t* __restrict__ pos, int64_t N, int32_t D, const RopeTurns turns) {
+  __shared__ float table[kThreads / 32][2][kMaxHalf];   // per warp: cos, sin
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t half = D / 2, chunks = half / V, items = (hq + hk) * chunks;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   constexpr double kTwoPi = 6.283185307179586476925;
-  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < N;
-       t += warps) {
+  float* cs = table[warp][0];
+  float* sn = table[warp][1];
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; t < N; t += warps) {
     const double p = (double)__ldg(pos + t);
     for (int32_t i = lane; i < half; i += 32) {
-      const double a = p * exp2(-2.0 * (double)i / (double)D * log2_theta);
-      const float r = (float)(a - kTwoPi * rint(a / kTwoPi));
-      float s, c;
-      sincosf(r, &s, &c);
-      for (int32_t h = 0; h < hq; ++h) {
-        T* v = q + (t * hq + h) * D;
-        const float x1 = to_f32(v[i]), x2 = to_f32(v[i + half]);
-        v[i] = from_f32<T>(x1 * c - x2 * s);
-        v[i + half] = from_f32<T>(x2 * c + x1 * s);
-      }
-      for (int32_t h = 0; h < hk; ++h) {
-        T* v = k + (t * hk + h) * D;
-        const float x1 = to_f32(v[i]), x2 = to_f32(v[i + half]);
-        v[i] = from_f32<T>(x1 * c - x2 * s);
-        v[i + half] = from_f32<T>(x2 * c + x1 * s);
-      }
+      const double a = p * turns.t[i];                      // in turns
+      const float r = (float)((a - rint(a)) * kTwoPi);      // in radians, |r| <= pi
+      sincosf(r, &sn[i], &cs[i]);
     }
+    __syncwarp();
+    for (int32_t item = lane; item < items; item += 32) {
+      const int32_t h = item / chunks, i0 = (item - h * chunks) * V;
+      T* v = h < hq ? q + (t * hq + h) * D : k + (t * hk + (h - hq)) * D;
+      Vec<T, V> x1 = load_vec<T, V>(v + i0), x2 = load_vec<T, V>(v + i0 + half);
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const float a1 = to_f32(x1.e[u]), a2 = to_f32(x2.e[u]);
+        const float c = cs[i0 + u], s2 = sn[i0 + u];
+        x1.e[u] = from_f32<T>(a1 * c - a2 * s2);
+        x2.e[u] = from_f32<T>(a2 * c + a1 * s2);
+      }
+      store_vec<T, V>(v + i0, x1);
+      store_vec<T, V>(v + i0 + half, x2);
+    }
+    __syncwarp();                                           // the table is rewritten next token
   }
 }
 
@@ -76,8 +118,10 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // One warp per row of C channels. h = x (+ residual, rounded to T); the mean,
 // then the variance as the mean of squared deviations, then the output - three
-// passes over the row, of which only the first reaches HBM.
-template <typename T>
+// passes over the row, of which only the first reaches HBM. Lanes move V
+// consecutive channels at a time (16-byte vectors when C and the pointers
+// allow, else V = 1).
+template <typename T, int V>
 __global__ void __launch_bounds__(kThreads)
 layernorm_kernel(const T* __restrict__ x, const T* __restrict__ res, const T* __restrict__ w,
                  const T* __restrict__ b, int64_t N, int32_t C, float eps, T* __restrict__ y,
@@ -88,26 +132,53 @@ layernorm_kernel(const T* __restrict__ x, const T* __restrict__ res, const T* __
        t += warps) {
     const T* xr = x + t * C;
     const T* rr = res ? res + t * C : nullptr;
-    auto h_at = [&](int32_t c) -> float {
-      if (!rr) return to_f32(xr[c]);
-      return to_f32(from_f32<T>(to_f32(xr[c]) + to_f32(rr[c])));  // as stored in res_out
+    // h of channels c .. c+V-1, as stored in res_out.
+    auto h_at = [&](int32_t c, float (&h)[V]) {
+      const Vec<T, V> xv = load_vec<T, V>(xr + c);
+      if (rr) {
+        const Vec<T, V> rv = load_vec<T, V>(rr + c);
+#pragma unroll
+        for (int u = 0; u < V; ++u) h[u] = to_f32(from_f32<T>(to_f32(xv.e[u]) + to_f32(rv.e[u])));
+      } else {
+#pragma unroll
+        for (int u = 0; u < V; ++u) h[u] = to_f32(xv.e[u]);
+      }
     };
     float sum = 0.f;
-    for (int32_t c = lane; c < C; c += 32) {
-      const float h = h_at(c);
-      if (res_out) res_out[t * C + c] = from_f32<T>(h);
-      sum += h;
+    for (int32_t c = lane * V; c < C; c += 32 * V) {
+      float h[V];
+      h_at(c, h);
+      if (res_out) {
+        Vec<T, V> hv;
+#pragma unroll
+        for (int u = 0; u < V; ++u) hv.e[u] = from_f32<T>(h[u]);
+        store_vec<T, V>(res_out + t * C + c, hv);
+      }
+#pragma unroll
+      for (int u = 0; u < V; ++u) sum += h[u];
     }
     const float mean = warp_sum(sum) / (float)C;
     float sq = 0.f;
-    for (int32_t c = lane; c < C; c += 32) {
-      const float d = h_at(c) - mean;
-      sq = fmaf(d, d, sq);
+    for (int32_t c = lane * V; c < C; c += 32 * V) {
+      float h[V];
+      h_at(c, h);
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const float d = h[u] - mean;
+        sq = fmaf(d, d, sq);
+      }
     }
     const float rstd = rsqrtf(warp_sum(sq) / (float)C + eps);
-    for (int32_t c = lane; c < C; c += 32) {
-      const float v = (h_at(c) - mean) * rstd * to_f32(w[c]) + (b ? to_f32(b[c]) : 0.f);
-      y[t * C + c] = from_f32<T>(v);
+    for (int32_t c = lane * V; c < C; c += 32 * V) {
+      float h[V];
+      h_at(c, h);
+      const Vec<T, V> wv = load_vec<T, V>(w + c);
+      Vec<T, V> out;
+#pragma unroll
+      for (int u = 0; u < V; ++u)
+        out.e[u] = from_f32<T>((h[u] - mean) * rstd * to_f32(wv.e[u]) +
+                               (b ? to_f32(b[c + u]) : 0.f));
+      store_vec<T, V>(y + t * C + c, out);
     }
   }
 }
@@ -153,8 +224,19 @@ unsigned grid_for(int64_t units_per_block_work, int64_t units) {
 template <typename T>
 pe_status launch_rope(void* q, int32_t hq, void* k, int32_t hk, const int32_t* pos, int64_t N,
                       int32_t D, double theta, cudaStream_t stream) {
-  rope_kernel<T><<<grid_for(kThreads / 32, N), kThreads, 0, stream>>>(
-      static_cast<T*>(q), hq, static_cast<T*>(k), hk, pos, N, D, log2(theta));
+  RopeTurns turns;
+  const double two_pi = 6.283185307179586476925;
+  for (int i = 0; i < kMaxHalf; ++i)
+    turns.t[i] = i < D / 2 ? pow(theta, -2.0 * i / D) / two_pi : 0.0;
+  constexpr int V = 16 / sizeof(T);
+  const unsigned grid = grid_for(kThreads / 32, N);
+  const bool vec = (D / 2) % V == 0 && aligned(q, 16) && (!k || aligned(k, 16));
+  if (vec)
+    rope_kernel<T, V><<<grid, kThreads, 0, stream>>>(static_cast<T*>(q), hq, static_cast<T*>(k),
+                                                      hk, pos, N, D, turns);
+  else
+    rope_kernel<T, 1><<<grid, kThreads, 0, stream>>>(static_cast<T*>(q), hq, static_cast<T*>(k),
+                                                      hk, pos, N, D, turns);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }
@@ -163,7 +245,11 @@ template <typename T>
 pe_status launch_layernorm(const void* x, const void* res, const void* w, const void* b,
                            int64_t N, int32_t C, float eps, void* y, void* res_out,
                            cudaStream_t stream) {
-  layernorm_kernel<T><<<grid_for(kThreads / 32, N), kThreads, 0, stream>>>(
+  constexpr int V = 16 / sizeof(T);
+  const bool vec = C % V == 0 && aligned(x, 16) && aligned(w, 16) && aligned(y, 16) &&
+                   (!res || aligned(res, 16)) && (!res_out || aligned(res_out, 16));
+  auto kernel = vec ? layernorm_kernel<T, V> : layernorm_kernel<T, 1>;
+  kernel<<<grid_for(kThreads / 32, N), kThreads, 0, stream>>>(
       static_cast<const T*>(x), static_cast<const T*>(res), static_cast<const T*>(w),
       static_cast<const T*>(b), N, C, eps, static_cast<T*>(y), static_cast<T*>(res_out));
   PE_CUDA_TRY(cudaGetLastError());
@@ -212,6 +298,7 @@ extern "C" pe_status pe_rope_packed(pe_dtype dtype, void* q, int32_t q_heads, vo
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!dtype_ok(dtype)) return PE_ERR_UNSUPPORTED;
   if (N < 0 || q_heads < 0 || k_heads < 0 || head_dim < 2 || head_dim % 2 != 0 ||
+      head_dim > 2 * kMaxHalf ||
       !(theta > 1.0) || !isfinite(theta))
     return PE_ERR_INVALID_ARG;
   if (!k) k_heads = 0;
