@@ -245,7 +245,10 @@ def run_ours(args, rank, world):
         events.append((e0, e1))
         return result
 
-    def step(lengths_t, grids, record):
+    def step(lengths_t, grids, record, outs=None):
+        # outs: (output buffer, gradient buffers) to write into; the shared
+        # ones by default, a pipeline buffer set in the end-to-end leg.
+        o_buf, g_bufs = outs if outs is not None else (og, grad_grids)
         if args.packed:
             cu = packed_cu
             q, k, v = grids[:3]
@@ -262,14 +265,14 @@ def run_ours(args, rank, world):
         out, lse = timed(record, fwd_events,
                          lambda: attention_fwd(q, k, v, cu, s, wl.scale, need_lse=train))
         if args.packed or rows_layout:
-            og.copy_(out)          # packed rows: the output stays packed (a THD consumer)
+            o_buf.copy_(out)       # packed rows: the output stays packed (a THD consumer)
         else:
-            pe.pe_scatter_padded(out, cu, s, out=og)
+            pe.pe_scatter_padded(out, cu, s, out=o_buf)
         if train:
             do = grids[3] if args.packed else pe.pe_gather_packed(grids[3], flat, n)
             grads = timed(record, bwd_events,
                           lambda: attention_bwd(do, q, k, v, out, lse, cu, s, wl.scale))
-            for g, grid in zip(grads, grad_grids):
+            for g, grid in zip(grads, g_bufs):
                 if args.packed or rows_layout:
                     grid.copy_(g)
                 else:
@@ -311,34 +314,75 @@ def run_ours(args, rank, world):
     ms_per_step = elapsed_ms / args.steps
 
     # End to end through the same public calls: pinned host grids in, padded
-    # output back to pinned host memory, copies inside the timed region.
+    # output (and gradients) back to pinned host memory, every step's copies
+    # inside the timed region. Steps are pipelined as a serving or training
+    # loop would run them: the host-to-device copies of step i+1 (on their own
+    # stream) and the device-to-host copy of step i-1's result (on a third)
+    # overlap step i's compute, with two buffer sets alternating.
     e2e = None
     if not args.no_e2e:
         host_in = [t.pin_memory() for t in host_grids]
         hlen = torch.from_numpy(meta_host).pin_memory()
-        dev_in = [torch.empty_like(t, device=dev) for t in host_in]
-        dlen = torch.empty_like(lengths_d)
-        results = [og] + (grad_grids if train else [])
-        host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in results]
+        nbuf = 2
+        dev_in = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(nbuf)]
+        dlen = [torch.empty_like(lengths_d) for _ in range(nbuf)]
+        outs = [(torch.empty_like(og), [torch.empty_like(g) for g in grad_grids] if train else None)
+                for _ in range(nbuf)]
+        host_out = [[torch.empty_like(t, device="cpu").pin_memory()
+                     for t in [o] + (g if g is not None else [])] for o, g in outs]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        comp = stream
+        in_free = [torch.cuda.Event() for _ in range(nbuf)]    # compute done with inputs b
+        in_ready = [torch.cuda.Event() for _ in range(nbuf)]   # inputs b uploaded
+        out_ready = [torch.cuda.Event() for _ in range(nbuf)]  # results b computed
+        out_free = [torch.cuda.Event() for _ in range(nbuf)]   # results b downloaded
+        for b in range(nbuf):
+            for ev in (in_free[b], out_free[b]):
+                ev.record(comp)
 
-        def e2e_step():
-            dlen.copy_(hlen, non_blocking=True)
-            for dst, src in zip(dev_in, host_in):
-                dst.copy_(src, non_blocking=True)
-            step(dlen, dev_in, False)
-            for dst, src in zip(host_out, results):
-                dst.copy_(src, non_blocking=True)
+        def upload(i):
+            b = i % nbuf
+            up.wait_event(in_free[b])
+            with torch.cuda.stream(up):
+                dlen[b].copy_(hlen, non_blocking=True)
+                for dst, src in zip(dev_in[b], host_in):
+                    dst.copy_(src, non_blocking=True)
+                in_ready[b].record(up)
 
-        for _ in range(max(1, min(args.warmup, 3))):
-            e2e_step()
+        def compute_and_download(i):
+            b = i % nbuf
+            comp.wait_event(in_ready[b])
+            comp.wait_event(out_free[b])
+            step(dlen[b], dev_in[b], False, outs[b])
+            in_free[b].record(comp)
+            out_ready[b].record(comp)
+            down.wait_event(out_ready[b])
+            with torch.cuda.stream(down):
+                results = [outs[b][0]] + (outs[b][1] if train else [])
+                for dst, src in zip(host_out[b], results):
+                    dst.copy_(src, non_blocking=True)
+                out_free[b].record(down)
+
+        def run(n):
+            upload(0)
+            for i in range(n):
+                if i + 1 < n:
+                    upload(i + 1)              # the next step's inputs, during this compute
+                compute_and_download(i)
+
+        run(max(2, min(args.warmup, 3)))
+        torch.cuda.synchronize(dev)
         barrier()
-        e2e_steps = max(1, min(args.steps, 10))
+        e2e_steps = max(2, min(args.steps, 10))
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        t1.record(stream)
+        t0.record(comp)
+        up.wait_event(t0)
+        run(e2e_steps)
+        comp.wait_stream(down)
+        comp.wait_stream(up)
+        t1.record(comp)
+        torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = t0.elapsed_time(t1) / e2e_steps
         if world > 1:
@@ -346,9 +390,10 @@ def run_ours(args, rank, world):
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e2e_ms = float(t.item())
         h2d = sum(x.numel() * x.element_size() for x in [hlen] + host_in)
-        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        d2h = sum(x.numel() * x.element_size() for x in host_out[0])
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "pipelined": "uploads of step i+1 and downloads of step i-1 overlap step i"}
 
     peaks, peaks_src = load_peaks()
     # The dominant kernel: the forward, or the backward when it takes longer.
