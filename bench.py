@@ -320,7 +320,10 @@ def run_ours(args, rank, world):
     # stream) and the device-to-host copy of step i-1's result (on a third)
     # overlap step i's compute, with two buffer sets alternating.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not (args.packed or rows_layout):
+        e2e = e2e_padded(args, pe, torch, dev, stream, lengths, host_grids, s, wl, train,
+                         flops, n_tokens, attention_fwd, attention_bwd, barrier, world)
+    elif not args.no_e2e:
         host_in = [t.pin_memory() for t in host_grids]
         hlen = torch.from_numpy(meta_host).pin_memory()
         nbuf = 2
@@ -469,6 +472,110 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows, args.seed, window)
     return line
+
+
+# --------------------------------------------------------------------------- end to end
+
+def e2e_padded(args, pe, torch, dev, comp, lengths, host_grids, s, wl, train, flops, n_tokens,
+               attention_fwd, attention_bwd, barrier, world):
+    """End to end from pinned host memory through the public calls, every step
+    inside the timed region: upload the lengths and pack (its one host read),
+    upload the real rows of the pinned padded q, k, v (and dO) grids straight
+    into packed device buffers with the copy engines (pe_upload_packed: one
+    copy per sequence, no padding crosses the host link), attention (and
+    backward), scatter the padded output (and gradients) on the device and
+    copy them back to pinned host memory. Steps are pipelined over four
+    streams with two buffer sets: step i+1's uploads and step i-1's download
+    overlap step i's attention (the copy engines need no SMs)."""
+    host_in = [t.pin_memory() for t in host_grids]
+    hlen = torch.from_numpy(lengths).pin_memory()
+    nbuf = 2
+    io, up, down = (torch.cuda.Stream(dev) for _ in range(3))
+    row_shape = tuple(host_in[0].shape[2:])
+    dlen = [torch.empty(lengths.shape, dtype=torch.int32, device=dev) for _ in range(nbuf)]
+    packed = [[torch.empty((n_tokens,) + row_shape, dtype=t.dtype, device=dev) for t in host_in]
+              for _ in range(nbuf)]
+    n_out = 4 if train else 1
+    dev_out = [[torch.empty_like(host_in[0], device=dev) for _ in range(n_out)]
+               for _ in range(nbuf)]
+    host_out = [[torch.empty_like(host_in[0]).pin_memory() for _ in range(n_out)]
+                for _ in range(nbuf)]
+    state = [None] * nbuf
+    ev = {name: [torch.cuda.Event() for _ in range(nbuf)]
+          for name in ("packed", "uploaded", "computed", "downloaded")}
+    for b in range(nbuf):
+        ev["computed"][b].record(comp)
+        ev["downloaded"][b].record(comp)
+
+    def prep(i):
+        b = i % nbuf
+        with torch.cuda.stream(io):
+            io.wait_event(ev["computed"][b])      # buffer set b is free again
+            dlen[b].copy_(hlen, non_blocking=True)
+            _, cu, _ = pe.pe_pack_sequences(dlen[b], s)
+            cu.record_stream(comp)
+            state[b] = cu
+            ev["packed"][b].record(io)
+        with torch.cuda.stream(up):
+            up.wait_event(ev["computed"][b])
+            for src, dst in zip(host_in, packed[b]):
+                pe.pe_upload_packed(src, lengths, out=dst)
+            ev["uploaded"][b].record(up)
+
+    def compute(i):
+        b = i % nbuf
+        comp.wait_event(ev["packed"][b])
+        comp.wait_event(ev["uploaded"][b])
+        comp.wait_event(ev["downloaded"][b])     # step i-2's results have left the device
+        cu = state[b]
+        q, k, v = packed[b][:3]
+        out, lse = attention_fwd(q, k, v, cu, s, wl.scale, need_lse=train)
+        results = [out]
+        if train:
+            results += list(attention_bwd(packed[b][3], q, k, v, out, lse, cu, s, wl.scale))
+        for src, dst in zip(results, dev_out[b]):
+            pe.pe_scatter_padded(src, cu, s, out=dst)
+        ev["computed"][b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev["computed"][b])
+            for src, dst in zip(dev_out[b], host_out[b]):
+                dst.copy_(src, non_blocking=True)
+            ev["downloaded"][b].record(down)
+
+    def run(n):
+        prep(0)
+        for i in range(n):
+            if i + 1 < n:
+                prep(i + 1)                       # overlaps step i's attention
+            compute(i)
+
+    run(max(2, min(args.warmup, 3)))
+    torch.cuda.synchronize(dev)
+    barrier()
+    steps = max(2, min(args.steps, 10))
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(comp)
+    for st in (io, up, down):
+        st.wait_event(t0)
+    run(steps)
+    for st in (io, up, down):
+        comp.wait_stream(st)
+    t1.record(comp)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = t0.elapsed_time(t1) / steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    row_bytes = host_in[0].element_size() * int(np.prod(row_shape))
+    h2d = hlen.numel() * hlen.element_size() + len(host_in) * n_tokens * row_bytes
+    d2h = n_out * host_in[0].numel() * host_in[0].element_size()
+    return {"value": world * flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "real rows of the pinned padded inputs uploaded by the copy engines "
+                    "(pe_upload_packed), padded results copied back; step i+1's uploads and "
+                    "step i-1's download overlap step i"}
 
 
 # --------------------------------------------------------------------------- layer tail

@@ -53,7 +53,7 @@ const char* pe_status_string(int status);
 /* Version of this ABI (incremented when an entry point is added or changed;
  * 2 added pe_packed_attention_fwd_local, pe_packed_attention_bwd_local,
  * pe_rows_workspace_size, pe_pack_document_ids, pe_flatten_packed_metadata,
- * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu). */
+ * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu, pe_upload_packed). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -87,8 +87,12 @@ pe_status pe_pack_sequences(const int32_t* lengths, int32_t num_sequences, int32
  * Padded -> packed gather: packed[t, :] = padded[flat_index[t], :]
  * (module docstring, "Data flow of a packed forward": grid.flatten()[flat_index]).
  *
- * padded:     device, rows of row_bytes bytes (any number of rows; every
- *             flat_index value must name one of them).
+ * padded:     device memory, or pinned host memory mapped into the device
+ *             address space (cudaHostAlloc / cudaHostRegister memory, mapped
+ *             by default under unified addressing): the kernel then reads only
+ *             the real rows across the host link, with no separate copy of
+ *             the padded grid. Rows of row_bytes bytes (any number of rows;
+ *             every flat_index value must name one of them).
  * flat_index: int64 [num_tokens], device (from pe_pack_sequences).
  * packed:     device, [num_tokens] rows of row_bytes bytes.
  * 16-byte vector copies when row_bytes and both pointers are 16-byte aligned,
@@ -98,13 +102,37 @@ pe_status pe_gather_packed(const void* padded, const int64_t* flat_index, int64_
                            int64_t row_bytes, void* packed, pe_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Host padded grid -> packed device buffer with the copy engines: the same
+ * result as pe_gather_packed on a grid in host memory, for callers that hold
+ * the lengths on the host. Sequence i's rows are one contiguous run in both
+ * layouts (padded rows i*max_seq_len .. +L_i-1, packed rows cu_i .. +L_i-1),
+ * so the call enqueues one asynchronous host-to-device copy per sequence on
+ * `stream` and returns: only real rows cross the host link, and no kernel
+ * runs, so the copies overlap kernels running on other streams.
+ *
+ * padded_host:  host memory (pinned for asynchronous copies), [num_sequences *
+ *               max_seq_len] rows of row_bytes bytes.
+ * lengths_host: int32 [num_sequences], host; 1 <= L_i <= max_seq_len, else
+ *               PE_ERR_BAD_LENGTH before any copy; PE_ERR_OVERFLOW if
+ *               sum L_i >= 2^31.
+ * packed:       device, [sum L_i] rows of row_bytes bytes.
+ * The host buffers must stay valid until the copies complete.
+ * ------------------------------------------------------------------------ */
+pe_status pe_upload_packed(const void* padded_host, const int32_t* lengths_host,
+                           int32_t num_sequences, int32_t max_seq_len, int64_t row_bytes,
+                           void* packed, pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Packed -> padded scatter with zero fill (function _padded_packed_attention,
  * which unpacks with to_dense_batch, fill value 0):
  *   padded[i*max_seq_len + j, :] = j < L_i ? packed[cu_seqlens[i] + j, :] : 0
  *
  * packed:     device, [cu_seqlens[num_sequences]] rows of row_bytes bytes.
  * cu_seqlens: int32 [num_sequences + 1], device (trusted output of pack).
- * padded:     device, [num_sequences * max_seq_len] rows; every row is written.
+ * padded:     device memory, or pinned host memory mapped into the device
+ *             address space (then the kernel writes the rows across the host
+ *             link, with no separate copy back): [num_sequences * max_seq_len]
+ *             rows; every row is written.
  * ------------------------------------------------------------------------ */
 pe_status pe_scatter_padded(const void* packed, const int32_t* cu_seqlens, int32_t num_sequences,
                             int32_t max_seq_len, int64_t row_bytes, void* padded,

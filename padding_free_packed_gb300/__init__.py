@@ -25,4 +25,5 @@ from .binding import (  # noqa: F401
     pe_read_device_status,
     pe_rope_packed,
     pe_scatter_padded,
+    pe_upload_packed,
 )

@@ -12,6 +12,7 @@ import ctypes
 import math
 import os
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +27,7 @@ EXPORTED = (
     "pe_packed_attention_fwd", "pe_packed_attention_bwd", "pe_packed_attention_fwd_local",
     "pe_packed_attention_bwd_local", "pe_read_device_status", "pe_attention_kernel",
     "pe_rows_workspace_size", "pe_pack_document_ids", "pe_flatten_packed_metadata",
-    "pe_packed_positions", "pe_rope_packed", "pe_layernorm", "pe_geglu",
+    "pe_packed_positions", "pe_rope_packed", "pe_layernorm", "pe_geglu", "pe_upload_packed",
 )
 
 _lib = None
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH):
     lib.pe_flatten_packed_metadata.argtypes = [vp, vp, i32, i32, i32, vp, vp, c.POINTER(i64),
                                                c.POINTER(i32), vp, sz, vp]
     lib.pe_flatten_packed_metadata.restype = c.c_int
+    lib.pe_upload_packed.argtypes = [vp, vp, i32, i32, i64, vp, vp]
+    lib.pe_upload_packed.restype = c.c_int
     lib.pe_packed_positions.argtypes = [vp, i32, i64, vp, vp]
     lib.pe_packed_positions.restype = c.c_int
     lib.pe_rope_packed.argtypes = [c.c_int, vp, i32, vp, i32, vp, i64, i32, c.c_double, vp]
@@ -125,6 +128,15 @@ def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
     return t.contiguous()
+
+
+def _cuda_or_pinned(t: torch.Tensor, name: str) -> torch.Tensor:
+    """A CUDA tensor, or a pinned host tensor that kernels address directly."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -190,26 +202,52 @@ def pe_flatten_packed_metadata(token_indices: torch.Tensor, row_cu_seqlens: torc
     return flat[: n.value], cu[: d.value + 1], int(n.value)
 
 
-def pe_gather_packed(padded: torch.Tensor, flat_index: torch.Tensor, num_tokens: int | None = None):
-    """packed[t] = padded.flatten(0, 1)[flat_index[t]] for a [B, S, ...] grid."""
+def pe_gather_packed(padded: torch.Tensor, flat_index: torch.Tensor, num_tokens: int | None = None,
+                     out: torch.Tensor | None = None):
+    """packed[t] = padded.flatten(0, 1)[flat_index[t]] for a [B, S, ...] grid.
+    The grid may be pinned host memory: only the real rows cross the host link."""
     lib = load_library()
-    padded = _cuda(padded, "padded")
+    padded = _cuda_or_pinned(padded, "padded")
     flat_index = _cuda(flat_index, "flat_index")
+    dev = flat_index.device
     n = int(flat_index.numel()) if num_tokens is None else int(num_tokens)
     row_shape = tuple(padded.shape[2:])
-    packed = torch.empty((n,) + row_shape, dtype=padded.dtype, device=padded.device)
+    packed = (torch.empty((n,) + row_shape, dtype=padded.dtype, device=dev) if out is None
+              else out)
     row_bytes = padded.element_size() * math.prod(row_shape)
     _check("pe_gather_packed",
            lib.pe_gather_packed(_ptr(padded), _ptr(flat_index), n, row_bytes, _ptr(packed),
-                                _stream(padded.device)))
+                                _stream(dev)))
     return packed
+
+
+def pe_upload_packed(padded_host: torch.Tensor, lengths_host, out: torch.Tensor) -> torch.Tensor:
+    """Copies the real rows of a host [B, S, ...] grid into the packed device
+    buffer `out` [sum L, ...] with one asynchronous copy per sequence on the
+    current stream of out's device (pinned host memory for asynchrony)."""
+    lib = load_library()
+    if padded_host.is_cuda or not padded_host.is_contiguous():
+        raise ValueError("padded_host must be a contiguous host tensor")
+    lengths = np.ascontiguousarray(np.asarray(lengths_host, dtype=np.int32))
+    b, s = int(padded_host.shape[0]), int(padded_host.shape[1])
+    if lengths.shape != (b,):
+        raise ValueError("one length per grid row")
+    out = _cuda(out, "out")
+    row_bytes = padded_host.element_size() * math.prod(tuple(padded_host.shape[2:]))
+    _check("pe_upload_packed",
+           lib.pe_upload_packed(_ptr(padded_host), lengths.ctypes.data, b, s, row_bytes,
+                                _ptr(out), _stream(out.device)))
+    return out
 
 
 def pe_scatter_padded(packed: torch.Tensor, cu_seqlens: torch.Tensor, max_seq_len: int,
                       out: torch.Tensor | None = None):
-    """Returns the zero-padded [B, S, ...] grid of a packed [N, ...] buffer."""
+    """Returns the zero-padded [B, S, ...] grid of a packed [N, ...] buffer; `out`
+    may be pinned host memory (the rows are then written across the host link)."""
     lib = load_library()
     packed = _cuda(packed, "packed")
+    if out is not None:
+        out = _cuda_or_pinned(out, "out")
     cu_seqlens = _cuda(cu_seqlens, "cu_seqlens")
     b = int(cu_seqlens.numel()) - 1
     row_shape = tuple(packed.shape[1:])

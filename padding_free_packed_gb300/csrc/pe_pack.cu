@@ -303,3 +303,31 @@ extern "C" pe_status pe_scatter_padded(const void* packed, const int32_t* cu_seq
     return launch_scatter<uint32_t>(packed, cu_seqlens, B, S, row_bytes, padded, stream);
   return launch_scatter<uint8_t>(packed, cu_seqlens, B, S, row_bytes, padded, stream);
 }
+
+// Host-resident padded grid -> packed device buffer with the copy engines:
+// sequence i's rows are one contiguous run in both layouts, so each is one
+// asynchronous copy (no SM work; overlaps kernels on other streams).
+extern "C" pe_status pe_upload_packed(const void* padded_host, const int32_t* lengths_host,
+                                      int32_t B, int32_t S, int64_t row_bytes, void* packed,
+                                      pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (B < 0 || S < 1 || row_bytes < 1) return PE_ERR_INVALID_ARG;
+  if (B == 0) return PE_OK;
+  if (!padded_host || !lengths_host || !packed) return PE_ERR_INVALID_ARG;
+  int64_t total = 0;
+  for (int32_t i = 0; i < B; ++i) {
+    if (lengths_host[i] < 1 || lengths_host[i] > S) return PE_ERR_BAD_LENGTH;
+    total += lengths_host[i];
+  }
+  if (total >= (1LL << 31)) return PE_ERR_OVERFLOW;
+  const char* src = static_cast<const char*>(padded_host);
+  char* dst = static_cast<char*>(packed);
+  int64_t t = 0;
+  for (int32_t i = 0; i < B; ++i) {
+    PE_CUDA_TRY(cudaMemcpyAsync(dst + t * row_bytes, src + (int64_t)i * S * row_bytes,
+                                (size_t)lengths_host[i] * row_bytes, cudaMemcpyHostToDevice,
+                                stream));
+    t += lengths_host[i];
+  }
+  return PE_OK;
+}

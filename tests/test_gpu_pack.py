@@ -118,3 +118,36 @@ def test_longdoc_gather_and_scatter_full_size():
     want_grid = oracle.scatter_rows(want, o_cu, wl.max_seq_len)
     assert np.array_equal(back.cpu().view(torch.uint8).reshape(len(lengths), wl.max_seq_len, -1)
                           .numpy(), want_grid)
+
+
+@pytest.mark.parametrize("dtype,row", [(torch.bfloat16, (4, 64)), (torch.float32, (3, 5))])
+def test_host_grids_upload_gather_and_scatter(dtype, row):
+    """Host-resident padded grids: pe_upload_packed (copy engines, one copy per
+    sequence) and pe_gather_packed on pinned host memory both give the device
+    gather's packed buffer bit for bit; pe_scatter_padded into pinned host
+    memory gives the device scatter's grid."""
+    lengths = np.array([1, 77, 128, 5, 300, 2], np.int32)
+    s = 300
+    rng = np.random.default_rng(11)
+    grid = torch.from_numpy(rng.standard_normal((len(lengths), s) + row).astype(np.float32))
+    grid = grid.to(dtype).pin_memory()
+    flat, cu, n = pe.pe_pack_sequences(torch.from_numpy(lengths).to(DEV), s)
+    want = pe.pe_gather_packed(grid.to(DEV), flat, n)
+    up = torch.empty_like(want)
+    pe.pe_upload_packed(grid, lengths, out=up)
+    torch.cuda.synchronize()
+    assert torch.equal(up, want)
+    assert torch.equal(pe.pe_gather_packed(grid, flat, n), want)
+    host = torch.empty_like(grid).pin_memory()
+    pe.pe_scatter_padded(want, cu, s, out=host)
+    torch.cuda.synchronize()
+    assert torch.equal(host, pe.pe_scatter_padded(want, cu, s).cpu())
+
+
+def test_upload_rejects_bad_lengths():
+    grid = torch.zeros((2, 4, 8), dtype=torch.float32).pin_memory()
+    out = torch.empty((9, 8), device=DEV)
+    with pytest.raises(pe.PackedAttentionError):
+        pe.pe_upload_packed(grid, [5, 4], out=out)      # 5 > max_seq_len
+    with pytest.raises(pe.PackedAttentionError):
+        pe.pe_upload_packed(grid, [0, 4], out=out)
