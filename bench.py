@@ -172,7 +172,7 @@ def run_ours(args, rank, world):
     pe.load_library()
     wl = workloads.WORKLOADS[args.workload]
     # Weak scaling: every rank draws its own batch of the same workload.
-    train = wl.backward
+    train = wl.backward or args.backward
     rows_layout = args.layout == "rows"
     if rows_layout:
         # Documents packed several to a padded row (an indexed packing mask).
@@ -767,6 +767,8 @@ def main():
     ap.add_argument("--tail", action="store_true",
                     help="time the packed encoder layer tail (positions, RoPE, residual-"
                          "LayerNorm, GeGLU) on the workload's packed tokens instead")
+    ap.add_argument("--backward", action="store_true",
+                    help="add the attention backward (dO ~ N(0,1)) to a forward-only workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=98304,
