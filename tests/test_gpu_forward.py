@@ -100,6 +100,29 @@ def test_ragged_tile_boundaries(dtype, d):
         check(out1, ref[cu[:-1]], tag, f"ragged first-token d={d}")
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.float32, 64), (torch.float32, 72), (torch.float32, 128),
+                                     (torch.float32, 16), (torch.bfloat16, 96)])
+@pytest.mark.parametrize("window", [None, (10, 40), (40, 3)])
+def test_ffma_half_tile_boundaries(dtype, d, window):
+    """The FFMA kernel computes 32 rows of a tile with at most 32 real rows and
+    32 keys of a block with at most 32 real keys: tails of 31, 32 and 33 rows
+    and keys on each side of those edges, with and without a window."""
+    lengths = [31, 32, 33, 95, 96, 97, 160, 161, 4, 40, 225]
+    x = workloads.make_custom(lengths, 2, d, dtype, seed=9)
+    s = max(lengths)
+    cu, cu_d, q, k, v = _device_inputs(x)
+    scale = 1.0 / math.sqrt(d)
+    if window is None:
+        out, lse = pe.pe_packed_attention_fwd(q, k, v, cu_d, s, scale, need_lse=True)
+    else:
+        out, lse = pe.pe_packed_attention_fwd_local(q, k, v, cu_d, s, window[0], window[1], scale,
+                                                    need_lse=True)
+    ref, ref_lse = oracle.attention_fwd(x.q, x.k, x.v, cu, s, scale, window=window or (-1, -1))
+    tag = "fp32" if dtype == torch.float32 else "bf16"
+    check(out, ref, tag, f"half tiles d={d} window={window}")
+    assert float(np.abs(to64(lse) - ref_lse).max()) <= _lse_tol(tag)
+
+
 def test_length_one_sequences_output_their_value():
     x = workloads.make_custom([1] * 300, 4, 64, torch.bfloat16, seed=6)
     cu, cu_d, q, k, v = _device_inputs(x)
