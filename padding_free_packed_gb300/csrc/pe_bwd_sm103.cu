@@ -24,9 +24,13 @@
 //   warps 3, 4   issue the accumulations (warp 4 only in the key pass). A single
 //                thread issues one tcgen05.mma per ~130 cycles, hence four issuers.
 //   warps 8-15   elementwise step: warps 8-11 take columns 0-63, warps 12-15
-//                columns 64-127; one thread per TMEM lane (tile row), 32-column
-//                chunks, P and dS packed to bf16 into tensor memory. Then the
-//                epilogue (scale, store the rows inside the sequence).
+//                columns 64-127; one thread per TMEM lane (tile row). A warp
+//                loads its 64 columns of both products into registers and
+//                releases them at once, so the next block's products run while
+//                it computes P and dS; those are packed to bf16 and stored into
+//                tensor memory once the previous block's accumulations have
+//                read theirs. Then the epilogue (scale, store the rows inside
+//                the sequence). Warps 0-7 hand registers to these (setmaxnreg).
 // Tensor memory: T1 [0,128) T2 [128,256) P [256,320) dS [320,384)
 // ACC1 [384,448) ACC2 [448,512). Every wait is bounded as in the forward.
 // With local attention an item streams only the blocks inside the window band
@@ -47,6 +51,14 @@ constexpr int kRows = 128;
 constexpr int kD = 64;
 constexpr int kStages = 3;
 constexpr int kThreads = 512;
+// Registers per thread: 128 at launch (one CTA of 512 threads per SM); the
+// producer/issuer warpgroups drop to kRegsLow and the two elementwise
+// warpgroups rise to kRegsHigh, which holds a whole 64-column half-block of S
+// and dP in registers.
+constexpr uint32_t kRegsLaunch = 65536 / kThreads;
+constexpr uint32_t kRegsLow = 56, kRegsHigh = 200;
+static_assert(2 * 128 * (kRegsLow + kRegsHigh) <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTileBytes = kRows * kD * 2;
 constexpr uint32_t kColT1 = 0, kColT2 = 128, kColP = 256, kColDS = 320, kColAcc1 = 384,
                    kColAcc2 = 448;
@@ -58,7 +70,7 @@ struct Item {
 struct alignas(1024) Smem {
   __nv_bfloat16 st[2][kRows * kD];             // stationary tiles
   __nv_bfloat16 u[kStages][2][kRows * kD];     // streaming tile pairs
-  float vec[kStages][2][kRows];                // key pass: lse*log2e and Delta per query column
+  float vec[kStages][2][kRows];                // key pass: -lse*log2e and -Delta per query column
   uint64_t item_full[2], item_empty[2];
   uint64_t st_full, st_empty;
   uint64_t u_full[kStages], u_empty[kStages];
@@ -164,187 +176,193 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     return true;
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer (whole warp)
-    const CUtensorMap* st_map0 = kKeyPass ? &tm_k : &tm_q;
-    const CUtensorMap* st_map1 = kKeyPass ? &tm_v : &tm_do;
-    const CUtensorMap* u_map0 = kKeyPass ? &tm_q : &tm_k;
-    const CUtensorMap* u_map1 = kKeyPass ? &tm_do : &tm_v;
-    if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-      prefetch_tensormap(&tm_do);
-    }
-    uint32_t u_no = 0;
-    int pending_st = -1, pending_u[kStages];
-    for (int s = 0; s < kStages; ++s) pending_u[s] = -1;
-    bool ok = true;
-    for (uint32_t item_no = 0; ok; ++item_no) {
-      const int slot = item_no & 1;
-      if (!warp_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
-                     p.status, kSiteProducer)) {
-        ok = false;
-        break;
-      }
-      Item it;
+  // Warps 0-7 (producer, issuers, idle) hand registers to the elementwise
+  // warpgroups; each warpgroup's setmaxnreg heads its own branch.
+  if (warp < 8) {
+    regs_release<kRegsLow>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer (whole warp)
+      const CUtensorMap* st_map0 = kKeyPass ? &tm_k : &tm_q;
+      const CUtensorMap* st_map1 = kKeyPass ? &tm_v : &tm_do;
+      const CUtensorMap* u_map0 = kKeyPass ? &tm_q : &tm_k;
+      const CUtensorMap* u_map1 = kKeyPass ? &tm_do : &tm_v;
       if (lane == 0) {
-        const int32_t t = atomicAdd(p.plan.counter, 1);
-        if (t >= total) {
-          it.seq = -1;
-          it.head = it.blk = it.pad = 0;
-        } else {
-          int32_t seq, local;
-          plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
-          const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
-          const int32_t nb = (len + kRows - 1) / kRows;
-          it.seq = seq;
-          it.head = local / nb;
-          it.blk = local - it.head * nb;
-          it.pad = 0;
-        }
-        S.items[slot] = it;
-        mbar_arrive(smem_u32(&S.item_full[slot]));
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_do);
       }
-      it.seq = __shfl_sync(0xffffffffu, it.seq, 0);
-      it.head = __shfl_sync(0xffffffffu, it.head, 0);
-      it.blk = __shfl_sync(0xffffffffu, it.blk, 0);
-      if (it.seq < 0) break;
-      const int32_t start = __ldg(p.cu + it.seq);
-      const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      int32_t org, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
-      const int32_t x = it.head * kD;
-      if (!warp_wait(smem_u32(&S.st_empty), (item_no & 1) ^ 1, abort_flag, p.status,
-                     kSiteProducer)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_u32(&S.st_full), 2 * kTileBytes);
-        tma_load_2d(smem_u32(S.st[0]), st_map0, smem_u32(&S.st_full), x, start + it.blk * kRows);
-        tma_load_2d(smem_u32(S.st[1]), st_map1, smem_u32(&S.st_full), x, start + it.blk * kRows);
-      }
-      pending_st = item_no & 1;
-      for (int32_t i = 0; i < nb; ++i, ++u_no) {
-        const int s = u_no % kStages;
-        const uint32_t ph = (u_no / kStages) & 1;
-        if (!warp_wait(smem_u32(&S.u_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+      uint32_t u_no = 0;
+      int pending_st = -1, pending_u[kStages];
+      for (int s = 0; s < kStages; ++s) pending_u[s] = -1;
+      bool ok = true;
+      for (uint32_t item_no = 0; ok; ++item_no) {
+        const int slot = item_no & 1;
+        if (!warp_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
+                       p.status, kSiteProducer)) {
           ok = false;
           break;
         }
-        if (kKeyPass) {
-          // lse*log2e and Delta of the block's 128 queries; +inf / 0 past the
-          // sequence end, so those columns get P = 0.
-          const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + org + i * kRows;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int r = lane + 32 * u;
-            const bool in = org + i * kRows + r < len;
-            S.vec[s][0][r] = in ? __ldg(p.lse + base + r) * kLog2e : INFINITY;
-            S.vec[s][1][r] = in ? __ldg(p.delta + base + r) : 0.f;
-          }
-        }
-        __syncwarp();
+        Item it;
         if (lane == 0) {
-          mbar_arrive_expect_tx(smem_u32(&S.u_full[s]), 2 * kTileBytes);
-          tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x,
-                      start + org + i * kRows);
-          tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x,
-                      start + org + i * kRows);
+          const int32_t t = atomicAdd(p.plan.counter, 1);
+          if (t >= total) {
+            it.seq = -1;
+            it.head = it.blk = it.pad = 0;
+          } else {
+            int32_t seq, local;
+            plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
+            const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
+            const int32_t nb = (len + kRows - 1) / kRows;
+            it.seq = seq;
+            it.head = local / nb;
+            it.blk = local - it.head * nb;
+            it.pad = 0;
+          }
+          S.items[slot] = it;
+          mbar_arrive(smem_u32(&S.item_full[slot]));
         }
-        if (kKeyPass) mbar_arrive(smem_u32(&S.u_full[s]));
-        pending_u[s] = static_cast<int>(ph);
-      }
-    }
-    if (!ok && lane == 0) {
-      if (pending_st >= 0) mbar_drain_wait(smem_u32(&S.st_full), static_cast<uint32_t>(pending_st));
-      for (int s = 0; s < kStages; ++s)
-        if (pending_u[s] >= 0) mbar_drain_wait(smem_u32(&S.u_full[s]), static_cast<uint32_t>(pending_u[s]));
-    }
-  } else if (warp == 1 || warp == 2) {
-    // ------------------------------------------------------------ score-shaped products
-    // warp 1: T1 = A0 B0^T (S^T = K Q_i^T or S = Q K_j^T); warp 2: T2 = A1 B1^T (dP).
-    const int w = warp - 1;
-    constexpr uint32_t idesc = idesc_bf16(kRows, kRows, false, false);
-    const uint32_t a_addr = smem_u32(S.st[w]);
-    uint32_t u_no = 0, n_t = 0;
-    bool ok = true;
-    for (uint32_t item_no = 0; ok; ++item_no) {
-      Item it;
-      if (!read_item(item_no, it, kSiteT)) break;
-      if (it.seq < 0) break;
-      const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      int32_t org, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
-      if (!warp_wait(smem_u32(&S.st_full), item_no & 1, abort_flag, p.status, kSiteT)) break;
-      for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_t) {
-        const int s = u_no % kStages;
-        if (!warp_wait(smem_u32(&S.u_full[s]), (u_no / kStages) & 1, abort_flag, p.status,
-                       kSiteT) ||
-            (n_t > 0 && !warp_wait(smem_u32(&S.t_free), (n_t - 1) & 1, abort_flag, p.status,
-                                   kSiteT))) {
+        it.seq = __shfl_sync(0xffffffffu, it.seq, 0);
+        it.head = __shfl_sync(0xffffffffu, it.head, 0);
+        it.blk = __shfl_sync(0xffffffffu, it.blk, 0);
+        if (it.seq < 0) break;
+        const int32_t start = __ldg(p.cu + it.seq);
+        const int32_t len = __ldg(p.cu + it.seq + 1) - start;
+        int32_t org, nb;
+        stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
+        const int32_t x = it.head * kD;
+        if (!warp_wait(smem_u32(&S.st_empty), (item_no & 1) ^ 1, abort_flag, p.status,
+                       kSiteProducer)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t b_addr = smem_u32(S.u[s][w]);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss_warp(tmem + (w == 0 ? kColT1 : kColT2), smem_desc_sw128(a_addr + kk * 32, 16, 1024),
-                      smem_desc_sw128(b_addr + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
-        tc_commit_warp(smem_u32(&S.t_full[w]));
-        tc_commit_warp(smem_u32(&S.u_empty[s]));
-      }
-      if (ok) tc_commit_warp(smem_u32(&S.st_empty));
-    }
-    tc_commit_warp(smem_u32(&S.drain[w]));
-    mbar_drain_wait(smem_u32(&S.drain[w]), 0);
-  } else if (warp == 3 || (kKeyPass && warp == 4)) {
-    // ------------------------------------------------------------ accumulations
-    // key pass: warp 3 dV += P^T dO_i, warp 4 dK += dS^T Q_i;
-    // query pass: warp 3 dQ += dS K_j.
-    const int w = warp - 3;
-    constexpr uint32_t idesc = idesc_bf16(kRows, kD, false, true);
-    const uint32_t a_col = (kKeyPass && w == 0) ? kColP : kColDS;
-    const uint32_t d_col = w == 0 ? kColAcc1 : kColAcc2;
-    // The B operand: dO_i (dV), Q_i (dK) in the key pass; K_j in the query pass.
-    const int b_idx = kKeyPass ? (w == 0 ? 1 : 0) : 0;
-    uint32_t u_no = 0, n_p = 0;
-    bool ok = true;
-    for (uint32_t item_no = 0; ok; ++item_no) {
-      Item it;
-      if (!read_item(item_no, it, kSiteAcc)) break;
-      if (it.seq < 0) break;
-      const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      int32_t org, nb;
-      stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
-      // The previous item's accumulators must have been read by the epilogue.
-      if (!warp_wait(smem_u32(&S.o_free), (item_no & 1) ^ 1, abort_flag, p.status, kSiteAcc))
-        break;
-      for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_p) {
-        const int s = u_no % kStages;
-        if (!warp_wait(smem_u32(&S.u_full[s]), (u_no / kStages) & 1, abort_flag, p.status,
-                       kSiteAcc) ||
-            !warp_wait(smem_u32(&S.p_full), n_p & 1, abort_flag, p.status, kSiteAcc)) {
-          ok = false;
-          break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(smem_u32(&S.st_full), 2 * kTileBytes);
+          tma_load_2d(smem_u32(S.st[0]), st_map0, smem_u32(&S.st_full), x, start + it.blk * kRows);
+          tma_load_2d(smem_u32(S.st[1]), st_map1, smem_u32(&S.st_full), x, start + it.blk * kRows);
         }
-        tc_fence_after();
-        const uint32_t b_addr = smem_u32(S.u[s][b_idx]);
+        pending_st = item_no & 1;
+        for (int32_t i = 0; i < nb; ++i, ++u_no) {
+          const int s = u_no % kStages;
+          const uint32_t ph = (u_no / kStages) & 1;
+          if (!warp_wait(smem_u32(&S.u_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          if (kKeyPass) {
+            // -lse*log2e and -Delta of the block's 128 queries; -inf / 0 past
+            // the sequence end, so those columns get P = 0.
+            const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + org + i * kRows;
 #pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk)
-          mma_ts_warp(tmem + d_col, tmem + a_col + kk * 8,
-                      smem_desc_sw128(b_addr + kk * 16 * 128, 16, 1024), idesc,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit_warp(smem_u32(&S.acc_done[w]));
-        tc_commit_warp(smem_u32(&S.u_empty[s]));
+            for (int u = 0; u < 4; ++u) {
+              const int r = lane + 32 * u;
+              const bool in = org + i * kRows + r < len;
+              S.vec[s][0][r] = in ? -__ldg(p.lse + base + r) * kLog2e : -INFINITY;
+              S.vec[s][1][r] = in ? -__ldg(p.delta + base + r) : 0.f;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive_expect_tx(smem_u32(&S.u_full[s]), 2 * kTileBytes);
+            tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x,
+                        start + org + i * kRows);
+            tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x,
+                        start + org + i * kRows);
+          }
+          if (kKeyPass) mbar_arrive(smem_u32(&S.u_full[s]));
+          pending_u[s] = static_cast<int>(ph);
+        }
       }
-      if (ok) tc_commit_warp(smem_u32(&S.o_full));
+      if (!ok && lane == 0) {
+        if (pending_st >= 0) mbar_drain_wait(smem_u32(&S.st_full), static_cast<uint32_t>(pending_st));
+        for (int s = 0; s < kStages; ++s)
+          if (pending_u[s] >= 0) mbar_drain_wait(smem_u32(&S.u_full[s]), static_cast<uint32_t>(pending_u[s]));
+      }
+    } else if (warp == 1 || warp == 2) {
+      // ------------------------------------------------------------ score-shaped products
+      // warp 1: T1 = A0 B0^T (S^T = K Q_i^T or S = Q K_j^T); warp 2: T2 = A1 B1^T (dP).
+      const int w = warp - 1;
+      constexpr uint32_t idesc = idesc_bf16(kRows, kRows, false, false);
+      const uint32_t a_addr = smem_u32(S.st[w]);
+      uint32_t u_no = 0, n_t = 0;
+      bool ok = true;
+      for (uint32_t item_no = 0; ok; ++item_no) {
+        Item it;
+        if (!read_item(item_no, it, kSiteT)) break;
+        if (it.seq < 0) break;
+        const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
+        int32_t org, nb;
+        stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
+        if (!warp_wait(smem_u32(&S.st_full), item_no & 1, abort_flag, p.status, kSiteT)) break;
+        for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_t) {
+          const int s = u_no % kStages;
+          if (!warp_wait(smem_u32(&S.u_full[s]), (u_no / kStages) & 1, abort_flag, p.status,
+                         kSiteT) ||
+              (n_t > 0 && !warp_wait(smem_u32(&S.t_free), (n_t - 1) & 1, abort_flag, p.status,
+                                     kSiteT))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_addr = smem_u32(S.u[s][w]);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss_warp(tmem + (w == 0 ? kColT1 : kColT2), smem_desc_sw128(a_addr + kk * 32, 16, 1024),
+                        smem_desc_sw128(b_addr + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+          tc_commit_warp(smem_u32(&S.t_full[w]));
+          tc_commit_warp(smem_u32(&S.u_empty[s]));
+        }
+        if (ok) tc_commit_warp(smem_u32(&S.st_empty));
+      }
+      tc_commit_warp(smem_u32(&S.drain[w]));
+      mbar_drain_wait(smem_u32(&S.drain[w]), 0);
+    } else if (warp == 3 || (kKeyPass && warp == 4)) {
+      // ------------------------------------------------------------ accumulations
+      // key pass: warp 3 dV += P^T dO_i, warp 4 dK += dS^T Q_i;
+      // query pass: warp 3 dQ += dS K_j.
+      const int w = warp - 3;
+      constexpr uint32_t idesc = idesc_bf16(kRows, kD, false, true);
+      const uint32_t a_col = (kKeyPass && w == 0) ? kColP : kColDS;
+      const uint32_t d_col = w == 0 ? kColAcc1 : kColAcc2;
+      // The B operand: dO_i (dV), Q_i (dK) in the key pass; K_j in the query pass.
+      const int b_idx = kKeyPass ? (w == 0 ? 1 : 0) : 0;
+      uint32_t u_no = 0, n_p = 0;
+      bool ok = true;
+      for (uint32_t item_no = 0; ok; ++item_no) {
+        Item it;
+        if (!read_item(item_no, it, kSiteAcc)) break;
+        if (it.seq < 0) break;
+        const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
+        int32_t org, nb;
+        stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
+        // The previous item's accumulators must have been read by the epilogue.
+        if (!warp_wait(smem_u32(&S.o_free), (item_no & 1) ^ 1, abort_flag, p.status, kSiteAcc))
+          break;
+        for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_p) {
+          const int s = u_no % kStages;
+          if (!warp_wait(smem_u32(&S.u_full[s]), (u_no / kStages) & 1, abort_flag, p.status,
+                         kSiteAcc) ||
+              !warp_wait(smem_u32(&S.p_full), n_p & 1, abort_flag, p.status, kSiteAcc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_addr = smem_u32(S.u[s][b_idx]);
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_ts_warp(tmem + d_col, tmem + a_col + kk * 8,
+                        smem_desc_sw128(b_addr + kk * 16 * 128, 16, 1024), idesc,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          tc_commit_warp(smem_u32(&S.acc_done[w]));
+          tc_commit_warp(smem_u32(&S.u_empty[s]));
+        }
+        if (ok) tc_commit_warp(smem_u32(&S.o_full));
+      }
+      tc_commit_warp(smem_u32(&S.drain[2 + w]));
+      mbar_drain_wait(smem_u32(&S.drain[2 + w]), 0);
     }
-    tc_commit_warp(smem_u32(&S.drain[2 + w]));
-    mbar_drain_wait(smem_u32(&S.drain[2 + w]), 0);
-  } else if (warp >= 8) {
+  } else {
+    regs_claim<kRegsHigh>();
     // ------------------------------------------------------------ elementwise + epilogue
     const int h = (warp - 8) >> 2;                // column half
     const int quarter = warp & 3;
@@ -384,6 +402,65 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           break;
         }
         tc_fence_after();
+        // This half's 64 columns of both products into registers at once, so
+        // that the next block's products can overwrite them while P and dS
+        // are computed.
+        uint32_t sv[2][32], dv[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(lane_base + kColT1 + 64 * h + 32 * c, sv[c]);
+          tmem_ld32(lane_base + kColT2 + 64 * h + 32 * c, dv[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_wait_ld(sv[c]);
+          tmem_wait_ld(dv[c]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.t_free));
+        const int32_t col0_pos = org + i * kRows + 64 * h;  // row position of this half's column 0
+        const int32_t col_valid = len - col0_pos;           // query pass: valid keys in this half
+        const int32_t clo = vis_lo - col0_pos, chi = vis_hi - col0_pos;  // window, same origin
+        uint32_t pk[2][16], dk[2][16];
+        const uint64_t c2 = f2(scale_log2, scale_log2);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = 64 * h + 32 * c;
+          // Key pass: -lse*log2e and -Delta per query column, four at a time;
+          // query pass: this row's own.
+          const float4* nl4 = reinterpret_cast<const float4*>(&S.vec[s][0][col0]);
+          const float4* nd4 = reinterpret_cast<const float4*>(&S.vec[s][1][col0]);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            uint64_t nl2, nd2;
+            if (kKeyPass) {
+              const float4 l4 = nl4[e >> 1], d4 = nd4[e >> 1];
+              nl2 = (e & 1) ? f2(l4.z, l4.w) : f2(l4.x, l4.y);
+              nd2 = (e & 1) ? f2(d4.z, d4.w) : f2(d4.x, d4.y);
+            } else {
+              nl2 = f2(-row_lse2, -row_lse2);
+              nd2 = f2(-row_delta, -row_delta);
+            }
+            float x0, x1;
+            f2_split(ffma2(f2(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])),
+                           c2, nl2),
+                     x0, x1);
+            float pr[2] = {ex2(x0), ex2(x1)};
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int cc = 2 * e + u;
+              if (!kKeyPass && 32 * c + cc >= col_valid) pr[u] = 0.f;  // key past the sequence
+              if (windowed && (32 * c + cc < clo || 32 * c + cc > chi)) pr[u] = 0.f;
+            }
+            const uint64_t g2 =
+                fadd2(f2(__uint_as_float(dv[c][2 * e]), __uint_as_float(dv[c][2 * e + 1])), nd2);
+            float ds0, ds1;
+            f2_split(fmul2(f2(pr[0], pr[1]), g2), ds0, ds1);
+            pk[c][e] = pack_bf16x2(pr[0], pr[1]);
+            dk[c][e] = pack_bf16x2(ds0, ds1);
+          }
+        }
         // P and dS of the previous block must have been consumed before they are rewritten.
         if (n_blk > 0) {
           const uint32_t par = (n_blk - 1) & 1;
@@ -395,51 +472,15 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           tc_fence_after();
         }
-        const int32_t col0_pos = org + i * kRows + 64 * h;  // row position of this half's column 0
-        const int32_t col_valid = len - col0_pos;           // query pass: valid keys in this half
-        const int32_t clo = vis_lo - col0_pos, chi = vis_hi - col0_pos;  // window, same origin
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int col0 = 64 * h + 32 * c;
-          uint32_t sv[32], dv[32];
-          tmem_ld32(lane_base + kColT1 + col0, sv);
-          tmem_ld32(lane_base + kColT2 + col0, dv);
-          tmem_wait_ld(sv);
-          tmem_wait_ld(dv);
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float pr[2], ds[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cc = 2 * e + u;
-              float lse2, dlt;
-              if (kKeyPass) {
-                lse2 = S.vec[s][0][col0 + cc];
-                dlt = S.vec[s][1][col0 + cc];
-              } else {
-                lse2 = row_lse2;
-                dlt = row_delta;
-              }
-              float pv = ex2(fmaf(__uint_as_float(sv[cc]), scale_log2, -lse2));
-              if (!kKeyPass && 32 * c + cc >= col_valid) pv = 0.f;  // key past the sequence
-              if (windowed && (32 * c + cc < clo || 32 * c + cc > chi)) pv = 0.f;
-              pr[u] = pv;
-              ds[u] = pv * (__uint_as_float(dv[cc]) - dlt);
-            }
-            pk[e] = pack_bf16x2(pr[0], pr[1]);
-            dk[e] = pack_bf16x2(ds[0], ds[1]);
-          }
-          if (kKeyPass) tmem_st16(lane_base + kColP + 32 * h + 16 * c, pk);
-          tmem_st16(lane_base + kColDS + 32 * h + 16 * c, dk);
+          if (kKeyPass) tmem_st16(lane_base + kColP + 32 * h + 16 * c, pk[c]);
+          tmem_st16(lane_base + kColDS + 32 * h + 16 * c, dk[c]);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&S.t_free));
-          mbar_arrive(smem_u32(&S.p_full));
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&S.p_full));
       }
       if (!ok) break;
       // Epilogue: this half stores columns [32h, 32h+32) of each accumulator.
@@ -532,6 +573,12 @@ pe_status launch_pass(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
   const size_t smem = sizeof(Smem) + 1024;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
+  // The elementwise warpgroups' register claim is served from what the CTA
+  // was launched with; never launch a build whose count cannot serve it.
+  cudaFuncAttributes attr;
+  PE_CUDA_TRY(cudaFuncGetAttributes(&attr, kernel));
+  if (static_cast<uint32_t>(attr.numRegs) * kThreads < 2u * 128u * (kRegsLow + kRegsHigh))
+    return PE_ERR_UNSUPPORTED;
   PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, 0, prm.plan, nullptr, stream));
   kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mdo, prm);
   PE_CUDA_TRY(cudaGetLastError());
