@@ -422,6 +422,23 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int32_t col0_pos = org + i * kRows + 64 * h;  // row position of this half's column 0
         const int32_t col_valid = len - col0_pos;           // query pass: valid keys in this half
         const int32_t clo = vis_lo - col0_pos, chi = vis_hi - col0_pos;  // window, same origin
+        // Scores that must give P = 0 become -inf: keys past the sequence end
+        // (query pass, the sequence's last block only; the key pass gets them
+        // from the -inf lse of queries past the end) and pairs outside the window.
+        if (!kKeyPass && col_valid < 64) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              if (32 * c + cc >= col_valid) sv[c][cc] = 0xff800000u;
+        }
+        if (windowed && __any_sync(0xffffffffu, clo > 0 || chi < 63)) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              if (32 * c + cc < clo || 32 * c + cc > chi) sv[c][cc] = 0xff800000u;
+        }
         uint32_t pk[2][16], dk[2][16];
         const uint64_t c2 = f2(scale_log2, scale_log2);
 #pragma unroll
@@ -446,13 +463,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             f2_split(ffma2(f2(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])),
                            c2, nl2),
                      x0, x1);
-            float pr[2] = {ex2(x0), ex2(x1)};
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int cc = 2 * e + u;
-              if (!kKeyPass && 32 * c + cc >= col_valid) pr[u] = 0.f;  // key past the sequence
-              if (windowed && (32 * c + cc < clo || 32 * c + cc > chi)) pr[u] = 0.f;
-            }
+            const float pr[2] = {ex2(x0), ex2(x1)};
             const uint64_t g2 =
                 fadd2(f2(__uint_as_float(dv[c][2 * e]), __uint_as_float(dv[c][2 * e + 1])), nd2);
             float ds0, ds1;
