@@ -53,6 +53,13 @@ constexpr int kD = 64;                             // head_dim
 constexpr int kStages = 4;                         // K/V ring depth
 constexpr int kIssueWarps = 3;                     // QK issuer + one PV issuer per tile
 constexpr int kThreads = 384;
+// Registers per thread: 168 at launch (one CTA of 384 threads per SM); the
+// producer/issuer warpgroup drops to kRegsLow and the two softmax warpgroups
+// rise to kRegsHigh.
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsLow = 56, kRegsHigh = 224;
+static_assert(128 * (kRegsLow + 2 * kRegsHigh) <= kThreads * kRegsLaunch,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTileBytes = kRows * kD * 2;    // 16 KiB
 constexpr int kPairRows = 2 * kRows;               // query rows per work item
 
@@ -188,198 +195,204 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const uint32_t tmem = __shfl_sync(0xffffffffu, S.tmem_base, 0);
   const int32_t total = *p.plan.total_tiles;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
+  // Warpgroup 0 (TMA producer, MMA issuers) hands registers to the two
+  // softmax warpgroups; each warpgroup's setmaxnreg heads its own branch.
+  if (warp < 4) {
+    regs_release<kRegsLow>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        uint32_t kv_no = 0;
+        int pending_q = -1;                // parity of the last Q load not yet known complete
+        int pending_k[kStages], pending_v[kStages];  // parity of the last K / V load per stage
+        for (int s = 0; s < kStages; ++s) pending_k[s] = pending_v[s] = -1;
+        bool ok = true;
+        for (uint32_t item_no = 0; ok; ++item_no) {
+          const int slot = item_no & 1;
+          if (!mbar_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
+                         p.status, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          const int32_t t = atomicAdd(p.plan.counter, 1);
+          Item it;
+          if (t >= total) {
+            it.seq = -1;
+            it.head = it.pair = it.pad = 0;
+          } else {
+            decode_item(p, t, it);
+          }
+          S.items[slot] = it;
+          mbar_arrive(smem_u32(&S.item_full[slot]));
+          if (it.seq < 0) break;
+          const int32_t start = __ldg(p.cu + it.seq);
+          const int32_t len = __ldg(p.cu + it.seq + 1) - start;
+          const int32_t r0 = it.pair * kPairRows;
+          const int ntiles = (len - r0 > kRows) ? 2 : 1;
+          const ItemRange ir = item_range<kLocal>(p, len, r0);
+          const int32_t nkv = ir.nkv;
+          const int32_t x = it.head * kD;
+          if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
+                         kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
+          for (int tt = 0; tt < ntiles; ++tt)
+            tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full), x, start + r0 + tt * kRows);
+          pending_q = item_no & 1;
+          for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
+            const int s = kv_no % kStages;
+            const uint32_t ph = (kv_no / kStages) & 1;
+            if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
+            tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x,
+                        start + ir.kb0 + j * kRows);
+            pending_k[s] = (int)ph;
+            if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
+            tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x,
+                        start + ir.kb0 + j * kRows);
+            pending_v[s] = (int)ph;
+          }
+        }
+        if (!ok) {
+          // Let every copy this thread started land before the CTA exits.
+          if (pending_q >= 0) mbar_drain_wait(smem_u32(&S.q_full), (uint32_t)pending_q);
+          for (int s = 0; s < kStages; ++s) {
+            if (pending_k[s] >= 0) mbar_drain_wait(smem_u32(&S.k_full[s]), (uint32_t)pending_k[s]);
+            if (pending_v[s] >= 0) mbar_drain_wait(smem_u32(&S.v_full[s]), (uint32_t)pending_v[s]);
+          }
+        }
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ QK issuer (whole warp)
+      // S_t for key block j+1 is computed as soon as the softmax has read S_t(j),
+      // so it overlaps that softmax.
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kRows, false, false);
       uint32_t kv_no = 0;
-      int pending_q = -1;                // parity of the last Q load not yet known complete
-      int pending_k[kStages], pending_v[kStages];  // parity of the last K / V load per stage
-      for (int s = 0; s < kStages; ++s) pending_k[s] = pending_v[s] = -1;
+      uint32_t n_qk[2] = {0, 0};                     // QK MMA groups issued per tile, all items
       bool ok = true;
       for (uint32_t item_no = 0; ok; ++item_no) {
         const int slot = item_no & 1;
-        if (!mbar_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
-                       p.status, kSiteProducer)) {
-          ok = false;
+        if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+                       kSiteMma))
           break;
-        }
-        const int32_t t = atomicAdd(p.plan.counter, 1);
-        Item it;
-        if (t >= total) {
-          it.seq = -1;
-          it.head = it.pair = it.pad = 0;
-        } else {
-          decode_item(p, t, it);
-        }
-        S.items[slot] = it;
-        mbar_arrive(smem_u32(&S.item_full[slot]));
+        const Item it = S.items[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
         if (it.seq < 0) break;
-        const int32_t start = __ldg(p.cu + it.seq);
-        const int32_t len = __ldg(p.cu + it.seq + 1) - start;
+        const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
         const int32_t r0 = it.pair * kPairRows;
         const int ntiles = (len - r0 > kRows) ? 2 : 1;
         const ItemRange ir = item_range<kLocal>(p, len, r0);
         const int32_t nkv = ir.nkv;
-        const int32_t x = it.head * kD;
-        if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
-                       kSiteProducer)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
-        for (int tt = 0; tt < ntiles; ++tt)
-          tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full), x, start + r0 + tt * kRows);
-        pending_q = item_no & 1;
-        for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
-          const int s = kv_no % kStages;
-          const uint32_t ph = (kv_no / kStages) & 1;
-          if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+        if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
+        for (int32_t j = 0; j < nkv && ok; ++j) {
+          const uint32_t c = kv_no + j;
+          const int s = c % kStages;
+          if (!warp_wait(smem_u32(&S.k_full[s]), (c / kStages) & 1, abort_flag, p.status,
+                         kSiteMma)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
-          tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x,
-                      start + ir.kb0 + j * kRows);
-          pending_k[s] = (int)ph;
-          if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
+          const uint32_t k_addr = smem_u32(S.k[s]);
+          for (int t = 0; t < ntiles; ++t) {
+            if (kLocal && !ir.uses(t, j)) continue;  // outside every window of tile t
+            // The softmax must have read the previous S_t before it is overwritten.
+            if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag,
+                                          p.status, kSiteMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t q_addr = smem_u32(S.q[t]);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ss_warp(tmem + col_s(t), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
+                          smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            tc_commit_warp(smem_u32(&S.s_full[t]));
+            ++n_qk[t];
+          }
+          if (!ok) break;
+          tc_commit_warp(smem_u32(&S.k_empty[s]));  // K_j no longer needed by either tile
+        }
+        kv_no += nkv;
+        if (ok) tc_commit_warp(smem_u32(&S.q_empty));
+      }
+      // Every MMA this warp issued must finish before tensor memory is freed.
+      tc_commit_warp(smem_u32(&S.drain[0]));
+      mbar_drain_wait(smem_u32(&S.drain[0]), 0);
+    } else if (warp == 2 || warp == 3) {
+      // ------------------------------------------------------------ PV issuers (whole warps)
+      // O_t += P_t V_j as soon as the softmax has written P_t(j).
+      const int t = warp - 2;
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
+      uint32_t kv_no = 0, n_pv = 0;
+      bool ok = true;
+      for (uint32_t item_no = 0; ok; ++item_no) {
+        const int slot = item_no & 1;
+        if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
+                       kSiteMma))
+          break;
+        const Item it = S.items[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
+        if (it.seq < 0) break;
+        const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
+        const int32_t r0 = it.pair * kPairRows;
+        const int ntiles = (len - r0 > kRows) ? 2 : 1;
+        const ItemRange ir = item_range<kLocal>(p, len, r0);
+        const int32_t nkv = ir.nkv;
+        for (int32_t j = 0; j < nkv; ++j) {
+          const uint32_t c = kv_no + j;
+          const int s = c % kStages;
+          // Both PV warps take part in every V stage phase: each waits for every
+          // block and releases it once, so the producer can never refill a stage
+          // that either warp has not yet seen (which would make a parity wait
+          // match a later phase).
+          if (!warp_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
+                         kSiteMma)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
-          tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x,
-                      start + ir.kb0 + j * kRows);
-          pending_v[s] = (int)ph;
-        }
-      }
-      if (!ok) {
-        // Let every copy this thread started land before the CTA exits.
-        if (pending_q >= 0) mbar_drain_wait(smem_u32(&S.q_full), (uint32_t)pending_q);
-        for (int s = 0; s < kStages; ++s) {
-          if (pending_k[s] >= 0) mbar_drain_wait(smem_u32(&S.k_full[s]), (uint32_t)pending_k[s]);
-          if (pending_v[s] >= 0) mbar_drain_wait(smem_u32(&S.v_full[s]), (uint32_t)pending_v[s]);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ QK issuer (whole warp)
-    // S_t for key block j+1 is computed as soon as the softmax has read S_t(j),
-    // so it overlaps that softmax.
-    constexpr uint32_t idesc_qk = idesc_bf16(kRows, kRows, false, false);
-    uint32_t kv_no = 0;
-    uint32_t n_qk[2] = {0, 0};                     // QK MMA groups issued per tile, all items
-    bool ok = true;
-    for (uint32_t item_no = 0; ok; ++item_no) {
-      const int slot = item_no & 1;
-      if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
-                     kSiteMma))
-        break;
-      const Item it = S.items[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
-      if (it.seq < 0) break;
-      const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      const int32_t r0 = it.pair * kPairRows;
-      const int ntiles = (len - r0 > kRows) ? 2 : 1;
-      const ItemRange ir = item_range<kLocal>(p, len, r0);
-      const int32_t nkv = ir.nkv;
-      if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
-      for (int32_t j = 0; j < nkv && ok; ++j) {
-        const uint32_t c = kv_no + j;
-        const int s = c % kStages;
-        if (!warp_wait(smem_u32(&S.k_full[s]), (c / kStages) & 1, abort_flag, p.status,
-                       kSiteMma)) {
-          ok = false;
-          break;
-        }
-        const uint32_t k_addr = smem_u32(S.k[s]);
-        for (int t = 0; t < ntiles; ++t) {
-          if (kLocal && !ir.uses(t, j)) continue;  // outside every window of tile t
-          // The softmax must have read the previous S_t before it is overwritten.
-          if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag,
-                                        p.status, kSiteMma)) {
+          if (t >= ntiles || !ir.uses(t, j)) {       // this tile does not read V_j
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.v_empty[s]));
+            continue;
+          }
+          if (!warp_wait(smem_u32(&S.p_full[t]), n_pv & 1, abort_flag, p.status, kSiteMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t q_addr = smem_u32(S.q[t]);
+          const uint32_t v_addr = smem_u32(S.v[s]);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ss_warp(tmem + col_s(t), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
-                        smem_desc_sw128(k_addr + kk * 32, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-          tc_commit_warp(smem_u32(&S.s_full[t]));
-          ++n_qk[t];
+          for (int kk = 0; kk < kRows / 16; ++kk)
+            mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
+                        smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
+                        (j > ir.lo(t) || kk > 0) ? 1u : 0u);
+          tc_commit_warp(smem_u32(&S.pv_done[t]));
+          if (j == ir.hi(t)) tc_commit_warp(smem_u32(&S.o_full[t]));
+          ++n_pv;
+          tc_commit_warp(smem_u32(&S.v_empty[s]));
         }
-        if (!ok) break;
-        tc_commit_warp(smem_u32(&S.k_empty[s]));  // K_j no longer needed by either tile
+        kv_no += nkv;
       }
-      kv_no += nkv;
-      if (ok) tc_commit_warp(smem_u32(&S.q_empty));
+      tc_commit_warp(smem_u32(&S.drain[1 + t]));
+      mbar_drain_wait(smem_u32(&S.drain[1 + t]), 0);
     }
-    // Every MMA this warp issued must finish before tensor memory is freed.
-    tc_commit_warp(smem_u32(&S.drain[0]));
-    mbar_drain_wait(smem_u32(&S.drain[0]), 0);
-  } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------------------------ PV issuers (whole warps)
-    // O_t += P_t V_j as soon as the softmax has written P_t(j).
-    const int t = warp - 2;
-    constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
-    uint32_t kv_no = 0, n_pv = 0;
-    bool ok = true;
-    for (uint32_t item_no = 0; ok; ++item_no) {
-      const int slot = item_no & 1;
-      if (!warp_wait(smem_u32(&S.item_full[slot]), (item_no >> 1) & 1, abort_flag, p.status,
-                     kSiteMma))
-        break;
-      const Item it = S.items[slot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&S.item_empty[slot]));
-      if (it.seq < 0) break;
-      const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
-      const int32_t r0 = it.pair * kPairRows;
-      const int ntiles = (len - r0 > kRows) ? 2 : 1;
-      const ItemRange ir = item_range<kLocal>(p, len, r0);
-      const int32_t nkv = ir.nkv;
-      for (int32_t j = 0; j < nkv; ++j) {
-        const uint32_t c = kv_no + j;
-        const int s = c % kStages;
-        // Both PV warps take part in every V stage phase: each waits for every
-        // block and releases it once, so the producer can never refill a stage
-        // that either warp has not yet seen (which would make a parity wait
-        // match a later phase).
-        if (!warp_wait(smem_u32(&S.v_full[s]), (c / kStages) & 1, abort_flag, p.status,
-                       kSiteMma)) {
-          ok = false;
-          break;
-        }
-        if (t >= ntiles || !ir.uses(t, j)) {       // this tile does not read V_j
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&S.v_empty[s]));
-          continue;
-        }
-        if (!warp_wait(smem_u32(&S.p_full[t]), n_pv & 1, abort_flag, p.status, kSiteMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(S.v[s]);
-#pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk)
-          mma_ts_warp(tmem + col_o(t), tmem + col_p(t) + kk * 8,
-                      smem_desc_sw128(v_addr + kk * 16 * 128, 16, 1024), idesc_pv,
-                      (j > ir.lo(t) || kk > 0) ? 1u : 0u);
-        tc_commit_warp(smem_u32(&S.pv_done[t]));
-        if (j == ir.hi(t)) tc_commit_warp(smem_u32(&S.o_full[t]));
-        ++n_pv;
-        tc_commit_warp(smem_u32(&S.v_empty[s]));
-      }
-      kv_no += nkv;
-    }
-    tc_commit_warp(smem_u32(&S.drain[1 + t]));
-    mbar_drain_wait(smem_u32(&S.drain[1 + t]), 0);
-  } else if (warp >= 4) {
+  } else {
+    regs_claim<kRegsHigh>();
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;               // query tile of this warpgroup
     const int quarter = warp & 3;                // TMEM lanes 32*quarter .. +31
@@ -600,6 +613,12 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   auto kernel = win.active() ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
+  // The softmax warpgroups' register claim is served from what the CTA was
+  // launched with; never launch a build whose count cannot serve it.
+  cudaFuncAttributes attr;
+  PE_CUDA_TRY(cudaFuncGetAttributes(&attr, kernel));
+  if (static_cast<uint32_t>(attr.numRegs) * kThreads < 128u * (kRegsLow + 2 * kRegsHigh))
+    return PE_ERR_UNSUPPORTED;
   FwdParams prm;
   prm.cu = cu;
   prm.B = B;
