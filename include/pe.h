@@ -203,9 +203,14 @@ pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t
  * workspace: device, >= pe_attention_workspace_size(...) bytes. Its first 4
  *   bytes receive a device-side status (PE_OK or PE_ERR_DEVICE_TIMEOUT),
  *   readable with pe_read_device_status after the call. In first-token mode
- *   with max_seq_len > 1024 the reported size includes room to split each
- *   sequence's keys over several CTAs; a workspace without that room (but
- *   large enough otherwise) is accepted and runs one CTA per sequence and head.
+ *   the reported size includes room for partial softmax states, so that long
+ *   sequences can be spread over several CTAs: when a token row
+ *   (num_heads*head_dim elements) is 512, 1024, ..., 4096 bytes and head_dim
+ *   is 32, 64 or 128, the token range is cut into equal chunks of whole rows
+ *   (one CTA each) and each chunk keeps up to two partial states per head;
+ *   otherwise, with max_seq_len > 1024, each (sequence, head) is split into
+ *   1024-key chunks. A workspace without that room (but large enough
+ *   otherwise) is accepted and runs one CTA per sequence and head.
  * ------------------------------------------------------------------------ */
 size_t pe_attention_workspace_size(pe_dtype dtype, int32_t num_sequences, int64_t num_tokens,
                                    int32_t num_heads, int32_t head_dim, int32_t max_seq_len,

@@ -106,12 +106,14 @@ extern "C" const char* pe_status_string(int status) {
 
 extern "C" int pe_abi_version(void) { return 2; }
 
-extern "C" size_t pe_attention_workspace_size(pe_dtype /*dtype*/, int32_t B, int64_t N,
+extern "C" size_t pe_attention_workspace_size(pe_dtype dtype, int32_t B, int64_t N,
                                               int32_t H, int32_t D, int32_t S,
                                               int query_is_first_token, int backward) {
   if (B < 0 || N < 0 || H < 1 || D < 0 || S < 1) return 0;
   size_t bytes = attention_ws_bytes(B, N, H, query_is_first_token, backward);
-  if (query_is_first_token && !backward) bytes += first_token_partial_bytes(B, H, D, S);
+  if (query_is_first_token && !backward)
+    bytes += first_token_stream_supported(dtype, H, D) ? first_token_stream_partial_bytes(N, H, D)
+                                                       : first_token_partial_bytes(B, H, D, S);
   return bytes;
 }
 
@@ -136,18 +138,27 @@ extern "C" pe_status pe_packed_attention_fwd_local(
   const Window win = make_window(window_left, window_right, S);
   PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (B == 0) return PE_OK;
+  const TilePlan plan = plan_view(workspace, B);
+  // Streaming first-token form (whole token rows, equal token chunks per CTA)
+  // when the row shape allows it and the workspace holds its chunk partials.
+  if (query_is_first_token && first_token_stream_supported(dtype, H, D) &&
+      workspace_bytes >= plan_bytes(B) + first_token_stream_partial_bytes(N, H, D)) {
+    float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
+    return fwd_first_token_stream(dtype, D, q, k, v, cu_seqlens, B, H, N, S, scale, win, out,
+                                  lse, part, static_cast<DeviceStatus*>(workspace), stream);
+  }
   if (query_is_first_token) {
-    // Split sequences over key chunks when they are long on average (more
-    // than two chunks) and the workspace has room for the chunk partials.
+    // Otherwise one CTA per (sequence, head), split over key chunks when
+    // sequences are long on average (more than two chunks) and the workspace
+    // has room for those chunk partials.
     const size_t part_bytes = first_token_partial_bytes(B, H, D, S);
     float* part = nullptr;
     if (part_bytes > 0 && N > 2LL * kFirstTokenChunk * B &&
         workspace_bytes >= plan_bytes(B) + part_bytes)
       part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
     return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, S, scale, win, out, lse, part,
-                           plan_view(workspace, B), stream);
+                           plan, stream);
   }
-  TilePlan plan = plan_view(workspace, B);
   if (dtype == PE_BF16 && D == 64) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(), S, plan, nullptr,
                             stream));

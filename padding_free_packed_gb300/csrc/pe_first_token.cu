@@ -1,0 +1,487 @@
+// First-token query, streaming form.
+//
+// In first-token mode every sequence has one query row (its first token), so
+// the forward is a matrix-vector product per (sequence, head) whose cost is
+// reading k and v once (page "Source code for gigl.nn.packed_attention",
+// function `packed_attention`, `query_is_first_token`). The packed buffers are
+// token-major [N, H, D]: one token's keys for all heads are one contiguous row
+// of H*D elements. This kernel streams those rows in order instead of reading
+// one head's 2*D-byte slices at an H*D stride:
+//
+//  * the token range [0, N) is cut into equal chunks, one CTA each and as
+//    many as fit on the GPU at once (never shorter than 64 tokens), so every
+//    CTA moves the same number of bytes whatever the mix of sequence lengths;
+//  * a CTA walks the sequences that overlap its chunk. One producer thread
+//    streams their visible k and v rows into a five-stage shared-memory ring
+//    with bulk asynchronous copies (cp.async.bulk, completion counted in bytes
+//    on an mbarrier per stage), running ahead across sequence boundaries; four
+//    consumer warps read each row with 16-byte shared loads (each lane owns VPL
+//    vectors of a row, a head's D elements being LPH consecutive lanes), keep
+//    one online-softmax state per (lane, vector), release the stage, and at
+//    each sequence's end merge their states in shared memory;
+//  * a sequence that lies inside one chunk is finished there (output, lse); a
+//    sequence that crosses chunk edges leaves one partial state (m, l, o[D]
+//    per head) in every chunk it touches (slot 1 in its first chunk, slot 0
+//    in the others), which first_token_stream_merge_kernel combines in chunk
+//    order. Nothing is accumulated with atomics, so results are bitwise
+//    reproducible.
+//
+// Supported when a token row is a whole number (1..8) of 512-byte warp loads
+// and a head's row slice spans a power of two of lanes (D in {32, 64, 128});
+// other shapes run the per-(sequence, head) kernel in pe_fwd_simt.cu.
+#include "pe_kernels.cuh"
+#include "pe_sm103.cuh"
+
+namespace pe {
+namespace {
+
+using namespace sm103;
+
+constexpr int kStWarps = 4;                     // consumer warps
+constexpr int kStThreads = kStWarps * 32;       // consumer threads
+constexpr int kStBlock = kStThreads + 32;       // + one producer warp
+constexpr int kStStages = 5;
+constexpr int kStStageBytes = 8192;             // of k (and as much of v) per stage
+constexpr int32_t kStMaxChunks = 16384;
+enum StWaitSite { kSiteStProducer = 21, kSiteStConsumer = 22 };
+
+template <typename T, int D, int VPL>
+struct StShape {
+  static constexpr int kEPV = 16 / (int)sizeof(T);  // elements per 16-byte vector
+  static constexpr int kLPH = D / kEPV;              // lanes per head
+  static constexpr int kRow = 32 * VPL * kEPV;       // elements of one token row (H * D)
+  static constexpr int kRowBytes = kRow * (int)sizeof(T);
+  static constexpr int kH = kRow / D;                // heads
+  static constexpr int kRows = kStStageBytes / kRowBytes > 0 ? kStStageBytes / kRowBytes : 1;
+  static constexpr int kStageElems = kRows * kRow;   // of k (or v) per stage
+  static constexpr int kMinBlocks = VPL <= 6 ? 2 : 1;
+  static constexpr size_t kSmem = (size_t)kStStages * 2 * kStageElems * sizeof(T) +
+                                  (size_t)kStWarps * (kRow + 2 * kH) * sizeof(float);
+  static_assert(32 % kLPH == 0 && kLPH >= 1, "a head must span a power of two of lanes");
+  static_assert(kRowBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& r, float (&x)[16 / sizeof(T)]) {
+  if constexpr (sizeof(T) == 4) {
+    x[0] = __uint_as_float(r.x);
+    x[1] = __uint_as_float(r.y);
+    x[2] = __uint_as_float(r.z);
+    x[3] = __uint_as_float(r.w);
+  } else {
+    // bf16 element 2j is the low half of word j; a bf16 is the top half of an fp32.
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = __uint_as_float(w[j] << 16);
+      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ uint4 load16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global to shared memory, counted on the mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Barrier of the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kStThreads) : "memory");
+}
+
+// Largest i in [0, B) with cu[i] <= t (cu[0] = 0 <= t), found by the whole
+// warp: each round probes 32 evenly spaced entries and keeps the interval the
+// last true probe opens.
+__device__ __forceinline__ int32_t find_sequence(const int32_t* __restrict__ cu, int32_t B,
+                                                 int32_t t, int lane) {
+  int32_t lo = 0, hi = B;  // answer in [lo, hi)
+  while (hi - lo > 32) {
+    const int32_t step = (hi - lo + 31) / 32;
+    const int32_t idx = lo + lane * step;
+    const bool le = idx < hi && __ldg(cu + idx) <= t;
+    const int n = __popc(__ballot_sync(0xffffffffu, le));  // >= 1: cu[lo] <= t
+    lo += (n - 1) * step;
+    hi = min(hi, lo + step);
+  }
+  const int32_t idx = lo + lane;
+  const bool le = idx < hi && __ldg(cu + idx) <= t;
+  return lo + __popc(__ballot_sync(0xffffffffu, le)) - 1;
+}
+
+// Partial state of (chunk c, slot, head h): m, l, o[D].
+template <int D>
+__device__ __forceinline__ float* partial_state(float* part, int64_t c, int slot, int H, int h) {
+  return part + ((c * 2 + slot) * H + h) * (D + 2);
+}
+
+// The visible rows of one sequence inside a chunk: [a, vis_end) of sequence i,
+// whose keys seen by its query are [s0, e1).
+struct Segment {
+  int64_t s0, e1, a, vis_end, next;
+};
+
+__device__ __forceinline__ Segment segment_of(const int32_t* __restrict__ cu, int32_t i,
+                                              int64_t a, int64_t c1, int32_t key_limit) {
+  Segment g;
+  g.s0 = __ldg(cu + i);
+  const int64_t s1 = __ldg(cu + i + 1);
+  g.next = min(s1, c1);
+  g.e1 = min(s1, g.s0 + key_limit);
+  g.a = a;
+  g.vis_end = min(g.next, g.e1);
+  return g;
+}
+
+template <typename T, int D, int VPL>
+__global__ void __launch_bounds__(kStBlock, StShape<T, D, VPL>::kMinBlocks)
+first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                          const T* __restrict__ v, const int32_t* __restrict__ cu, int32_t B,
+                          int64_t N, int32_t chunk, float scale_log2, int32_t key_limit,
+                          T* __restrict__ out, float* __restrict__ lse, float* __restrict__ part,
+                          DeviceStatus* status) {
+  using Sh = StShape<T, D, VPL>;
+  constexpr int EPV = Sh::kEPV, LPH = Sh::kLPH, ROW = Sh::kRow, H = Sh::kH, R = Sh::kRows;
+  extern __shared__ __align__(128) unsigned char st_smem[];
+  T* ks = reinterpret_cast<T*>(st_smem);                       // [stages][R][ROW]
+  T* vs = ks + kStStages * Sh::kStageElems;                    // [stages][R][ROW]
+  float* s_o = reinterpret_cast<float*>(vs + kStStages * Sh::kStageElems);  // [warps][ROW]
+  float* s_m = s_o + kStWarps * ROW;                           // [warps][H]
+  float* s_l = s_m + kStWarps * H;                             // [warps][H]
+  __shared__ __align__(8) uint64_t full[kStStages], empty[kStStages];
+  __shared__ volatile int abort_flag;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c0 = (int64_t)blockIdx.x * chunk;
+  const int64_t c1 = min(N, c0 + chunk);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kStWarps);
+    }
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  const int32_t first = find_sequence(cu, B, (int32_t)c0, lane);
+
+  if (warp == kStWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    uint32_t g = 0;           // stages issued
+    bool ok = true;
+    int32_t i = first;
+    for (int64_t a = c0; ok && a < c1; ++i) {
+      const Segment sg = segment_of(cu, i, a, c1, key_limit);
+      for (int64_t r0 = sg.a; r0 < sg.vis_end; r0 += R, ++g) {
+        const int s = g % kStStages;
+        if (!mbar_wait(smem_u32(&empty[s]), ((g / kStStages) & 1) ^ 1, &abort_flag, status,
+                       kSiteStProducer)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bytes = (uint32_t)(min((int64_t)R, sg.vis_end - r0) * Sh::kRowBytes);
+        mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * bytes);
+        bulk_load(smem_u32(ks + s * Sh::kStageElems), k + r0 * ROW, bytes, smem_u32(&full[s]));
+        bulk_load(smem_u32(vs + s * Sh::kStageElems), v + r0 * ROW, bytes, smem_u32(&full[s]));
+      }
+      a = sg.next;
+    }
+    if (!ok) {
+      // Copies still in flight land in this CTA's shared memory: wait for them
+      // (bounded) before the CTA can retire.
+      for (uint32_t j = g > kStStages ? g - kStStages : 0; j < g; ++j)
+        mbar_drain_wait(smem_u32(&full[j % kStStages]), (j / kStStages) & 1);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  uint32_t g = 0;  // stages consumed
+  int32_t i = first;
+  for (int64_t a = c0; a < c1; ++i) {
+    const Segment sg = segment_of(cu, i, a, c1, key_limit);
+    a = sg.next;
+    if (sg.a >= sg.vis_end) continue;  // CTA-uniform
+    float qv[VPL][EPV];
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      unpack16<T>(load16(q + (int64_t)i * ROW + (u * 32 + lane) * EPV), qv[u]);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) qv[u][e] *= scale_log2;
+    }
+    float m[VPL], l[VPL], o[VPL][EPV];
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      m[u] = -INFINITY;
+      l[u] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) o[u][e] = 0.f;
+    }
+    for (int64_t r0 = sg.a; r0 < sg.vis_end; r0 += R, ++g) {
+      const int s = g % kStStages;
+      // Every consumer warp waits for and releases every stage, so all of them
+      // pass or all of them give up at the same stage.
+      if (!warp_wait(smem_u32(&full[s]), (g / kStStages) & 1, &abort_flag, status,
+                     kSiteStConsumer))
+        return;
+      const int nr = (int)min((int64_t)R, sg.vis_end - r0);
+      const T* kst = ks + s * Sh::kStageElems;
+      const T* vst = vs + s * Sh::kStageElems;
+      for (int r = warp; r < nr; r += kStWarps) {
+        float sc[VPL];
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+          float kx[EPV];
+          unpack16<T>(*reinterpret_cast<const uint4*>(kst + r * ROW + (u * 32 + lane) * EPV),
+                      kx);
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) d = fmaf(qv[u][e], kx[e], d);
+#pragma unroll
+          for (int off = 1; off < LPH; off <<= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+          sc[u] = d;
+        }
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+          const float mx = fmaxf(m[u], sc[u]);
+          const float corr = ex2(m[u] - mx);  // 0 on the first row
+          const float p = ex2(sc[u] - mx);
+          float vx[EPV];
+          unpack16<T>(*reinterpret_cast<const uint4*>(vst + r * ROW + (u * 32 + lane) * EPV),
+                      vx);
+          l[u] = fmaf(l[u], corr, p);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) o[u][e] = fmaf(p, vx[e], o[u][e] * corr);
+          m[u] = mx;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    }
+    // Merge the warps' states: each thread combines ROW / threads elements.
+#pragma unroll
+    for (int u = 0; u < VPL; ++u) {
+      const int col = (u * 32 + lane) * EPV;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) s_o[warp * ROW + col + e] = o[u][e];
+      if (lane % LPH == 0) {
+        const int h = (u * 32 + lane) / LPH;
+        s_m[warp * H + h] = m[u];
+        s_l[warp * H + h] = l[u];
+      }
+    }
+    consumers_sync();
+    const int64_t s0 = sg.s0, e1 = sg.e1;
+    const bool whole = s0 >= c0 && e1 <= c1;
+    const int slot = s0 < c0 ? 0 : 1;
+    for (int idx = threadIdx.x; idx < ROW; idx += kStThreads) {
+      const int h = idx / D, col = idx - h * D;
+      float gm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kStWarps; ++w) gm = fmaxf(gm, s_m[w * H + h]);
+      float gl = 0.f, go = 0.f;
+#pragma unroll
+      for (int w = 0; w < kStWarps; ++w) {
+        const float lw = s_l[w * H + h];
+        const float wt = lw > 0.f ? ex2(s_m[w * H + h] - gm) : 0.f;
+        gl = fmaf(lw, wt, gl);
+        go = fmaf(s_o[w * ROW + idx], wt, go);
+      }
+      if (whole) {
+        out[(int64_t)i * ROW + idx] = from_f32<T>(go / gl);
+        if (lse && col == 0) lse[(int64_t)h * B + i] = (gm + __log2f(gl)) * kLn2;
+      } else {
+        float* p = partial_state<D>(part, blockIdx.x, slot, H, h);
+        p[2 + col] = go;
+        if (col == 0) {
+          p[0] = gm;
+          p[1] = gl;
+        }
+      }
+    }
+    consumers_sync();  // s_o, s_m, s_l free for the next sequence
+  }
+}
+
+
+// One warp per (sequence, head) whose visible keys cross a chunk edge:
+// combines its partials in chunk order, m = max m_c, l = sum l_c 2^(m_c - m),
+// o = sum o_c 2^(m_c - m) / l. Lanes take partials (for m and l) or columns
+// (for o); loads are issued sixteen partials at a time.
+template <typename T, int D>
+__global__ void first_token_stream_merge_kernel(const float* __restrict__ part,
+                                                const int32_t* __restrict__ cu, int32_t B,
+                                                int32_t H, int32_t chunk, int32_t key_limit,
+                                                T* __restrict__ out, float* __restrict__ lse) {
+  constexpr int kU = 16;
+  static_assert(D % 32 == 0, "whole columns per lane");
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t ih = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       ih < (int64_t)B * H; ih += warps) {
+    const int32_t i = (int32_t)(ih / H), h = (int32_t)(ih - (int64_t)i * H);
+    const int64_t s0 = __ldg(cu + i), s1 = __ldg(cu + i + 1);
+    const int64_t e1 = min(s1, s0 + key_limit);
+    const int64_t cb = s0 / chunk, ce = (e1 - 1) / chunk;
+    if (cb == ce) continue;  // finished by the streaming kernel
+    auto state = [&](int64_t c) {
+      return part + ((c * 2 + (c == cb ? 1 : 0)) * H + h) * (D + 2);
+    };
+    float gm = -INFINITY;
+    for (int64_t c = cb + lane; c <= ce; c += 32) gm = fmaxf(gm, state(c)[0]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, off));
+    float gl = 0.f;
+    for (int64_t c = cb + lane; c <= ce; c += 32) {
+      const float* p = state(c);
+      if (p[1] > 0.f) gl = fmaf(p[1], ex2(p[0] - gm), gl);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) gl += __shfl_xor_sync(0xffffffffu, gl, off);
+    constexpr int kC = D / 32;  // columns per lane: lane, lane + 32, ...
+    float go[kC];
+#pragma unroll
+    for (int j = 0; j < kC; ++j) go[j] = 0.f;
+    for (int64_t c = cb; c <= ce; c += kU) {
+      float mc[kU], lc[kU], oc[kU][kC];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        lc[u] = 0.f;
+        mc[u] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kC; ++j) oc[u][j] = 0.f;
+        if (c + u <= ce) {
+          const float* p = state(c + u);
+          mc[u] = p[0];
+          lc[u] = p[1];
+#pragma unroll
+          for (int j = 0; j < kC; ++j) oc[u][j] = p[2 + lane + 32 * j];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float w = lc[u] > 0.f ? ex2(mc[u] - gm) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kC; ++j) go[j] = fmaf(oc[u][j], w, go[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kC; ++j)
+      out[((int64_t)i * H + h) * D + lane + 32 * j] = from_f32<T>(go[j] / gl);
+    if (lse && lane == 0) lse[(int64_t)h * B + i] = (gm + __log2f(gl)) * kLn2;
+  }
+}
+
+template <typename T, int D, int VPL>
+pe_status launch_stream(const void* q, const void* k, const void* v, const int32_t* cu,
+                        int32_t B, int32_t H, int64_t N, int32_t chunk, float scale,
+                        int32_t key_limit, void* out, float* lse, float* part,
+                        DeviceStatus* status, cudaStream_t stream) {
+  using Sh = StShape<T, D, VPL>;
+  const auto kernel = first_token_stream_kernel<T, D, VPL>;
+  PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)Sh::kSmem));
+  // One wave of equal token ranges: every CTA resident at once moves the same
+  // bytes, and long sequences leave few partials. The range never falls below
+  // the workspace's chunk, so the partials always fit.
+  chunk = (int32_t)max((int64_t)chunk,
+                       ceil_div(N, (int64_t)device_sm_count() * Sh::kMinBlocks));
+  const int64_t blocks = ceil_div(N, chunk);
+  kernel<<<(unsigned)blocks, kStBlock, Sh::kSmem, stream>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, N,
+      chunk, scale * kLog2e, key_limit, static_cast<T*>(out), lse, part, status);
+  PE_CUDA_TRY(cudaGetLastError());
+  int64_t mblocks = ceil_div((int64_t)B * H, 8);
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (mblocks > cap) mblocks = cap;
+  first_token_stream_merge_kernel<T, D><<<(unsigned)mblocks, 256, 0, stream>>>(
+      part, cu, B, H, chunk, key_limit, static_cast<T*>(out), lse);
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+template <typename T, int D>
+pe_status dispatch_vpl(int vpl, const void* q, const void* k, const void* v, const int32_t* cu,
+                       int32_t B, int32_t H, int64_t N, int32_t chunk, float scale,
+                       int32_t key_limit, void* out, float* lse, float* part,
+                       DeviceStatus* status, cudaStream_t stream) {
+  switch (vpl) {
+#define PE_CASE(n)                                                                        \
+  case n:                                                                                 \
+    return launch_stream<T, D, n>(q, k, v, cu, B, H, N, chunk, scale, key_limit, out, lse, \
+                                  part, status, stream);
+    PE_CASE(1) PE_CASE(2) PE_CASE(3) PE_CASE(4) PE_CASE(5) PE_CASE(6) PE_CASE(7) PE_CASE(8)
+#undef PE_CASE
+    default: return PE_ERR_UNSUPPORTED;
+  }
+}
+
+template <typename T>
+pe_status dispatch_d(int D, int vpl, const void* q, const void* k, const void* v,
+                     const int32_t* cu, int32_t B, int32_t H, int64_t N, int32_t chunk,
+                     float scale, int32_t key_limit, void* out, float* lse, float* part,
+                     DeviceStatus* status, cudaStream_t stream) {
+  switch (D) {
+    case 32:
+      return dispatch_vpl<T, 32>(vpl, q, k, v, cu, B, H, N, chunk, scale, key_limit, out, lse,
+                                 part, status, stream);
+    case 64:
+      return dispatch_vpl<T, 64>(vpl, q, k, v, cu, B, H, N, chunk, scale, key_limit, out, lse,
+                                 part, status, stream);
+    case 128:
+      return dispatch_vpl<T, 128>(vpl, q, k, v, cu, B, H, N, chunk, scale, key_limit, out, lse,
+                                  part, status, stream);
+    default: return PE_ERR_UNSUPPORTED;
+  }
+}
+
+int stream_vectors_per_lane(pe_dtype dtype, int32_t H, int32_t D) {
+  const int64_t row_bytes = (int64_t)H * D * (dtype == PE_FP32 ? 4 : 2);
+  if (row_bytes % 512 != 0) return 0;
+  const int64_t vpl = row_bytes / 512;
+  return vpl >= 1 && vpl <= 8 ? (int)vpl : 0;
+}
+
+}  // namespace
+
+bool first_token_stream_supported(pe_dtype dtype, int32_t H, int32_t D) {
+  return (D == 32 || D == 64 || D == 128) && stream_vectors_per_lane(dtype, H, D) > 0;
+}
+
+int32_t first_token_stream_chunk(int64_t N) {
+  int32_t chunk = 64;
+  while (ceil_div(N, chunk) > kStMaxChunks) chunk *= 2;
+  return chunk;
+}
+
+size_t first_token_stream_partial_bytes(int64_t N, int32_t H, int32_t D) {
+  const int64_t chunks = ceil_div(N, first_token_stream_chunk(N));
+  return ((size_t)chunks * 2 * H * (D + 2) * sizeof(float) + 15) / 16 * 16;
+}
+
+pe_status fwd_first_token_stream(pe_dtype dtype, int32_t D, const void* q, const void* k,
+                                 const void* v, const int32_t* cu, int32_t B, int32_t H,
+                                 int64_t N, int32_t S, float scale, Window win, void* out,
+                                 float* lse, float* part, DeviceStatus* status,
+                                 cudaStream_t stream) {
+  const int vpl = stream_vectors_per_lane(dtype, H, D);
+  if (!vpl || !part) return PE_ERR_UNSUPPORTED;
+  // With a window the query at position 0 sees keys 0 .. right.
+  const int32_t key_limit = win.right == kUnbounded ? S : min(S, win.right + 1);
+  const int32_t chunk = first_token_stream_chunk(N);
+  if (dtype == PE_FP32)
+    return dispatch_d<float>(D, vpl, q, k, v, cu, B, H, N, chunk, scale, key_limit, out, lse,
+                             part, status, stream);
+  return dispatch_d<__nv_bfloat16>(D, vpl, q, k, v, cu, B, H, N, chunk, scale, key_limit, out,
+                                   lse, part, status, stream);
+}
+
+}  // namespace pe

@@ -19,6 +19,20 @@ pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, c
                           Window win, void* out, float* lse, float* part, TilePlan plan,
                           cudaStream_t stream);
 
+// First-token query, streaming form: chunks of whole token rows per CTA (all
+// heads); sequences that cross chunk edges leave partial states that a second
+// kernel merges. Needs first_token_stream_partial_bytes() of scratch in
+// `part`; a pipeline wait that gives up records PE_ERR_DEVICE_TIMEOUT in
+// `status`. Returns PE_ERR_UNSUPPORTED for shapes it does not take.
+bool first_token_stream_supported(pe_dtype dtype, int32_t H, int32_t D);
+int32_t first_token_stream_chunk(int64_t N);
+size_t first_token_stream_partial_bytes(int64_t N, int32_t H, int32_t D);
+pe_status fwd_first_token_stream(pe_dtype dtype, int32_t D, const void* q, const void* k,
+                                 const void* v, const int32_t* cu, int32_t B, int32_t H,
+                                 int64_t N, int32_t S, float scale, Window win, void* out,
+                                 float* lse, float* part, DeviceStatus* status,
+                                 cudaStream_t stream);
+
 // CUDA-core backward; delta is [H, Nq] fp32 scratch.
 pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,

@@ -54,8 +54,10 @@ extern "C" pe_status pe_packed_attention_fwd_noalloc(
     const int32_t* cu_seqlens, float scale, int query_is_first_token, void* out, float* lse,
     pe_stream_t stream) {
   if (num_sequences > kNoAllocMaxSequences) return PE_ERR_WORKSPACE;
+  // What the forward requires; first-token calls use more (chunk partials)
+  // only when it fits, and otherwise run without it.
   const size_t need = pe_attention_workspace_size(dtype, num_sequences, num_tokens, num_heads,
-                                                  head_dim, max_seq_len, query_is_first_token, 0);
+                                                  head_dim, max_seq_len, 0, 0);
   if (need > kNoAllocScratchBytes) return PE_ERR_WORKSPACE;
   void* scratch = nullptr;
   pe_status st = scratch_for_current_device(&scratch);
