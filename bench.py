@@ -133,9 +133,11 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- traffic
 
-def committed_traffic(kernel_name: str, source_file: str):
+def committed_traffic(kernel_name: str, source_file: str, config: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its sha1 is recorded in the summary)."""
+    the current kernel source (its sha1 is recorded in the summary) and for the
+    same workload and mode (`config`, e.g. "longdoc_bf16" or
+    "graph_fp32 first-token")."""
     path = os.path.join(ROOT, "profiles", f"{kernel_name}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -146,7 +148,7 @@ def committed_traffic(kernel_name: str, source_file: str):
             fields[key.strip()] = value.strip()
     src = os.path.join(ROOT, "padding_free_packed_gb300", "csrc", source_file)
     sha = hashlib.sha1(open(src, "rb").read()).hexdigest() if os.path.exists(src) else ""
-    if fields.get("source_sha1") != sha:
+    if fields.get("source_sha1") != sha or fields.get("config") != config:
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
@@ -155,7 +157,7 @@ def committed_traffic(kernel_name: str, source_file: str):
 
 
 KERNEL_SOURCES = {"tcgen05_bf16_d64": "pe_fwd_sm103.cu", "simt_ffma": "pe_fwd_simt.cu",
-                  "first_token_gemv": "pe_fwd_simt.cu"}
+                  "first_token_gemv": "pe_first_token.cu"}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -422,7 +424,12 @@ def run_ours(args, rank, world):
         achieved = hbm_bytes / (dom_ms * 1e-3) / 1e9
     else:
         achieved = dom_flops / (dom_ms * 1e-3) / 1e12
-    traffic = committed_traffic(dom_kernel, KERNEL_SOURCES.get(dom_kernel, ""))
+    traffic_config = (args.workload + (f"[:{args.sequences}]" if args.sequences else "")
+                      + (" first-token" if args.first_token else "")
+                      + (f" window {window[0]} {window[1]}" if window else "")
+                      + (" backward" if train and dom_kernel == bwd_kernel else "")
+                      + (f" seed {args.seed + rank}" if args.seed + rank else ""))
+    traffic = committed_traffic(dom_kernel, KERNEL_SOURCES.get(dom_kernel, ""), traffic_config)
     value = world * flops / (ms_per_step * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
