@@ -138,9 +138,11 @@ __device__ __forceinline__ void plan_decode(const int32_t* __restrict__ order,
   local = t - (lo > 0 ? __ldg(tile_end + lo - 1) : 0);
 }
 
-// Launches the plan kernel: tiles of sequence i = heads * ceil(L_i / rows_per_tile).
+// Launches the plan kernel: tiles of sequence i = heads * ceil(L_i / rows_per_tile),
+// or ceil(heads / 2) when L_i <= pair_heads_rows (a kernel that runs two heads
+// of such a sequence in one work item; 0 turns this off).
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
-                           int32_t rows_per_tile, int32_t max_seq_len, TilePlan plan,
+                           int32_t rows_per_tile, int32_t pair_heads_rows, TilePlan plan,
                            DeviceStatus* status, cudaStream_t stream);
 
 // First-token queries split each sequence's keys into chunks of this many keys

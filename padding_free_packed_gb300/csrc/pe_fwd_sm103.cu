@@ -25,7 +25,9 @@
 //               epilogue (normalise, store the real rows, log-sum-exp).
 // A work item is (sequence, head, pair of 128-row query tiles); both tiles
 // share every K/V block, and while one tile's softmax runs the tensor cores
-// work on the other tile. With local attention (a window of key positions
+// work on the other tile. A sequence of at most 128 tokens has a single query
+// tile, so (without a window) its items take two heads instead: tile t runs
+// head h + t against its own K/V block, and both softmax warpgroups work. With local attention (a window of key positions
 // around each query position) an item visits only the key blocks its rows can
 // see, and the softmax masks each row to its window. Keys past the sequence end are masked to -inf;
 // query rows past it are computed but never stored. TMA zero-fills rows
@@ -70,7 +72,8 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 384u + 64u * t; }
 constexpr uint32_t kTmemCols = 512;
 
 struct Item {
-  int32_t seq, head, pair, pad;
+  int32_t seq, head, pair;
+  int32_t dual;  // tiles 0 and 1 run heads head and head + 1 of a short sequence
 };
 
 struct alignas(1024) Smem {
@@ -90,6 +93,7 @@ struct alignas(1024) Smem {
 struct FwdParams {
   const int32_t* cu;
   int32_t B, H;
+  int32_t pair_heads_rows;  // sequences up to this long run two heads per item (0: never)
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -115,8 +119,16 @@ struct ItemRange {
 };
 
 template <bool kLocal>
-__device__ __forceinline__ ItemRange item_range(const FwdParams& p, int32_t len, int32_t r0) {
+__device__ __forceinline__ ItemRange item_range(const FwdParams& p, int32_t len, int32_t r0,
+                                                bool dual) {
   ItemRange ir;
+  if (dual) {  // block j holds the keys of head + j and serves tile j only
+    ir.kb0 = 0;
+    ir.nkv = 2;
+    ir.lo0 = ir.hi0 = 0;
+    ir.lo1 = ir.hi1 = 1;
+    return ir;
+  }
   if (!kLocal) {
     ir.kb0 = 0;
     ir.nkv = (len + kRows - 1) / kRows;
@@ -143,11 +155,17 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
   int32_t seq, local;
   plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
   const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
-  const int32_t npairs = (len + kPairRows - 1) / kPairRows;
   it.seq = seq;
+  if (len <= p.pair_heads_rows) {  // local indexes pairs of heads
+    it.head = 2 * local;
+    it.pair = 0;
+    it.dual = it.head + 1 < p.H;
+    return;
+  }
+  const int32_t npairs = (len + kPairRows - 1) / kPairRows;
   it.head = local / npairs;
   it.pair = local - it.head * npairs;
-  it.pad = 0;
+  it.dual = 0;
 }
 
 // kLocal selects the local-attention variant (window masks, block ranges and
@@ -221,7 +239,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           Item it;
           if (t >= total) {
             it.seq = -1;
-            it.head = it.pair = it.pad = 0;
+            it.head = it.pair = it.dual = 0;
           } else {
             decode_item(p, t, it);
           }
@@ -231,8 +249,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const int32_t start = __ldg(p.cu + it.seq);
           const int32_t len = __ldg(p.cu + it.seq + 1) - start;
           const int32_t r0 = it.pair * kPairRows;
-          const int ntiles = (len - r0 > kRows) ? 2 : 1;
-          const ItemRange ir = item_range<kLocal>(p, len, r0);
+          const int ntiles = (it.dual || len - r0 > kRows) ? 2 : 1;
+          const ItemRange ir = item_range<kLocal>(p, len, r0, it.dual);
           const int32_t nkv = ir.nkv;
           const int32_t x = it.head * kD;
           if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
@@ -241,8 +259,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
+          // A two-head item loads both tiles (and both K/V blocks) from the
+          // sequence's first row, one head's columns each.
           for (int tt = 0; tt < ntiles; ++tt)
-            tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full), x, start + r0 + tt * kRows);
+            tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full),
+                        it.dual ? x + tt * kD : x, it.dual ? start : start + r0 + tt * kRows);
           pending_q = item_no & 1;
           for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
             const int s = kv_no % kStages;
@@ -251,17 +272,17 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               ok = false;
               break;
             }
+            const int32_t kx = it.dual ? x + j * kD : x;
+            const int32_t ky = it.dual ? start : start + ir.kb0 + j * kRows;
             mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
-            tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), x,
-                        start + ir.kb0 + j * kRows);
+            tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), kx, ky);
             pending_k[s] = (int)ph;
             if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
-            tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), x,
-                        start + ir.kb0 + j * kRows);
+            tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), kx, ky);
             pending_v[s] = (int)ph;
           }
         }
@@ -293,8 +314,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (it.seq < 0) break;
         const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
         const int32_t r0 = it.pair * kPairRows;
-        const int ntiles = (len - r0 > kRows) ? 2 : 1;
-        const ItemRange ir = item_range<kLocal>(p, len, r0);
+        const int ntiles = (it.dual || len - r0 > kRows) ? 2 : 1;
+        const ItemRange ir = item_range<kLocal>(p, len, r0, it.dual);
         const int32_t nkv = ir.nkv;
         if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
         for (int32_t j = 0; j < nkv && ok; ++j) {
@@ -307,7 +328,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
           const uint32_t k_addr = smem_u32(S.k[s]);
           for (int t = 0; t < ntiles; ++t) {
-            if (kLocal && !ir.uses(t, j)) continue;  // outside every window of tile t
+            // Outside every window of tile t, or the other head's block.
+            if ((kLocal || it.dual) && !ir.uses(t, j)) continue;
             // The softmax must have read the previous S_t before it is overwritten.
             if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag,
                                           p.status, kSiteMma)) {
@@ -350,8 +372,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (it.seq < 0) break;
         const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
         const int32_t r0 = it.pair * kPairRows;
-        const int ntiles = (len - r0 > kRows) ? 2 : 1;
-        const ItemRange ir = item_range<kLocal>(p, len, r0);
+        const int ntiles = (it.dual || len - r0 > kRows) ? 2 : 1;
+        const ItemRange ir = item_range<kLocal>(p, len, r0, it.dual);
         const int32_t nkv = ir.nkv;
         for (int32_t j = 0; j < nkv; ++j) {
           const uint32_t c = kv_no + j;
@@ -411,9 +433,11 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.seq < 0) break;
       const int32_t start = __ldg(p.cu + it.seq);
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      const int32_t r0 = it.pair * kPairRows + t * kRows;
+      // A two-head item: this tile runs head + t over the sequence's rows.
+      const int32_t r0 = it.dual ? 0 : it.pair * kPairRows + t * kRows;
+      const int32_t head = it.dual ? it.head + t : it.head;
       if (r0 >= len) continue;                   // this tile of the pair is empty
-      const ItemRange ir = item_range<kLocal>(p, len, it.pair * kPairRows);
+      const ItemRange ir = item_range<kLocal>(p, len, it.pair * kPairRows, it.dual);
       // This row's visible key positions (local attention).
       const int32_t vis_lo = kLocal ? window_lo(p.win, r0 + row) : 0;
       const int32_t vis_hi = kLocal ? window_hi(p.win, r0 + row, len) : len - 1;
@@ -436,7 +460,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.s_free[t]));
-        const int32_t kb = ir.kb0 + j * kRows;     // key position of column 0
+        const int32_t kb = it.dual ? 0 : ir.kb0 + j * kRows;  // key position of column 0
         const int32_t kv_valid = len - kb;         // > 0; columns at or past it are masked
         if (kLocal) {
           // Columns outside [vis_lo, vis_hi] (which also ends before len).
@@ -543,7 +567,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (r0 + row < len) {
         const int64_t tok = static_cast<int64_t>(start) + r0 + row;
         const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + it.head) * kD);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + head) * kD);
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint32_t* src = o[g >> 2] + (g & 3) * 8;
@@ -554,7 +578,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
           dst[g] = w;
         }
-        if (p.lse) p.lse[static_cast<int64_t>(it.head) * p.lse_stride + tok] =
+        if (p.lse) p.lse[static_cast<int64_t>(head) * p.lse_stride + tok] =
             (m + __log2f(l)) * kLn2;
       }
     }
@@ -600,6 +624,7 @@ pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H) {
 }  // namespace
 
 int sm103_fwd_rows_per_item() { return kPairRows; }
+int sm103_fwd_pair_heads_rows(Window win) { return win.active() ? 0 : kRows; }
 
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
@@ -623,6 +648,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.cu = cu;
   prm.B = B;
   prm.H = H;
+  prm.pair_heads_rows = sm103_fwd_pair_heads_rows(win);
   prm.scale_log2 = scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;

@@ -43,6 +43,9 @@ pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
 // Tensor-core forward, bf16, head_dim 64 (sm_103a). Work items are pairs of
 // 128-row query tiles, so the tile plan is built with sm103_fwd_rows_per_item().
 int sm103_fwd_rows_per_item();
+// Sequences of at most this many tokens run two heads per work item (tile 0
+// and tile 1 take one head each); 0 with a window.
+int sm103_fwd_pair_heads_rows(Window win);
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
                     TilePlan plan, DeviceStatus* status, cudaStream_t stream);

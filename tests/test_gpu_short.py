@@ -70,3 +70,18 @@ def test_contrastive_workload_groups_match_oracle():
     ref, ref_lse = oracle.attention_fwd(x.q, x.k, x.v, cu, wl.max_seq_len, wl.scale)
     check(out, ref, "bf16", "contrastive")
     assert float(np.abs(to64(lse) - ref_lse).max()) <= 2e-3
+
+
+@pytest.mark.parametrize("heads", [1, 2, 5, 12])
+def test_two_head_items_match_oracle(heads):
+    """Sequences of at most 128 tokens run two heads per work item (tile t takes
+    head h + t); an odd head count leaves a one-head item. Lengths sit on both
+    sides of the 128-token tile and the 256-token item."""
+    rng = np.random.default_rng(60 + heads)
+    lengths = np.concatenate([[1, 2, 127, 128, 129, 255, 256, 257],
+                              rng.integers(1, 129, 120), rng.integers(129, 600, 6)])
+    rng.shuffle(lengths)
+    x, s, cu, out, lse = _run(lengths.tolist(), heads=heads, seed=61)
+    ref, ref_lse = oracle.attention_fwd(x.q, x.k, x.v, cu, s, 1 / 8.0)
+    check(out, ref, "bf16", f"two-head items, {heads} heads")
+    assert float(np.abs(to64(lse) - ref_lse).max()) <= 2e-3
