@@ -36,6 +36,11 @@
 // With local attention an item streams only the blocks inside the window band
 // (key pass: the queries that can see its keys; query pass: the keys its rows
 // can see) and the elementwise step zeroes P outside each row's window.
+// Without a window, a sequence of at most 64 tokens runs two heads per item:
+// every 128-row tile holds head h's rows in rows 0-63 and head h+1's in rows
+// 64-127 (two 64-row TMA boxes), so each product's two diagonal 64x64 blocks
+// are the two heads' and the elementwise step zeroes P and dS in the other two;
+// the accumulations then need no change.
 #include <cudaTypedefs.h>
 
 #include "pe_kernels.cuh"
@@ -64,8 +69,10 @@ constexpr uint32_t kColT1 = 0, kColT2 = 128, kColP = 256, kColDS = 320, kColAcc1
                    kColAcc2 = 448;
 
 struct Item {
-  int32_t seq, head, blk, pad;
+  int32_t seq, head, blk;
+  int32_t dual;  // rows 0-63 of every tile are head `head`, rows 64-127 head + 1
 };
+constexpr uint32_t kHalfTileBytes = kTileBytes / 2;  // 64 rows
 
 struct alignas(1024) Smem {
   __nv_bfloat16 st[2][kRows * kD];             // stationary tiles
@@ -86,6 +93,7 @@ struct alignas(1024) Smem {
 struct BwdParams {
   const int32_t* cu;
   int32_t B, H;
+  int32_t pair_heads_rows;     // sequences up to this long run two heads per item (0: never)
   int64_t Nq;                  // lse / Delta row stride (= N)
   float scale, scale_log2;
   const float* lse;            // [H, N], natural log
@@ -125,7 +133,10 @@ template <bool kKeyPass, bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                 const BwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_q64,
+                 const __grid_constant__ CUtensorMap tm_k64,
+                 const __grid_constant__ CUtensorMap tm_v64,
+                 const __grid_constant__ CUtensorMap tm_do64, const BwdParams p) {
   constexpr int kAccWarps = kKeyPass ? 2 : 1;
   constexpr int kUseWarps = 2 + kAccWarps;     // warps reading each streaming pair
   extern __shared__ uint8_t smem_raw[];
@@ -186,6 +197,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const CUtensorMap* st_map1 = kKeyPass ? &tm_v : &tm_do;
       const CUtensorMap* u_map0 = kKeyPass ? &tm_q : &tm_k;
       const CUtensorMap* u_map1 = kKeyPass ? &tm_do : &tm_v;
+      // 64-row boxes for two-head items.
+      const CUtensorMap* st_half0 = kKeyPass ? &tm_k64 : &tm_q64;
+      const CUtensorMap* st_half1 = kKeyPass ? &tm_v64 : &tm_do64;
+      const CUtensorMap* u_half0 = kKeyPass ? &tm_q64 : &tm_k64;
+      const CUtensorMap* u_half1 = kKeyPass ? &tm_do64 : &tm_v64;
       if (lane == 0) {
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
@@ -208,16 +224,22 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const int32_t t = atomicAdd(p.plan.counter, 1);
           if (t >= total) {
             it.seq = -1;
-            it.head = it.blk = it.pad = 0;
+            it.head = it.blk = it.dual = 0;
           } else {
             int32_t seq, local;
             plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
             const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
-            const int32_t nb = (len + kRows - 1) / kRows;
             it.seq = seq;
-            it.head = local / nb;
-            it.blk = local - it.head * nb;
-            it.pad = 0;
+            if (len <= p.pair_heads_rows) {  // local indexes pairs of heads
+              it.head = 2 * local;
+              it.blk = 0;
+              it.dual = it.head + 1 < p.H;
+            } else {
+              const int32_t nb = (len + kRows - 1) / kRows;
+              it.head = local / nb;
+              it.blk = local - it.head * nb;
+              it.dual = 0;
+            }
           }
           S.items[slot] = it;
           mbar_arrive(smem_u32(&S.item_full[slot]));
@@ -225,6 +247,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         it.seq = __shfl_sync(0xffffffffu, it.seq, 0);
         it.head = __shfl_sync(0xffffffffu, it.head, 0);
         it.blk = __shfl_sync(0xffffffffu, it.blk, 0);
+        it.dual = __shfl_sync(0xffffffffu, it.dual, 0);
         if (it.seq < 0) break;
         const int32_t start = __ldg(p.cu + it.seq);
         const int32_t len = __ldg(p.cu + it.seq + 1) - start;
@@ -238,8 +261,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         if (lane == 0) {
           mbar_arrive_expect_tx(smem_u32(&S.st_full), 2 * kTileBytes);
-          tma_load_2d(smem_u32(S.st[0]), st_map0, smem_u32(&S.st_full), x, start + it.blk * kRows);
-          tma_load_2d(smem_u32(S.st[1]), st_map1, smem_u32(&S.st_full), x, start + it.blk * kRows);
+          if (it.dual) {
+            for (int hh = 0; hh < 2; ++hh) {
+              tma_load_2d(smem_u32(S.st[0]) + hh * kHalfTileBytes, st_half0, smem_u32(&S.st_full),
+                          x + hh * kD, start);
+              tma_load_2d(smem_u32(S.st[1]) + hh * kHalfTileBytes, st_half1, smem_u32(&S.st_full),
+                          x + hh * kD, start);
+            }
+          } else {
+            tma_load_2d(smem_u32(S.st[0]), st_map0, smem_u32(&S.st_full), x,
+                        start + it.blk * kRows);
+            tma_load_2d(smem_u32(S.st[1]), st_map1, smem_u32(&S.st_full), x,
+                        start + it.blk * kRows);
+          }
         }
         pending_st = item_no & 1;
         for (int32_t i = 0; i < nb; ++i, ++u_no) {
@@ -252,22 +286,35 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           if (kKeyPass) {
             // -lse*log2e and -Delta of the block's 128 queries; -inf / 0 past
             // the sequence end, so those columns get P = 0.
-            const int64_t base = static_cast<int64_t>(it.head) * p.Nq + start + org + i * kRows;
+            // A two-head item's columns 0-63 are head `head`'s queries at
+            // positions 0-63, columns 64-127 head + 1's.
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int r = lane + 32 * u;
-              const bool in = org + i * kRows + r < len;
-              S.vec[s][0][r] = in ? -__ldg(p.lse + base + r) * kLog2e : -INFINITY;
-              S.vec[s][1][r] = in ? -__ldg(p.delta + base + r) : 0.f;
+              const int32_t pos = it.dual ? (r & 63) : org + i * kRows + r;
+              const int32_t hd = it.dual ? it.head + (r >> 6) : it.head;
+              const int64_t idx = static_cast<int64_t>(hd) * p.Nq + start + pos;
+              const bool in = pos < len;
+              S.vec[s][0][r] = in ? -__ldg(p.lse + idx) * kLog2e : -INFINITY;
+              S.vec[s][1][r] = in ? -__ldg(p.delta + idx) : 0.f;
             }
           }
           __syncwarp();
           if (lane == 0) {
             mbar_arrive_expect_tx(smem_u32(&S.u_full[s]), 2 * kTileBytes);
-            tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x,
-                        start + org + i * kRows);
-            tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x,
-                        start + org + i * kRows);
+            if (it.dual) {
+              for (int hh = 0; hh < 2; ++hh) {
+                tma_load_2d(smem_u32(S.u[s][0]) + hh * kHalfTileBytes, u_half0,
+                            smem_u32(&S.u_full[s]), x + hh * kD, start);
+                tma_load_2d(smem_u32(S.u[s][1]) + hh * kHalfTileBytes, u_half1,
+                            smem_u32(&S.u_full[s]), x + hh * kD, start);
+              }
+            } else {
+              tma_load_2d(smem_u32(S.u[s][0]), u_map0, smem_u32(&S.u_full[s]), x,
+                          start + org + i * kRows);
+              tma_load_2d(smem_u32(S.u[s][1]), u_map1, smem_u32(&S.u_full[s]), x,
+                          start + org + i * kRows);
+            }
           }
           if (kKeyPass) mbar_arrive(smem_u32(&S.u_full[s]));
           pending_u[s] = static_cast<int>(ph);
@@ -380,16 +427,22 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       int32_t org, nb;
       stream_blocks<kKeyPass, kLocal>(p, len, it.blk, org, nb);
       const int32_t r0 = it.blk * kRows;
+      // This thread's row: in a two-head item rows 64-127 are head + 1's rows
+      // at positions 0-63, and the column half that is the other head's is
+      // off the diagonal (P = dS = 0 there).
+      const bool off_diag = it.dual && (row >> 6) != h;  // warp-uniform
       // Streaming positions this row pairs with inside the window: the queries
       // that see this key (key pass) or the keys this query sees (query pass).
       constexpr bool windowed = kLocal;
       const Window wrow = kKeyPass ? Window{p.win.right, p.win.left} : p.win;
       const int32_t vis_lo = window_lo(wrow, r0 + row), vis_hi = window_hi(wrow, r0 + row, len);
       // Query pass: this thread's query row carries its own lse and Delta.
+      // Off the diagonal of a two-head item an infinite lse makes P = 0.
       float row_lse2 = 0.f, row_delta = 0.f;
-      if (!kKeyPass && r0 + row < len) {
-        const int64_t idx = static_cast<int64_t>(it.head) * p.Nq + start + r0 + row;
-        row_lse2 = __ldg(p.lse + idx) * kLog2e;
+      if (!kKeyPass && (it.dual ? (row & 63) : r0 + row) < len) {
+        const int64_t idx = static_cast<int64_t>(it.dual ? it.head + (row >> 6) : it.head) * p.Nq +
+                            start + (it.dual ? (row & 63) : r0 + row);
+        row_lse2 = off_diag ? INFINITY : __ldg(p.lse + idx) * kLog2e;
         row_delta = __ldg(p.delta + idx);
       }
       for (int32_t i = 0; i < nb; ++i, ++u_no, ++n_blk) {
@@ -419,13 +472,19 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.t_free));
-        const int32_t col0_pos = org + i * kRows + 64 * h;  // row position of this half's column 0
+        // Row position of this half's column 0.
+        const int32_t col0_pos = it.dual ? 0 : org + i * kRows + 64 * h;
         const int32_t col_valid = len - col0_pos;           // query pass: valid keys in this half
         const int32_t clo = vis_lo - col0_pos, chi = vis_hi - col0_pos;  // window, same origin
         // Scores that must give P = 0 become -inf: keys past the sequence end
         // (query pass, the sequence's last block only; the key pass gets them
         // from the -inf lse of queries past the end) and pairs outside the window.
-        if (!kKeyPass && col_valid < 64) {
+        if (kKeyPass && off_diag) {  // (the query pass gets P = 0 from its row's lse)
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) sv[c][cc] = 0xff800000u;
+        } else if (!kKeyPass && col_valid < 64) {
 #pragma unroll
           for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -508,9 +567,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&S.o_free));
-      if (r0 + row < len) {
-        const int64_t tok = static_cast<int64_t>(start) + r0 + row;
-        const int64_t off = (tok * p.H + it.head) * kD + 32 * h;
+      const int32_t pos_r = it.dual ? (row & 63) : r0 + row;
+      const int32_t head_r = it.dual ? it.head + (row >> 6) : it.head;
+      if (pos_r < len) {
+        const int64_t tok = static_cast<int64_t>(start) + pos_r;
+        const int64_t off = (tok * p.H + head_r) * kD + 32 * h;
         // key pass: acc1 = dV (unscaled), acc2 = dK (times scale); query pass: acc1 = dQ * scale.
         const float s1 = kKeyPass ? 1.f : p.scale;
         uint4* d1 = reinterpret_cast<uint4*>((kKeyPass ? p.out2 : p.out1) + off);
@@ -564,10 +625,11 @@ pe_status get_encoder_bwd() {
   return PE_OK;
 }
 
-pe_status make_map_bwd(CUtensorMap* map, const void* base, int64_t N, int32_t H) {
+pe_status make_map_bwd(CUtensorMap* map, const void* base, int64_t N, int32_t H,
+                       uint32_t box_rows = kRows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * kD, static_cast<cuuint64_t>(N)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * kD * 2};
-  cuuint32_t box[2] = {kD, kRows};
+  cuuint32_t box[2] = {kD, box_rows};
   cuuint32_t elem_strides[2] = {1, 1};
   CUresult r = g_encode_bwd(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
                             dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -577,8 +639,7 @@ pe_status make_map_bwd(CUtensorMap* map, const void* base, int64_t N, int32_t H)
 }
 
 template <bool kKeyPass>
-pe_status launch_pass(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                      const CUtensorMap& mdo, const BwdParams& prm, cudaStream_t stream) {
+pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, cudaStream_t stream) {
   auto kernel = prm.win.active() ? bwd_sm103_kernel<kKeyPass, true>
                                  : bwd_sm103_kernel<kKeyPass, false>;
   const size_t smem = sizeof(Smem) + 1024;
@@ -590,8 +651,10 @@ pe_status launch_pass(const CUtensorMap& mq, const CUtensorMap& mk, const CUtens
   PE_CUDA_TRY(cudaFuncGetAttributes(&attr, kernel));
   if (static_cast<uint32_t>(attr.numRegs) * kThreads < 2u * 128u * (kRegsLow + kRegsHigh))
     return PE_ERR_UNSUPPORTED;
-  PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, 0, prm.plan, nullptr, stream));
-  kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mdo, prm);
+  PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, prm.pair_heads_rows, prm.plan, nullptr,
+                          stream));
+  kernel<<<device_sm_count(), kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6],
+                                                        m[7], prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }
@@ -604,15 +667,15 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
                     DeviceStatus* status, cudaStream_t stream) {
   PE_TRY(get_encoder_bwd());
-  CUtensorMap mq, mk, mv, mdo;
-  PE_TRY(make_map_bwd(&mq, q, N, H));
-  PE_TRY(make_map_bwd(&mk, k, N, H));
-  PE_TRY(make_map_bwd(&mv, v, N, H));
-  PE_TRY(make_map_bwd(&mdo, dout, N, H));
+  // q, k, v, dO with 128-row boxes, then with 64-row boxes (two-head items).
+  CUtensorMap maps[8];
+  const void* bases[4] = {q, k, v, dout};
+  for (int m = 0; m < 8; ++m) PE_TRY(make_map_bwd(&maps[m], bases[m % 4], N, H, m < 4 ? kRows : 64));
   BwdParams prm;
   prm.cu = cu;
   prm.B = B;
   prm.H = H;
+  prm.pair_heads_rows = win.active() ? 0 : 64;
   prm.Nq = N;
   prm.scale = scale;
   prm.scale_log2 = scale * kLog2e;
@@ -623,10 +686,10 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.status = status;
   prm.out1 = static_cast<__nv_bfloat16*>(dk);
   prm.out2 = static_cast<__nv_bfloat16*>(dv);
-  PE_TRY(launch_pass<true>(mq, mk, mv, mdo, prm, stream));
+  PE_TRY(launch_pass<true>(maps, prm, stream));
   prm.out1 = static_cast<__nv_bfloat16*>(dq);
   prm.out2 = nullptr;
-  return launch_pass<false>(mq, mk, mv, mdo, prm, stream);
+  return launch_pass<false>(maps, prm, stream);
 }
 
 }  // namespace pe

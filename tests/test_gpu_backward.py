@@ -10,7 +10,7 @@ import torch
 import oracle
 import padding_free_packed_gb300 as pe
 from padding_free_packed_gb300 import workloads
-from parity import check, to64
+from parity import check, check_grad, to64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -78,3 +78,20 @@ def test_gradient_invariants_hold_per_sequence():
         rows = slice(int(cu[i]), int(cu[i + 1]))
         assert float(dk[rows].double().sum(0).abs().max()) <= 1e-4
         assert float((dv[rows].double().sum(0) - do[rows].double().sum(0)).abs().max()) <= 1e-4
+
+
+@pytest.mark.parametrize("heads", [1, 3, 12])
+def test_two_head_items_gradients(heads):
+    """Sequences of at most 64 tokens run two heads per backward work item
+    (rows 0-63 of every tile one head, rows 64-127 the next); an odd head count
+    leaves a one-head item. Lengths sit on both sides of 64 and 128."""
+    rng = np.random.default_rng(70 + heads)
+    lengths = np.concatenate([[1, 2, 63, 64, 65, 127, 128, 129], rng.integers(1, 65, 60),
+                              rng.integers(65, 400, 4)])
+    rng.shuffle(lengths)
+    x = workloads.make_custom(lengths, heads, 64, torch.bfloat16, seed=71, with_dout=True)
+    s = int(lengths.max())
+    cu, _, out, (dq, dk, dv) = _run(x, s, 0.125)
+    rq, rk, rv = oracle.attention_bwd(x.q, x.k, x.v, x.dout, cu, 0.125)
+    for name, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        check_grad(got, want, "bf16", f"two-head {name}, {heads} heads")
