@@ -161,12 +161,12 @@ extern "C" pe_status pe_packed_attention_fwd_local(
   }
   if (dtype == PE_BF16 && D == 64) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(),
-                            sm103_fwd_pair_heads_rows(win), plan, nullptr,
-                            stream));
+                            sm103_fwd_pair_heads_rows(win), sm103_fwd_quad_heads_rows(win), plan,
+                            nullptr, stream));
     return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan,
                      static_cast<DeviceStatus*>(workspace), stream);
   }
-  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_tile(), 0, plan, nullptr, stream));
+  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_tile(), 0, 0, plan, nullptr, stream));
   return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, win, out, lse, N, plan, stream);
 }
 

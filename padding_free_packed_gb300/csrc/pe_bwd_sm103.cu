@@ -651,8 +651,8 @@ pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, cudaStrea
   PE_CUDA_TRY(cudaFuncGetAttributes(&attr, kernel));
   if (static_cast<uint32_t>(attr.numRegs) * kThreads < 2u * 128u * (kRegsLow + kRegsHigh))
     return PE_ERR_UNSUPPORTED;
-  PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, prm.pair_heads_rows, prm.plan, nullptr,
-                          stream));
+  PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, prm.pair_heads_rows, 0, prm.plan,
+                          nullptr, stream));
   kernel<<<device_sm_count(), kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                         m[7], prm);
   PE_CUDA_TRY(cudaGetLastError());

@@ -139,11 +139,13 @@ __device__ __forceinline__ void plan_decode(const int32_t* __restrict__ order,
 }
 
 // Launches the plan kernel: tiles of sequence i = heads * ceil(L_i / rows_per_tile),
-// or ceil(heads / 2) when L_i <= pair_heads_rows (a kernel that runs two heads
-// of such a sequence in one work item; 0 turns this off).
+// or ceil(heads / 4) when L_i <= quad_heads_rows and ceil(heads / 2) when
+// L_i <= pair_heads_rows (kernels that run four or two heads of such a sequence
+// in one work item; 0 turns either off).
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
-                           int32_t rows_per_tile, int32_t pair_heads_rows, TilePlan plan,
-                           DeviceStatus* status, cudaStream_t stream);
+                           int32_t rows_per_tile, int32_t pair_heads_rows,
+                           int32_t quad_heads_rows, TilePlan plan, DeviceStatus* status,
+                           cudaStream_t stream);
 
 // First-token queries split each sequence's keys into chunks of this many keys
 // (one CTA each) when sequences are long (see the forward entry point); chunk

@@ -27,7 +27,10 @@
 // share every K/V block, and while one tile's softmax runs the tensor cores
 // work on the other tile. A sequence of at most 128 tokens has a single query
 // tile, so (without a window) its items take two heads instead: tile t runs
-// head h + t against its own K/V block, and both softmax warpgroups work. With local attention (a window of key positions
+// head h + t against its own K/V block, and both softmax warpgroups work. A
+// sequence of at most 64 tokens packs two heads into each tile as well (rows
+// 0-63 one head, rows 64-127 the next, loaded as 64-row boxes; each row masks
+// the other head's half of the key columns), so an item takes four heads. With local attention (a window of key positions
 // around each query position) an item visits only the key blocks its rows can
 // see, and the softmax masks each row to its window. Keys past the sequence end are masked to -inf;
 // query rows past it are computed but never stored. TMA zero-fills rows
@@ -71,10 +74,15 @@ __host__ __device__ constexpr uint32_t col_p(int t) { return 256u + 64u * t; }
 __host__ __device__ constexpr uint32_t col_o(int t) { return 384u + 64u * t; }
 constexpr uint32_t kTmemCols = 512;
 
+// Heads of a work item: one (kOneHead), one per tile (kHeadPerTile: tile t runs
+// head + t), or two per tile (kTwoHeadsPerTile: tile t runs head + 2t in rows
+// 0-63 and head + 2t + 1 in rows 64-127).
+enum : int32_t { kOneHead = 0, kHeadPerTile = 1, kTwoHeadsPerTile = 2 };
 struct Item {
   int32_t seq, head, pair;
-  int32_t dual;  // tiles 0 and 1 run heads head and head + 1 of a short sequence
+  int32_t multi;
 };
+constexpr uint32_t kHalfTileBytes = kTileBytes / 2;  // 64 rows
 
 struct alignas(1024) Smem {
   __nv_bfloat16 q[2][kRows * kD];
@@ -93,7 +101,8 @@ struct alignas(1024) Smem {
 struct FwdParams {
   const int32_t* cu;
   int32_t B, H;
-  int32_t pair_heads_rows;  // sequences up to this long run two heads per item (0: never)
+  int32_t pair_heads_rows;  // sequences up to this long run a head per tile (0: never)
+  int32_t quad_heads_rows;  // ... and up to this long two heads per tile (0: never)
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -118,15 +127,23 @@ struct ItemRange {
   __device__ bool uses(int t, int32_t j) const { return j >= lo(t) && j <= hi(t); }
 };
 
+// Query tiles of an item.
+__device__ __forceinline__ int item_tiles(const FwdParams& p, const Item& it, int32_t len) {
+  if (it.multi == kHeadPerTile) return 2;
+  if (it.multi == kTwoHeadsPerTile) return p.H - it.head > 2 ? 2 : 1;
+  return len - it.pair * kPairRows > kRows ? 2 : 1;
+}
+
 template <bool kLocal>
 __device__ __forceinline__ ItemRange item_range(const FwdParams& p, int32_t len, int32_t r0,
-                                                bool dual) {
+                                                int32_t multi, int ntiles) {
   ItemRange ir;
-  if (dual) {  // block j holds the keys of head + j and serves tile j only
+  if (multi != kOneHead) {  // block j holds the keys of tile j's heads and serves it only
     ir.kb0 = 0;
-    ir.nkv = 2;
+    ir.nkv = ntiles;
     ir.lo0 = ir.hi0 = 0;
-    ir.lo1 = ir.hi1 = 1;
+    ir.lo1 = 1;
+    ir.hi1 = ntiles - 1;
     return ir;
   }
   if (!kLocal) {
@@ -156,16 +173,29 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
   plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
   const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
   it.seq = seq;
+  it.pair = 0;
+  if (len <= p.quad_heads_rows) {  // local indexes groups of four heads
+    it.head = 4 * local;
+    it.multi = kTwoHeadsPerTile;
+    return;
+  }
   if (len <= p.pair_heads_rows) {  // local indexes pairs of heads
     it.head = 2 * local;
-    it.pair = 0;
-    it.dual = it.head + 1 < p.H;
+    it.multi = it.head + 1 < p.H ? kHeadPerTile : kOneHead;
     return;
   }
   const int32_t npairs = (len + kPairRows - 1) / kPairRows;
   it.head = local / npairs;
   it.pair = local - it.head * npairs;
-  it.dual = 0;
+  it.multi = kOneHead;
+}
+
+// Head loaded into half hh (rows 64*hh ..) of tile (or block) t of a
+// two-heads-per-tile item; a missing last head repeats the tile's first head,
+// whose rows there are computed but never stored.
+__device__ __forceinline__ int32_t packed_head(const FwdParams& p, const Item& it, int t, int hh) {
+  const int32_t h = it.head + 2 * t + hh;
+  return h < p.H ? h : it.head + 2 * t;
 }
 
 // kLocal selects the local-attention variant (window masks, block ranges and
@@ -174,7 +204,10 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
 template <bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_q64,
+                 const __grid_constant__ CUtensorMap tm_k64,
+                 const __grid_constant__ CUtensorMap tm_v64, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -239,7 +272,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           Item it;
           if (t >= total) {
             it.seq = -1;
-            it.head = it.pair = it.dual = 0;
+            it.head = it.pair = it.multi = 0;
           } else {
             decode_item(p, t, it);
           }
@@ -249,8 +282,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const int32_t start = __ldg(p.cu + it.seq);
           const int32_t len = __ldg(p.cu + it.seq + 1) - start;
           const int32_t r0 = it.pair * kPairRows;
-          const int ntiles = (it.dual || len - r0 > kRows) ? 2 : 1;
-          const ItemRange ir = item_range<kLocal>(p, len, r0, it.dual);
+          const int ntiles = item_tiles(p, it, len);
+          const ItemRange ir = item_range<kLocal>(p, len, r0, it.multi, ntiles);
           const int32_t nkv = ir.nkv;
           const int32_t x = it.head * kD;
           if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
@@ -259,11 +292,19 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
-          // A two-head item loads both tiles (and both K/V blocks) from the
-          // sequence's first row, one head's columns each.
-          for (int tt = 0; tt < ntiles; ++tt)
-            tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full),
-                        it.dual ? x + tt * kD : x, it.dual ? start : start + r0 + tt * kRows);
+          // Multi-head items load every tile (and K/V block) from the
+          // sequence's first row: one head's columns per tile, or two heads'
+          // in 64-row halves.
+          for (int tt = 0; tt < ntiles; ++tt) {
+            if (it.multi == kTwoHeadsPerTile) {
+              for (int hh = 0; hh < 2; ++hh)
+                tma_load_2d(smem_u32(S.q[tt]) + hh * kHalfTileBytes, &tm_q64, smem_u32(&S.q_full),
+                            packed_head(p, it, tt, hh) * kD, start);
+            } else {
+              tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full),
+                          it.multi ? x + tt * kD : x, it.multi ? start : start + r0 + tt * kRows);
+            }
+          }
           pending_q = item_no & 1;
           for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
             const int s = kv_no % kStages;
@@ -272,17 +313,30 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               ok = false;
               break;
             }
-            const int32_t kx = it.dual ? x + j * kD : x;
-            const int32_t ky = it.dual ? start : start + ir.kb0 + j * kRows;
+            const bool packed = it.multi == kTwoHeadsPerTile;
+            const int32_t kx = it.multi ? x + j * kD : x;
+            const int32_t ky = it.multi ? start : start + ir.kb0 + j * kRows;
             mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
-            tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), kx, ky);
+            if (packed) {
+              for (int hh = 0; hh < 2; ++hh)
+                tma_load_2d(smem_u32(S.k[s]) + hh * kHalfTileBytes, &tm_k64,
+                            smem_u32(&S.k_full[s]), packed_head(p, it, j, hh) * kD, start);
+            } else {
+              tma_load_2d(smem_u32(S.k[s]), &tm_k, smem_u32(&S.k_full[s]), kx, ky);
+            }
             pending_k[s] = (int)ph;
             if (!mbar_wait(smem_u32(&S.v_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(smem_u32(&S.v_full[s]), kTileBytes);
-            tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), kx, ky);
+            if (packed) {
+              for (int hh = 0; hh < 2; ++hh)
+                tma_load_2d(smem_u32(S.v[s]) + hh * kHalfTileBytes, &tm_v64,
+                            smem_u32(&S.v_full[s]), packed_head(p, it, j, hh) * kD, start);
+            } else {
+              tma_load_2d(smem_u32(S.v[s]), &tm_v, smem_u32(&S.v_full[s]), kx, ky);
+            }
             pending_v[s] = (int)ph;
           }
         }
@@ -314,8 +368,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (it.seq < 0) break;
         const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
         const int32_t r0 = it.pair * kPairRows;
-        const int ntiles = (it.dual || len - r0 > kRows) ? 2 : 1;
-        const ItemRange ir = item_range<kLocal>(p, len, r0, it.dual);
+        const int ntiles = item_tiles(p, it, len);
+        const ItemRange ir = item_range<kLocal>(p, len, r0, it.multi, ntiles);
         const int32_t nkv = ir.nkv;
         if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
         for (int32_t j = 0; j < nkv && ok; ++j) {
@@ -329,7 +383,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const uint32_t k_addr = smem_u32(S.k[s]);
           for (int t = 0; t < ntiles; ++t) {
             // Outside every window of tile t, or the other head's block.
-            if ((kLocal || it.dual) && !ir.uses(t, j)) continue;
+            if ((kLocal || it.multi) && !ir.uses(t, j)) continue;
             // The softmax must have read the previous S_t before it is overwritten.
             if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.s_free[t]), (n_qk[t] - 1) & 1, abort_flag,
                                           p.status, kSiteMma)) {
@@ -372,8 +426,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (it.seq < 0) break;
         const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
         const int32_t r0 = it.pair * kPairRows;
-        const int ntiles = (it.dual || len - r0 > kRows) ? 2 : 1;
-        const ItemRange ir = item_range<kLocal>(p, len, r0, it.dual);
+        const int ntiles = item_tiles(p, it, len);
+        const ItemRange ir = item_range<kLocal>(p, len, r0, it.multi, ntiles);
         const int32_t nkv = ir.nkv;
         for (int32_t j = 0; j < nkv; ++j) {
           const uint32_t c = kv_no + j;
@@ -433,11 +487,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.seq < 0) break;
       const int32_t start = __ldg(p.cu + it.seq);
       const int32_t len = __ldg(p.cu + it.seq + 1) - start;
-      // A two-head item: this tile runs head + t over the sequence's rows.
-      const int32_t r0 = it.dual ? 0 : it.pair * kPairRows + t * kRows;
-      const int32_t head = it.dual ? it.head + t : it.head;
-      if (r0 >= len) continue;                   // this tile of the pair is empty
-      const ItemRange ir = item_range<kLocal>(p, len, it.pair * kPairRows, it.dual);
+      // Multi-head items: this tile runs head + t over the sequence's rows, or
+      // (two heads per tile) head + 2t in rows 0-63 and head + 2t + 1 in rows
+      // 64-127, each row seeing its own head's half of the key columns.
+      const int ntiles = item_tiles(p, it, len);
+      if (t >= ntiles) continue;                 // this tile of the item is empty
+      const bool packed = it.multi == kTwoHeadsPerTile;
+      const int32_t r0 = it.multi ? 0 : it.pair * kPairRows + t * kRows;
+      const int32_t head = packed ? it.head + 2 * t + (quarter >> 1)
+                                  : (it.multi ? it.head + t : it.head);
+      const int32_t pos = packed ? (row & 63) : r0 + row;   // this row's query position
+      const int32_t coff = packed ? (quarter >> 1) * 64 : 0;  // column of key position 0
+      const ItemRange ir = item_range<kLocal>(p, len, it.pair * kPairRows, it.multi, ntiles);
       // This row's visible key positions (local attention).
       const int32_t vis_lo = kLocal ? window_lo(p.win, r0 + row) : 0;
       const int32_t vis_hi = kLocal ? window_hi(p.win, r0 + row, len) : len - 1;
@@ -460,7 +521,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.s_free[t]));
-        const int32_t kb = it.dual ? 0 : ir.kb0 + j * kRows;  // key position of column 0
+        const int32_t kb = it.multi ? 0 : ir.kb0 + j * kRows;  // key position of column coff
         const int32_t kv_valid = len - kb;         // > 0; columns at or past it are masked
         if (kLocal) {
           // Columns outside [vis_lo, vis_hi] (which also ends before len).
@@ -477,7 +538,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (32 * c + e >= kv_valid) sr[c][e] = 0xff800000u;  // -inf
+              if (32 * c + e < coff || 32 * c + e >= coff + kv_valid) sr[c][e] = 0xff800000u;
         }
         // Row maximum of the raw scores (scale > 0 commutes with max), four
         // independent chains of 3-input max.
@@ -564,8 +625,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_ld32(lane_base + col_o(t) + 32, o[1]);
       tmem_wait_ld(o[0]);
       tmem_wait_ld(o[1]);
-      if (r0 + row < len) {
-        const int64_t tok = static_cast<int64_t>(start) + r0 + row;
+      if (pos < len && head < p.H) {  // (a repeated head's rows are not stored)
+        const int64_t tok = static_cast<int64_t>(start) + pos;
         const float inv = 1.f / l;
         uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + head) * kD);
 #pragma unroll
@@ -608,11 +669,12 @@ pe_status get_encoder() {
   return PE_OK;
 }
 
-// [N, H*64] bf16 rows; boxes of 128 rows x 64 columns (one head), 128-byte swizzle.
-pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H) {
+// [N, H*64] bf16 rows; boxes of box_rows rows x 64 columns (one head), 128-byte swizzle.
+pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H,
+                   uint32_t box_rows = kRows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * kD, static_cast<cuuint64_t>(N)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * kD * 2};
-  cuuint32_t box[2] = {kD, kRows};
+  cuuint32_t box[2] = {kD, box_rows};
   cuuint32_t elem_strides[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                         strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -625,15 +687,19 @@ pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H) {
 
 int sm103_fwd_rows_per_item() { return kPairRows; }
 int sm103_fwd_pair_heads_rows(Window win) { return win.active() ? 0 : kRows; }
+int sm103_fwd_quad_heads_rows(Window win) { return win.active() ? 0 : kRows / 2; }
 
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
                     TilePlan plan, DeviceStatus* status, cudaStream_t stream) {
   PE_TRY(get_encoder());
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mq64, mk64, mv64;
   PE_TRY(make_map(&mq, q, N, H));
   PE_TRY(make_map(&mk, k, N, H));
   PE_TRY(make_map(&mv, v, N, H));
+  PE_TRY(make_map(&mq64, q, N, H, 64));
+  PE_TRY(make_map(&mk64, k, N, H, 64));
+  PE_TRY(make_map(&mv64, v, N, H, 64));
   const size_t smem = sizeof(Smem) + 1024;
   auto kernel = win.active() ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -649,6 +715,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.B = B;
   prm.H = H;
   prm.pair_heads_rows = sm103_fwd_pair_heads_rows(win);
+  prm.quad_heads_rows = sm103_fwd_quad_heads_rows(win);
   prm.scale_log2 = scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;
@@ -656,7 +723,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.plan = plan;
   prm.win = win;
   prm.status = status;
-  kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, prm);
+  kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mq64, mk64, mv64, prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -46,6 +46,8 @@ int sm103_fwd_rows_per_item();
 // Sequences of at most this many tokens run two heads per work item (tile 0
 // and tile 1 take one head each); 0 with a window.
 int sm103_fwd_pair_heads_rows(Window win);
+// ... and at most this many four heads (two per tile, 64 rows each).
+int sm103_fwd_quad_heads_rows(Window win);
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
                     TilePlan plan, DeviceStatus* status, cudaStream_t stream);

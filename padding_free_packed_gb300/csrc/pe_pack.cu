@@ -183,7 +183,8 @@ constexpr int kPlanBins = 2048;
 
 __global__ void __launch_bounds__(kScanThreads)
 tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32_t rows_per_tile,
-                 int32_t pair_heads_rows, TilePlan plan, DeviceStatus* status) {
+                 int32_t pair_heads_rows, int32_t quad_heads_rows, TilePlan plan,
+                 DeviceStatus* status) {
   __shared__ int32_t start[kPlanBins];
   __shared__ long long warp_sums[32];
   const int tid = threadIdx.x;
@@ -218,8 +219,9 @@ tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32
     if (pos < B) {
       const int32_t i = plan.order[pos];
       const int32_t len = __ldg(cu + i + 1) - __ldg(cu + i);
-      tiles = len <= pair_heads_rows ? (long long)(heads + 1) / 2
-                                     : (long long)heads * ceil_div(len, rows_per_tile);
+      tiles = len <= quad_heads_rows   ? (long long)(heads + 3) / 4
+              : len <= pair_heads_rows ? (long long)(heads + 1) / 2
+                                       : (long long)heads * ceil_div(len, rows_per_tile);
     }
     long long total;
     const long long incl = block_inclusive_scan(tiles, warp_sums, total);
@@ -235,11 +237,13 @@ tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32
 }  // namespace
 
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
-                           int32_t rows_per_tile, int32_t pair_heads_rows, TilePlan plan,
-                           DeviceStatus* /*status*/, cudaStream_t stream) {
+                           int32_t rows_per_tile, int32_t pair_heads_rows,
+                           int32_t quad_heads_rows, TilePlan plan, DeviceStatus* /*status*/,
+                           cudaStream_t stream) {
   static_assert(kPlanBins == 2 * kScanThreads, "plan scan covers two bins per thread");
   tile_plan_kernel<<<1, kScanThreads, 0, stream>>>(cu_seqlens, B, heads, rows_per_tile,
-                                                   pair_heads_rows, plan, nullptr);
+                                                   pair_heads_rows, quad_heads_rows, plan,
+                                                   nullptr);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

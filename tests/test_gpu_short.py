@@ -72,16 +72,18 @@ def test_contrastive_workload_groups_match_oracle():
     assert float(np.abs(to64(lse) - ref_lse).max()) <= 2e-3
 
 
-@pytest.mark.parametrize("heads", [1, 2, 5, 12])
-def test_two_head_items_match_oracle(heads):
+@pytest.mark.parametrize("heads", [1, 2, 3, 4, 5, 7, 12])
+def test_multi_head_items_match_oracle(heads):
     """Sequences of at most 128 tokens run two heads per work item (tile t takes
-    head h + t); an odd head count leaves a one-head item. Lengths sit on both
-    sides of the 128-token tile and the 256-token item."""
+    head h + t), and those of at most 64 tokens four (two per tile, 64 rows
+    each); head counts that do not divide leave items with fewer heads (a
+    missing head's half repeats a loaded one and is not stored). Lengths sit on
+    both sides of 64, the 128-token tile and the 256-token item."""
     rng = np.random.default_rng(60 + heads)
-    lengths = np.concatenate([[1, 2, 127, 128, 129, 255, 256, 257],
+    lengths = np.concatenate([[1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257],
                               rng.integers(1, 129, 120), rng.integers(129, 600, 6)])
     rng.shuffle(lengths)
     x, s, cu, out, lse = _run(lengths.tolist(), heads=heads, seed=61)
     ref, ref_lse = oracle.attention_fwd(x.q, x.k, x.v, cu, s, 1 / 8.0)
-    check(out, ref, "bf16", f"two-head items, {heads} heads")
+    check(out, ref, "bf16", f"multi-head items, {heads} heads")
     assert float(np.abs(to64(lse) - ref_lse).max()) <= 2e-3
