@@ -183,19 +183,123 @@ layernorm_kernel(const T* __restrict__ x, const T* __restrict__ res, const T* __
   }
 }
 
+// Rows of C = 32 * V * kIter channels held in registers: every load of the
+// row (and residual) is issued before any arithmetic, then mean, variance and
+// output come from registers, so a row costs one round trip to memory.
+template <typename T, int V, int kIter>
+__global__ void __launch_bounds__(kThreads)
+layernorm_row_kernel(const T* __restrict__ x, const T* __restrict__ res, const T* __restrict__ w,
+                     const T* __restrict__ b, int64_t N, float eps, T* __restrict__ y,
+                     T* __restrict__ res_out) {
+  constexpr int32_t C = 32 * V * kIter;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < N;
+       t += warps) {
+    Vec<T, V> xv[kIter], rv[kIter];
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) xv[it] = load_vec<T, V>(x + t * C + (it * 32 + lane) * V);
+    if (res) {
+#pragma unroll
+      for (int it = 0; it < kIter; ++it)
+        rv[it] = load_vec<T, V>(res + t * C + (it * 32 + lane) * V);
+    }
+    // h (= x, or x + residual rounded to T as stored in res_out) is kept in
+    // T: exact, and half the registers for bf16.
+    float sum = 0.f;
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+      if (res) {
+#pragma unroll
+        for (int u = 0; u < V; ++u)
+          xv[it].e[u] = from_f32<T>(to_f32(xv[it].e[u]) + to_f32(rv[it].e[u]));
+      }
+      if (res_out) store_vec<T, V>(res_out + t * C + (it * 32 + lane) * V, xv[it]);
+#pragma unroll
+      for (int u = 0; u < V; ++u) sum += to_f32(xv[it].e[u]);
+    }
+    const float mean = warp_sum(sum) / (float)C;
+    float sq = 0.f;
+#pragma unroll
+    for (int it = 0; it < kIter; ++it)
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const float d = to_f32(xv[it].e[u]) - mean;
+        sq = fmaf(d, d, sq);
+      }
+    const float rstd = rsqrtf(warp_sum(sq) / (float)C + eps);
+#pragma unroll
+    for (int it = 0; it < kIter; ++it) {
+      const int32_t c = (it * 32 + lane) * V;
+      const Vec<T, V> wv = load_vec<T, V>(w + c);
+      Vec<T, V> bv;
+      if (b) bv = load_vec<T, V>(b + c);
+      Vec<T, V> out;
+#pragma unroll
+      for (int u = 0; u < V; ++u)
+        out.e[u] = from_f32<T>((to_f32(xv[it].e[u]) - mean) * rstd * to_f32(wv.e[u]) +
+                               (b ? to_f32(bv.e[u]) : 0.f));
+      store_vec<T, V>(y + t * C + c, out);
+    }
+  }
+}
+
+// Exact (erf) GELU, gelu(a) = a/2 (1 + erf(a / sqrt 2)), with erf from
+// Abramowitz and Stegun, Handbook of Mathematical Functions, formula 7.1.26:
+// for z >= 0, erf(z) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) e^(-z^2)
+// with t = 1 / (1 + p z) and an absolute error of at most 1.5e-7. With
+// q = (a1 t + ... + a5 t^5) e^(-z^2) and z = |a| / sqrt 2, 1 + erf is 2 - q for
+// a >= 0 and q for a < 0 (no cancellation; the error stays absolute, as with
+// 1 + erff). One reciprocal and one exponential replace the longer erff
+// evaluation, which made this kernel issue-bound.
 __device__ __forceinline__ float gelu_exact(float a) {
-  return 0.5f * a * (1.f + erff(a * 0.70710678118654752f));
+  constexpr float kP = 0.3275911f;
+  constexpr float kA1 = 0.254829592f, kA2 = -0.284496736f, kA3 = 1.421413741f,
+                  kA4 = -1.453152027f, kA5 = 1.061405429f;
+  const float z = fabsf(a) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(kP, z, 1.f));
+  const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kA5, kA4), kA3), kA2), kA1);
+  const float q = poly * ex2(-(z * z) * kLog2e);
+  return 0.5f * a * (a >= 0.f ? 2.f - q : q);
 }
 
 // y[t, f] = gelu(x[t, f]) * x[t, F + f]; V consecutive features per thread
-// (16-byte vectors when the row and pointers allow it, else V = 1).
+// (16-byte vectors when the row and pointers allow it, else V = 1). With
+// vectors a thread loads two of them (two grid strides apart) before it
+// computes either, to keep more bytes in flight.
 template <typename T, int V>
 __global__ void __launch_bounds__(kThreads)
 geglu_kernel(const T* __restrict__ x, int64_t N, int32_t F, T* __restrict__ y) {
   const int64_t per_row = F / V;
   const int64_t total = N * per_row;
-  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if constexpr (V > 1) {
+    for (; e + stride < total; e += 2 * stride) {
+      const int64_t e2 = e + stride;
+      const int64_t t1 = e / per_row, t2 = e2 / per_row;
+      const int32_t f1 = (int32_t)(e - t1 * per_row) * V, f2 = (int32_t)(e2 - t2 * per_row) * V;
+      const T* a1 = x + t1 * 2 * F + f1;
+      const T* a2 = x + t2 * 2 * F + f2;
+      const uint4 av1 = *reinterpret_cast<const uint4*>(a1);
+      const uint4 gv1 = *reinterpret_cast<const uint4*>(a1 + F);
+      const uint4 av2 = *reinterpret_cast<const uint4*>(a2);
+      const uint4 gv2 = *reinterpret_cast<const uint4*>(a2 + F);
+      T o1[V], o2[V];
+      const T* ae1 = reinterpret_cast<const T*>(&av1);
+      const T* ge1 = reinterpret_cast<const T*>(&gv1);
+      const T* ae2 = reinterpret_cast<const T*>(&av2);
+      const T* ge2 = reinterpret_cast<const T*>(&gv2);
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        o1[u] = from_f32<T>(gelu_exact(to_f32(ae1[u])) * to_f32(ge1[u]));
+        o2[u] = from_f32<T>(gelu_exact(to_f32(ae2[u])) * to_f32(ge2[u]));
+      }
+      *reinterpret_cast<uint4*>(y + t1 * F + f1) = *reinterpret_cast<const uint4*>(o1);
+      *reinterpret_cast<uint4*>(y + t2 * F + f2) = *reinterpret_cast<const uint4*>(o2);
+    }
+  }
+  for (; e < total; e += stride) {
     const int64_t t = e / per_row;
     const int32_t f = (int32_t)(e - t * per_row) * V;
     const T* a = x + t * 2 * F + f;
@@ -248,6 +352,28 @@ pe_status launch_layernorm(const void* x, const void* res, const void* w, const 
   constexpr int V = 16 / sizeof(T);
   const bool vec = C % V == 0 && aligned(x, 16) && aligned(w, 16) && aligned(y, 16) &&
                    (!res || aligned(res, 16)) && (!res_out || aligned(res_out, 16));
+  // Whole rows in registers when a row is 1..8 warp-wide vectors.
+  const int32_t iters = C / (32 * V);
+  if (vec && C % (32 * V) == 0 && iters >= 1 && iters <= 8 && (!b || aligned(b, 16))) {
+    const unsigned grid = grid_for(kThreads / 32, N);
+    const T* xt = static_cast<const T*>(x);
+    const T* rt = static_cast<const T*>(res);
+    const T* wt = static_cast<const T*>(w);
+    const T* bt = static_cast<const T*>(b);
+    T* yt = static_cast<T*>(y);
+    T* ot = static_cast<T*>(res_out);
+    switch (iters) {
+#define PE_CASE(n)                                                                          \
+  case n:                                                                                   \
+    layernorm_row_kernel<T, V, n><<<grid, kThreads, 0, stream>>>(xt, rt, wt, bt, N, eps, yt, \
+                                                                 ot);                       \
+    break;
+      PE_CASE(1) PE_CASE(2) PE_CASE(3) PE_CASE(4) PE_CASE(5) PE_CASE(6) PE_CASE(7) PE_CASE(8)
+#undef PE_CASE
+    }
+    PE_CUDA_TRY(cudaGetLastError());
+    return PE_OK;
+  }
   auto kernel = vec ? layernorm_kernel<T, V> : layernorm_kernel<T, 1>;
   kernel<<<grid_for(kThreads / 32, N), kThreads, 0, stream>>>(
       static_cast<const T*>(x), static_cast<const T*>(res), static_cast<const T*>(w),

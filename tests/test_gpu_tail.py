@@ -67,7 +67,7 @@ def test_rope_matches_oracle(dtype, d, hq, hk, theta):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("c", [768, 1024, 1000, 64])
+@pytest.mark.parametrize("c", [768, 1024, 1000, 64, 128, 256, 2048])
 @pytest.mark.parametrize("with_bias,with_residual", [(False, True), (True, False), (False, False)])
 def test_layernorm_matches_oracle(dtype, c, with_bias, with_residual):
     rng = np.random.default_rng(203)
@@ -93,6 +93,19 @@ def test_layernorm_matches_oracle(dtype, c, with_bias, with_residual):
 def test_geglu_matches_oracle(dtype, f):
     x = torch.from_numpy(np.random.default_rng(204).standard_normal((2500, 2 * f)) * 1.5).to(dtype)
     _close(pe.pe_geglu(x.to(DEV)), oracle.geglu(x), dtype, f"geglu f={f}")
+
+
+def test_gelu_against_exact_gelu_on_a_dense_range():
+    """GeGLU's GELU takes erf from Abramowitz and Stegun's formula 7.1.26
+    (|error| <= 1.5e-7 in erf, so |error| <= 0.75e-7 |x| in GELU before fp32
+    rounding): with a gate of 1, fp32 outputs over [-12, 12] stay within
+    3e-6 max(1, |x|) of the exact GELU in fp64."""
+    x = np.linspace(-12.0, 12.0, 200001).astype(np.float32)
+    inp = torch.from_numpy(np.stack([x, np.ones_like(x)], axis=1))
+    got = to64(pe.pe_geglu(inp.to(DEV))).ravel()
+    exact = to64(torch.nn.functional.gelu(torch.from_numpy(x.astype(np.float64))))
+    err = np.abs(got - exact)
+    assert float((err - 3e-6 * np.maximum(1.0, np.abs(x))).max()) <= 0
 
 
 def test_layer_tail_in_a_cuda_graph():
