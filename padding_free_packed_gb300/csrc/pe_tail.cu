@@ -267,18 +267,21 @@ __device__ __forceinline__ float gelu_exact(float a) {
 // (16-byte vectors when the row and pointers allow it, else V = 1). With
 // vectors a thread loads two of them (two grid strides apart) before it
 // computes either, to keep more bytes in flight.
-template <typename T, int V>
+// Idx is the index type: 32-bit when N * F / V fits, so that splitting a
+// vector index into (token, feature) is a 32-bit division.
+template <typename T, int V, typename Idx>
 __global__ void __launch_bounds__(kThreads)
-geglu_kernel(const T* __restrict__ x, int64_t N, int32_t F, T* __restrict__ y) {
-  const int64_t per_row = F / V;
-  const int64_t total = N * per_row;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+geglu_kernel(const T* __restrict__ x, Idx N, int32_t F, T* __restrict__ y) {
+  const Idx per_row = (Idx)(F / V);
+  const Idx total = N * per_row;
+  const Idx stride = (Idx)gridDim.x * blockDim.x;
+  Idx e = (Idx)blockIdx.x * blockDim.x + threadIdx.x;
   if constexpr (V > 1) {
-    for (; e + stride < total; e += 2 * stride) {
-      const int64_t e2 = e + stride;
-      const int64_t t1 = e / per_row, t2 = e2 / per_row;
-      const int32_t f1 = (int32_t)(e - t1 * per_row) * V, f2 = (int32_t)(e2 - t2 * per_row) * V;
+    for (; e < total - min(total, stride); e += 2 * stride) {  // e + stride < total
+      const Idx e2 = e + stride;
+      const Idx q1 = e / per_row, q2 = e2 / per_row;
+      const int32_t f1 = (int32_t)(e - q1 * per_row) * V, f2 = (int32_t)(e2 - q2 * per_row) * V;
+      const int64_t t1 = q1, t2 = q2;
       const T* a1 = x + t1 * 2 * F + f1;
       const T* a2 = x + t2 * 2 * F + f2;
       const uint4 av1 = *reinterpret_cast<const uint4*>(a1);
@@ -300,8 +303,9 @@ geglu_kernel(const T* __restrict__ x, int64_t N, int32_t F, T* __restrict__ y) {
     }
   }
   for (; e < total; e += stride) {
-    const int64_t t = e / per_row;
-    const int32_t f = (int32_t)(e - t * per_row) * V;
+    const Idx q = e / per_row;
+    const int32_t f = (int32_t)(e - q * per_row) * V;
+    const int64_t t = q;
     const T* a = x + t * 2 * F + f;
     const T* g = a + F;
     T out[V];
@@ -385,12 +389,24 @@ pe_status launch_layernorm(const void* x, const void* res, const void* w, const 
 template <typename T>
 pe_status launch_geglu(const void* x, int64_t N, int32_t F, void* y, cudaStream_t stream) {
   constexpr int V = 16 / sizeof(T);
+  // 32-bit indices while every vector index and the grid stride past it fit.
+  const bool idx32 = N * F < (1LL << 31);
   if (F % V == 0 && aligned(x, 16) && aligned(y, 16)) {
-    geglu_kernel<T, V><<<grid_for(kThreads, N * (F / V)), kThreads, 0, stream>>>(
-        static_cast<const T*>(x), N, F, static_cast<T*>(y));
+    const unsigned grid = grid_for(kThreads, N * (F / V));
+    if (idx32)
+      geglu_kernel<T, V, uint32_t><<<grid, kThreads, 0, stream>>>(
+          static_cast<const T*>(x), (uint32_t)N, F, static_cast<T*>(y));
+    else
+      geglu_kernel<T, V, int64_t><<<grid, kThreads, 0, stream>>>(
+          static_cast<const T*>(x), N, F, static_cast<T*>(y));
   } else {
-    geglu_kernel<T, 1><<<grid_for(kThreads, N * F), kThreads, 0, stream>>>(
-        static_cast<const T*>(x), N, F, static_cast<T*>(y));
+    const unsigned grid = grid_for(kThreads, N * F);
+    if (idx32)
+      geglu_kernel<T, 1, uint32_t><<<grid, kThreads, 0, stream>>>(
+          static_cast<const T*>(x), (uint32_t)N, F, static_cast<T*>(y));
+    else
+      geglu_kernel<T, 1, int64_t><<<grid, kThreads, 0, stream>>>(
+          static_cast<const T*>(x), N, F, static_cast<T*>(y));
   }
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
