@@ -28,6 +28,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -80,11 +81,13 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str | None = None):
         self.gpu_index = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/pe_clocks_{os.getpid()}.csv"
+        # The raw samples go where --clocks-csv says, else to a temporary file.
+        self.keep = path is not None
+        self.path = path.replace("{gpu}", str(gpu_index)) if path else os.path.join(
+            tempfile.gettempdir(), f"pe_clocks_gpu{gpu_index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -125,6 +128,8 @@ class ClockSampler:
                 for name, flag in zip(names, parts[5:9]):
                     if flag.lower() == "active":
                         reasons.add(name)
+        if not self.keep:
+            os.remove(self.path)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
@@ -299,7 +304,7 @@ def run_ours(args, rank, world):
     for _ in range(args.warmup):
         step(lengths_d, dev_grids, False)
     barrier()
-    with ClockSampler(local_rank) as clocks:
+    with ClockSampler(local_rank, args.clocks_csv) as clocks:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
         for _ in range(args.steps):
@@ -643,7 +648,7 @@ def run_tail(args, rank, world):
     for _ in range(args.warmup):
         step(False)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local_rank) as clocks:
+    with ClockSampler(local_rank, args.clocks_csv) as clocks:
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for _ in range(args.steps):
@@ -778,6 +783,9 @@ def main():
                     help="add the attention backward (dO ~ N(0,1)) to a forward-only workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the raw nvidia-smi clock samples of the timed region in this file "
+                         "({gpu} is replaced by the GPU index)")
     ap.add_argument("--cpu-rows", type=int, default=98304,
                     help="query rows in the cpu_baseline sample (about 10-30 s of CPU work)")
     ap.add_argument("--ref-rows", type=int, default=2048,
