@@ -94,3 +94,44 @@ def test_no_gpu_means_unsupported(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fwd(lib) == 4
+
+
+def _round16(x):
+    return (x + 15) // 16 * 16
+
+
+def _plan_bytes(b):
+    return 32 + 2 * _round16(4 * b)
+
+
+def _stream_partials(n, h, d):
+    chunk = 64
+    while -(-n // chunk) > 16384:
+        chunk *= 2
+    return _round16(-(-n // chunk) * 2 * h * (d + 2) * 4)
+
+
+def _split_partials(b, h, d, s):
+    ns = 1 if s <= 1024 else -(-s // 1024)
+    return 0 if ns == 1 else _round16(b * h * ns * (d + 2) * 4)
+
+
+@pytest.mark.parametrize("dtype,b,n,h,d,s,streaming", [
+    (0, 32, 169151, 16, 64, 8192, True),     # long documents: 2 KiB bf16 rows
+    (0, 600, 2_000_000, 4, 64, 8192, True),  # past 16384 chunks of 64: chunk 128
+    (1, 1024, 90487, 8, 64, 256, True),      # graph workload: 2 KiB fp32 rows
+    (0, 320, 32299, 12, 64, 8192, True),     # contrastive: 1.5 KiB rows
+    (0, 10, 40000, 3, 64, 5000, False),      # 384-byte rows: per-(sequence, head) split
+    (0, 10, 40000, 16, 96, 5000, False),     # head_dim 96: per-(sequence, head) split
+    (1, 8, 91, 2, 8, 32, False),             # tiny rows, short sequences: no partials
+])
+def test_first_token_workspace_holds_the_partial_states(lib, dtype, b, n, h, d, s, streaming):
+    """First-token forwards report room for partial softmax states: equal token
+    chunks (>= 64 tokens, at most 16384 of them) with two states of H*(d+2)
+    fp32 each when a token row is 1..8 x 512 bytes and head_dim is 32, 64 or
+    128; otherwise 1024-key chunks per (sequence, head) when max_seq_len > 1024."""
+    got = lib.pe_attention_workspace_size(dtype, b, n, h, d, s, 1, 0)
+    extra = _stream_partials(n, h, d) if streaming else _split_partials(b, h, d, s)
+    assert got == _plan_bytes(b) + extra
+    # Without the first-token flag only the plan is needed.
+    assert lib.pe_attention_workspace_size(dtype, b, n, h, d, s, 0, 0) == _plan_bytes(b)
