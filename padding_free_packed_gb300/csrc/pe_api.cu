@@ -166,7 +166,7 @@ extern "C" pe_status pe_packed_attention_fwd_local(
     return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan,
                      static_cast<DeviceStatus*>(workspace), stream);
   }
-  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_tile(), 0, 0, plan, nullptr, stream));
+  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_item(), 0, 0, plan, nullptr, stream));
   return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, win, out, lse, N, plan, stream);
 }
 

@@ -226,7 +226,7 @@ pe_status dispatch_first(int D, const void* q, const void* k, const void* v, con
 
 }  // namespace
 
-int simt_rows_per_tile() { return kBM; }
+int simt_rows_per_item() { return kItemRows; }
 
 pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, float scale, Window win, void* out,

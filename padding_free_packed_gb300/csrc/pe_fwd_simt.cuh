@@ -7,8 +7,11 @@
 // head_dim has no tensor-core kernel. Every sequence attends only to its own
 // keys (module docstring, "Data flow of a packed forward").
 //
-// A persistent grid claims tiles of 64 query rows of one (sequence, head) from
-// the longest-first tile plan. Each CTA runs 256 threads as a 16 x 16 grid:
+// A persistent grid claims work items of 128 query rows of one (sequence,
+// head) from the longest-first tile plan and runs them as two tiles of 64
+// rows; when all of the sequence's keys fit in the staging buffers (at most
+// two blocks of 64 for fp32, one for bf16), the second tile reuses the first
+// tile's staged K and V instead of loading them again. Each CTA runs 256 threads as a 16 x 16 grid:
 // thread (ty, tx) owns query rows ty + 16*ii and, per key block of 64, key
 // columns tx + 16*jj (ii, jj < 4) of the score tile and output columns
 // tx*CPT .. tx*CPT+CPT-1. Softmax is online, in the base-2 domain, with the
@@ -37,6 +40,7 @@ namespace pe {
 namespace fwd_simt_impl {
 
 constexpr int kBM = 64;          // query rows per tile
+constexpr int kItemRows = 2 * kBM;  // query rows per work item (two tiles)
 constexpr int kBN = 64;          // keys per block
 constexpr int kThreads = 256;    // 16 x 16
 constexpr int kPsPitch = kBN + 16;  // fp32 words per row of P: a warp's two rows sit 16 banks apart
@@ -221,7 +225,9 @@ __device__ __forceinline__ void attend_block(const float* __restrict__ Qs,
   }
 }
 
-// One 64-row query tile of (sequence, head) with NI x 16 rows computed.
+// One 64-row query tile of (sequence, head) with NI x 16 rows computed. With
+// kv_resident the key blocks are already in the stages, in block order from
+// stage 0 (full attention with at most kStages blocks), and are not staged again.
 template <typename T, int D, bool kLocal, int NI>
 __device__ __forceinline__ void attend_tile(const T* __restrict__ q, const T* __restrict__ k,
                                             const T* __restrict__ v, int32_t H, float scale_log2,
@@ -229,7 +235,7 @@ __device__ __forceinline__ void attend_tile(const T* __restrict__ q, const T* __
                                             float* __restrict__ lse, int64_t lse_stride,
                                             float* Qs, float* Ks0, float* Vs0, float* Ps,
                                             int32_t start, int32_t len, int32_t h, int32_t q0,
-                                            int rows_valid) {
+                                            int rows_valid, bool kv_resident) {
   using Shape = SimtShape<T, D>;
   constexpr int P = Shape::kPitch;
   constexpr int CPT = Shape::kCPT;
@@ -248,9 +254,11 @@ __device__ __forceinline__ void attend_tile(const T* __restrict__ q, const T* __
 
   if constexpr (Shape::kAsync) {
     stage_rows_async<D>(Qs, qt, row_stride, rows_valid);
-    const int kv0 = min(kBN, kb_end - kb_begin);
-    stage_rows_async<D>(Ks0, kh + (int64_t)kb_begin * row_stride, row_stride, kv0);
-    stage_rows_async<D>(Vs0, vh + (int64_t)kb_begin * row_stride, row_stride, kv0);
+    if (!kv_resident) {
+      const int kv0 = min(kBN, kb_end - kb_begin);
+      stage_rows_async<D>(Ks0, kh + (int64_t)kb_begin * row_stride, row_stride, kv0);
+      stage_rows_async<D>(Vs0, vh + (int64_t)kb_begin * row_stride, row_stride, kv0);
+    }
     cp_async_commit();
   } else {
     stage_rows<T, D>(Qs, qt, row_stride, rows_valid);
@@ -279,7 +287,7 @@ __device__ __forceinline__ void attend_tile(const T* __restrict__ q, const T* __
       // no longer read by the previous block.
       __syncthreads();
       const int32_t nb = kb + kBN;
-      if (nb < kb_end) {
+      if (!kv_resident && nb < kb_end) {
         const int nv = min(kBN, kb_end - nb);
         float* Kn = Ks0 + (stage ^ 1) * kStageFloats;
         float* Vn = Vs0 + (stage ^ 1) * kStageFloats;
@@ -290,8 +298,10 @@ __device__ __forceinline__ void attend_tile(const T* __restrict__ q, const T* __
       stage ^= 1;
     } else {
       __syncthreads();  // previous block's Ks/Vs/Ps fully consumed
-      stage_rows<T, D>(Ks, kh + (int64_t)kb * row_stride, row_stride, keys_valid);
-      stage_rows<T, D>(Vs, vh + (int64_t)kb * row_stride, row_stride, keys_valid);
+      if (!kv_resident) {
+        stage_rows<T, D>(Ks, kh + (int64_t)kb * row_stride, row_stride, keys_valid);
+        stage_rows<T, D>(Vs, vh + (int64_t)kb * row_stride, row_stride, keys_valid);
+      }
       __syncthreads();
     }
     if (keys_valid > 32)
@@ -348,16 +358,21 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     int32_t seq, local;
     plan_decode(plan.order, plan.tile_end, B, t, seq, local);
     const int32_t start = __ldg(cu + seq), len = __ldg(cu + seq + 1) - start;
-    const int32_t nqb = (len + kBM - 1) / kBM;
+    const int32_t nqb = (len + kItemRows - 1) / kItemRows;
     const int32_t h = local / nqb, qb = local - h * nqb;
-    const int32_t q0 = qb * kBM;
-    const int rows_valid = min(kBM, len - q0);
-    if (rows_valid > 32)
-      attend_tile<T, D, kLocal, 4>(q, k, v, H, scale_log2, win, out, lse, lse_stride, Qs, Ks0,
-                                   Vs0, Ps, start, len, h, q0, rows_valid);
-    else
-      attend_tile<T, D, kLocal, 2>(q, k, v, H, scale_log2, win, out, lse, lse_stride, Qs, Ks0,
-                                   Vs0, Ps, start, len, h, q0, rows_valid);
+    // The item's second tile keeps the staged keys when they are all of the
+    // sequence's (full attention, at most kStages blocks).
+    const bool reuse = !kLocal && len <= Shape::kStages * kBN;
+    for (int32_t q0 = qb * kItemRows; q0 < min(len, (qb + 1) * kItemRows); q0 += kBM) {
+      const int rows_valid = min(kBM, len - q0);
+      const bool resident = reuse && q0 > qb * kItemRows;
+      if (rows_valid > 32)
+        attend_tile<T, D, kLocal, 4>(q, k, v, H, scale_log2, win, out, lse, lse_stride, Qs, Ks0,
+                                     Vs0, Ps, start, len, h, q0, rows_valid, resident);
+      else
+        attend_tile<T, D, kLocal, 2>(q, k, v, H, scale_log2, win, out, lse, lse_stride, Qs, Ks0,
+                                     Vs0, Ps, start, len, h, q0, rows_valid, resident);
+    }
   }
 }
 

@@ -6,7 +6,7 @@
 namespace pe {
 
 // CUDA-core forward (fp32 any head_dim; bf16 head_dims without a tensor-core kernel).
-int simt_rows_per_tile();
+int simt_rows_per_item();
 pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, float scale, Window win, void* out,
                    float* lse, int64_t N, TilePlan plan, cudaStream_t stream);
