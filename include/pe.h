@@ -53,7 +53,8 @@ const char* pe_status_string(int status);
 /* Version of this ABI (incremented when an entry point is added or changed;
  * 2 added pe_packed_attention_fwd_local, pe_packed_attention_bwd_local,
  * pe_rows_workspace_size, pe_pack_document_ids, pe_flatten_packed_metadata,
- * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu, pe_upload_packed). */
+ * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu, pe_upload_packed;
+ * later additions within 2: pe_download_padded). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -121,6 +122,30 @@ pe_status pe_gather_packed(const void* padded, const int64_t* flat_index, int64_
 pe_status pe_upload_packed(const void* padded_host, const int32_t* lengths_host,
                            int32_t num_sequences, int32_t max_seq_len, int64_t row_bytes,
                            void* packed, pe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Packed device buffer -> host padded grid with the copy engines: the real
+ * rows of pe_scatter_padded's result (function _padded_packed_attention,
+ * to_dense_batch) written into a grid in host memory, for callers that hold
+ * the lengths on the host. One asynchronous device-to-host copy per sequence
+ * (packed rows cu_i .. +L_i-1 to padded rows i*max_seq_len .. +L_i-1) on
+ * `stream`; no kernel runs, and only real rows cross the host link.
+ *
+ * Pad rows (j >= L_i) of padded_host are NOT written: to_dense_batch's zero
+ * fill is the caller's, once per layout (e.g. a host grid allocated zeroed and
+ * reused for batches of the same lengths).
+ *
+ * packed:       device, [sum L_i] rows of row_bytes bytes.
+ * lengths_host: int32 [num_sequences], host; 1 <= L_i <= max_seq_len, else
+ *               PE_ERR_BAD_LENGTH before any copy; PE_ERR_OVERFLOW if
+ *               sum L_i >= 2^31.
+ * padded_host:  host memory (pinned for asynchronous copies), [num_sequences *
+ *               max_seq_len] rows of row_bytes bytes.
+ * The rows are on the host once `stream` has passed the copies.
+ * ------------------------------------------------------------------------ */
+pe_status pe_download_padded(const void* packed, const int32_t* lengths_host,
+                             int32_t num_sequences, int32_t max_seq_len, int64_t row_bytes,
+                             void* padded_host, pe_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Packed -> padded scatter with zero fill (function _padded_packed_attention,

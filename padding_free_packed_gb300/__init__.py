@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     attention_workspace_bytes,
     load_library,
     pe_attention_kernel,
+    pe_download_padded,
     pe_gather_packed,
     pe_flatten_packed_metadata,
     pe_geglu,

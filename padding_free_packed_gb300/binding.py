@@ -28,6 +28,7 @@ EXPORTED = (
     "pe_packed_attention_bwd_local", "pe_read_device_status", "pe_attention_kernel",
     "pe_rows_workspace_size", "pe_pack_document_ids", "pe_flatten_packed_metadata",
     "pe_packed_positions", "pe_rope_packed", "pe_layernorm", "pe_geglu", "pe_upload_packed",
+    "pe_download_padded",
 )
 
 _lib = None
@@ -90,6 +91,8 @@ def load_library(path: str = LIB_PATH):
     lib.pe_flatten_packed_metadata.restype = c.c_int
     lib.pe_upload_packed.argtypes = [vp, vp, i32, i32, i64, vp, vp]
     lib.pe_upload_packed.restype = c.c_int
+    lib.pe_download_padded.argtypes = [vp, vp, i32, i32, i64, vp, vp]
+    lib.pe_download_padded.restype = c.c_int
     lib.pe_packed_positions.argtypes = [vp, i32, i64, vp, vp]
     lib.pe_packed_positions.restype = c.c_int
     lib.pe_rope_packed.argtypes = [c.c_int, vp, i32, vp, i32, vp, i64, i32, c.c_double, vp]
@@ -238,6 +241,30 @@ def pe_upload_packed(padded_host: torch.Tensor, lengths_host, out: torch.Tensor)
            lib.pe_upload_packed(_ptr(padded_host), lengths.ctypes.data, b, s, row_bytes,
                                 _ptr(out), _stream(out.device)))
     return out
+
+
+def pe_download_padded(packed: torch.Tensor, lengths_host, out_host: torch.Tensor) -> torch.Tensor:
+    """Copies the packed device rows [sum L, ...] into the real rows of the host
+    [B, S, ...] grid `out_host` with one asynchronous copy per sequence on the
+    current stream of packed's device (pinned host memory for asynchrony). Pad
+    rows of out_host are not written: allocate it zeroed for to_dense_batch's
+    zero fill."""
+    lib = load_library()
+    if out_host.is_cuda or not out_host.is_contiguous():
+        raise ValueError("out_host must be a contiguous host tensor")
+    lengths = np.ascontiguousarray(np.asarray(lengths_host, dtype=np.int32))
+    b, s = int(out_host.shape[0]), int(out_host.shape[1])
+    if lengths.shape != (b,):
+        raise ValueError("one length per grid row")
+    packed = _cuda(packed, "packed")
+    row_bytes = out_host.element_size() * math.prod(tuple(out_host.shape[2:]))
+    if packed.dtype != out_host.dtype or packed.numel() != int(lengths.sum()) * (
+            row_bytes // out_host.element_size()):
+        raise ValueError("packed must hold sum(L) rows of the grid's row shape and dtype")
+    _check("pe_download_padded",
+           lib.pe_download_padded(_ptr(packed), lengths.ctypes.data, b, s, row_bytes,
+                                  _ptr(out_host), _stream(packed.device)))
+    return out_host
 
 
 def pe_scatter_padded(packed: torch.Tensor, cu_seqlens: torch.Tensor, max_seq_len: int,

@@ -337,3 +337,30 @@ extern "C" pe_status pe_upload_packed(const void* padded_host, const int32_t* le
   }
   return PE_OK;
 }
+
+// Packed device buffer -> host-resident padded grid with the copy engines,
+// the mirror of pe_upload_packed; pad rows are left as they are.
+extern "C" pe_status pe_download_padded(const void* packed, const int32_t* lengths_host,
+                                        int32_t B, int32_t S, int64_t row_bytes,
+                                        void* padded_host, pe_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (B < 0 || S < 1 || row_bytes < 1) return PE_ERR_INVALID_ARG;
+  if (B == 0) return PE_OK;
+  if (!padded_host || !lengths_host || !packed) return PE_ERR_INVALID_ARG;
+  int64_t total = 0;
+  for (int32_t i = 0; i < B; ++i) {
+    if (lengths_host[i] < 1 || lengths_host[i] > S) return PE_ERR_BAD_LENGTH;
+    total += lengths_host[i];
+  }
+  if (total >= (1LL << 31)) return PE_ERR_OVERFLOW;
+  const char* src = static_cast<const char*>(packed);
+  char* dst = static_cast<char*>(padded_host);
+  int64_t t = 0;
+  for (int32_t i = 0; i < B; ++i) {
+    PE_CUDA_TRY(cudaMemcpyAsync(dst + (int64_t)i * S * row_bytes, src + t * row_bytes,
+                                (size_t)lengths_host[i] * row_bytes, cudaMemcpyDeviceToHost,
+                                stream));
+    t += lengths_host[i];
+  }
+  return PE_OK;
+}

@@ -89,6 +89,21 @@ def test_host_checks_reject_bad_arguments(lib):
     assert lib.pe_scatter_padded(16, 16, 0, 4, 16, 16, None) == 0
 
 
+def test_host_copies_check_lengths_before_any_copy(lib):
+    """pe_upload_packed and pe_download_padded read the host lengths and reject
+    bad ones before enqueuing anything (fake, never-used device addresses)."""
+    bad = (ctypes.c_int32 * 2)(5, 4)     # 5 > max_seq_len 4
+    zero = (ctypes.c_int32 * 2)(0, 4)
+    for fn in (lib.pe_upload_packed, lib.pe_download_padded):
+        assert fn(16, bad, 2, 4, 32, 16, None) == 2
+        assert fn(16, zero, 2, 4, 32, 16, None) == 2
+        assert fn(16, bad, -1, 4, 32, 16, None) == 1
+        assert fn(16, bad, 2, 0, 32, 16, None) == 1
+        assert fn(16, bad, 2, 4, 0, 16, None) == 1
+        assert fn(16, None, 2, 4, 32, 16, None) == 1
+        assert fn(16, bad, 0, 4, 32, 16, None) == 0   # nothing to move
+
+
 def test_no_gpu_means_unsupported(lib):
     import torch
     if torch.cuda.is_available():

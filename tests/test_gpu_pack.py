@@ -151,3 +151,38 @@ def test_upload_rejects_bad_lengths():
         pe.pe_upload_packed(grid, [5, 4], out=out)      # 5 > max_seq_len
     with pytest.raises(pe.PackedAttentionError):
         pe.pe_upload_packed(grid, [0, 4], out=out)
+
+
+@pytest.mark.parametrize("dtype,row", [(torch.bfloat16, (4, 64)), (torch.float32, (3, 5))])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_download_padded_writes_the_real_rows(dtype, row, pinned):
+    """pe_download_padded (copy engines, one copy per sequence) puts the packed
+    rows where the device scatter puts them, bit for bit, and leaves the pad
+    rows of the host grid as the caller filled them (zero, for
+    to_dense_batch's fill; a sentinel here, to see that they are untouched)."""
+    lengths = np.array([1, 77, 128, 5, 300, 2], np.int32)
+    s = 300
+    rng = np.random.default_rng(12)
+    n = int(lengths.sum())
+    packed = torch.from_numpy(rng.standard_normal((n,) + row).astype(np.float32)).to(dtype)
+    packed = packed.to(DEV)
+    _, cu, _ = pe.pe_pack_sequences(torch.from_numpy(lengths).to(DEV), s)
+    want = pe.pe_scatter_padded(packed, cu, s).cpu()
+    host = torch.full((len(lengths), s) + row, 7.0, dtype=dtype)
+    if pinned:
+        host = host.pin_memory()
+    pe.pe_download_padded(packed, lengths, out_host=host)
+    torch.cuda.synchronize()
+    real = torch.from_numpy(np.arange(s)[None, :] < lengths[:, None])
+    assert torch.equal(host[real], want[real])
+    assert bool((host[~real] == 7.0).all())
+
+
+def test_download_rejects_bad_lengths():
+    """Lengths outside [1, max_seq_len] are refused before any copy (the packed
+    buffer holds sum(L) rows, so the binding's own size check passes)."""
+    host = torch.zeros((2, 4, 8), dtype=torch.float32).pin_memory()
+    with pytest.raises(pe.PackedAttentionError):
+        pe.pe_download_padded(torch.zeros((9, 8), device=DEV), [5, 4], out_host=host)  # 5 > 4
+    with pytest.raises(pe.PackedAttentionError):
+        pe.pe_download_padded(torch.zeros((4, 8), device=DEV), [0, 4], out_host=host)
