@@ -358,10 +358,12 @@ const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_f
  * device-wide synchronisation.
  *
  * Same arguments and results as pe_packed_attention_fwd without the
- * workspace. The scratch (status word and tile plan) lives in a 512 KiB
- * device array inside the library that every GPU loading it holds until the
- * process exits; num_sequences may be at most 65536, larger batches return
- * PE_ERR_WORKSPACE before anything runs. The call allocates nothing.
+ * workspace. The scratch (status word and tile plan, and a first-token
+ * forward's partial softmax states when they fit; otherwise that forward runs
+ * one CTA per sequence and head) lives in a 512 KiB device array inside the
+ * library that every GPU loading it holds until the process exits;
+ * num_sequences may be at most 65536, larger batches return PE_ERR_WORKSPACE
+ * before anything runs. The call allocates nothing.
  * The first call on a device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.
  * All calls on a device share the array and it keeps the last call's

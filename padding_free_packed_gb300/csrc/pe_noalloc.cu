@@ -5,8 +5,11 @@
 // API (a serving process or a framework plugin), or a latency-critical loop
 // where a cudaMalloc/cudaFree pair would add implicit device-wide
 // synchronisation. For them this entry point keeps the forward's scratch (the
-// device status word and the longest-first tile plan) in a file-scope device
-// array that every GPU loading the library holds until the process exits.
+// device status word and the longest-first tile plan, plus a first-token
+// forward's partial softmax states when they fit) in a file-scope device
+// array that every GPU loading the library holds until the process exits. A
+// first-token call whose partial states do not fit runs the same forward
+// without them (one CTA per sequence and head).
 //
 // Set-up: the first call on a device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress and caches it; make that
