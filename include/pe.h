@@ -9,13 +9,21 @@
  *
  * Conventions shared by every call:
  *   - Every buffer argument is DEVICE memory owned by the caller, except the
- *     host out-parameter of pe_pack_sequences and pe_read_device_status.
- *     The library allocates nothing and keeps no state between calls.
+ *     host out-parameters and the host grids of pe_upload_packed and
+ *     pe_download_padded. The library allocates nothing; between calls it
+ *     keeps only per-device attribute caches, the process-wide wait limit
+ *     (pe_set_wait_limit_ns) and the allocation-free forward's static array.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
- *     stream), except pe_pack_sequences, which performs the one host read of
- *     the token count, and pe_read_device_status.
+ *     stream), except pe_pack_sequences, pe_pack_document_ids and
+ *     pe_flatten_packed_metadata, which perform one host read each, and the
+ *     status readers.
  *   - Arguments are checked on the host before anything is launched; a
- *     failed check returns a status and launches nothing.
+ *     failed check returns a status and launches nothing. The return value of
+ *     an asynchronous call can only carry what the host checks: what the
+ *     attention kernels find later (a cu_seqlens that fails the device-side
+ *     layout check, a pipeline wait that gave up) is recorded in the status
+ *     word at the head of the call's workspace, which pe_read_device_status
+ *     reads back (pe_read_noalloc_status for the allocation-free forward).
  *   - Rows are row-major and tightly packed. bf16 is IEEE bfloat16; fp32 is
  *     IEEE binary32. Accumulation is always fp32.
  *   - Kernels run on the current CUDA device, which must be compute
@@ -42,7 +50,8 @@ typedef enum pe_status {
   PE_ERR_UNSUPPORTED = 4,    /* head_dim, dtype, alignment or device not supported */
   PE_ERR_WORKSPACE = 5,      /* workspace null or smaller than *_workspace_size     */
   PE_ERR_CUDA = 6,           /* a CUDA runtime call failed                         */
-  PE_ERR_DEVICE_TIMEOUT = 7  /* a kernel gave up waiting on its own pipeline        */
+  PE_ERR_DEVICE_TIMEOUT = 7  /* a kernel gave up waiting on its own pipeline
+                                (device status word only, never a return value) */
 } pe_status;
 
 typedef enum pe_dtype { PE_BF16 = 0, PE_FP32 = 1 } pe_dtype;
@@ -54,7 +63,9 @@ const char* pe_status_string(int status);
  * 2 added pe_packed_attention_fwd_local, pe_packed_attention_bwd_local,
  * pe_rows_workspace_size, pe_pack_document_ids, pe_flatten_packed_metadata,
  * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu, pe_upload_packed;
- * later additions within 2: pe_download_padded). */
+ * later additions within 2: pe_download_padded; 3 added the device-side
+ * layout check of the attention calls, pe_set_wait_limit_ns and
+ * pe_read_noalloc_status). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------
@@ -218,15 +229,25 @@ pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t
  *   equals row cu_seqlens[i] of the full-mode output.
  * k, v: [num_tokens, H, D]. dtype applies to q, k, v and out.
  * lse: fp32 [H, Nq] (Nq = num_tokens or num_sequences), or NULL to skip it.
- * cu_seqlens: int32 [num_sequences + 1], device, trusted output of
- *   pe_pack_sequences (lengths >= 1 and <= max_seq_len).
+ * cu_seqlens: int32 [num_sequences + 1], device, normally the output of
+ *   pe_pack_sequences. Before any kernel reads q, k or v through it, the call
+ *   checks it on the device: cu_seqlens[0] = 0, cu_seqlens[num_sequences] =
+ *   num_tokens and 1 <= cu_seqlens[i+1] - cu_seqlens[i] <= max_seq_len (every
+ *   sequence non-empty, so no packed layout can make one sequence attend
+ *   across another's tokens or past the buffers; page
+ *   "nemo_automodel.components.models.common.packing" fails such layouts
+ *   loudly too). A layout that fails records PE_ERR_BAD_LENGTH (a length out
+ *   of range) or PE_ERR_INVALID_ARG (a wrong first or last entry) in the
+ *   workspace status word, and the call then computes nothing: out and lse
+ *   are left as they were. Only the num_sequences + 1 entries are read.
  * scale: finite and > 0 (1/sqrt(D) is the pages' default).
  * head_dim: a multiple of 8 (the module docstring's "Constraints" require
  *   it for the aligned kernels), at most 128; bf16 with head_dim 64 runs on the
  *   tcgen05 tensor cores.
  * All tensor pointers 16-byte aligned.
  * workspace: device, >= pe_attention_workspace_size(...) bytes. Its first 4
- *   bytes receive a device-side status (PE_OK or PE_ERR_DEVICE_TIMEOUT),
+ *   bytes receive a device-side status (PE_OK, PE_ERR_BAD_LENGTH or
+ *   PE_ERR_INVALID_ARG from the layout check, or PE_ERR_DEVICE_TIMEOUT),
  *   readable with pe_read_device_status after the call. In first-token mode
  *   the reported size includes room for partial softmax states, so that long
  *   sequences can be spread over several CTAs: when a token row
@@ -369,6 +390,10 @@ const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_f
  * All calls on a device share the array and it keeps the last call's
  * contents (the call clears what must start at zero itself): calls whose
  * executions overlap on the GPU race and must be serialised by the caller.
+ * The array's address is cached per device for the life of the process; the
+ * cache does not survive cudaDeviceReset (call nothing here after one).
+ * The device-side status of the last call (the layout check and the bounded
+ * pipeline waits) sits in the array too: pe_read_noalloc_status reads it.
  * ------------------------------------------------------------------------ */
 pe_status pe_packed_attention_fwd_noalloc(pe_dtype dtype, int32_t num_sequences,
                                           int64_t num_tokens, int32_t num_heads, int32_t head_dim,
@@ -378,9 +403,27 @@ pe_status pe_packed_attention_fwd_noalloc(pe_dtype dtype, int32_t num_sequences,
                                           pe_stream_t stream);
 
 /* Synchronizes `stream` and returns the device-side status that the last
- * attention call on `workspace` left in its first 4 bytes (PE_OK when every
- * pipeline wait completed). */
+ * attention call on `workspace` left in its first 4 bytes (PE_OK when the
+ * layout passed its check and every pipeline wait completed). */
 pe_status pe_read_device_status(const void* workspace, pe_stream_t stream);
+
+/* The same for pe_packed_attention_fwd_noalloc: synchronizes `stream` and
+ * returns the device-side status of the last allocation-free call on the
+ * current device (copied from the library's static array into host stack
+ * memory; nothing is allocated). PE_ERR_CUDA if the array's address cannot be
+ * looked up. */
+pe_status pe_read_noalloc_status(pe_stream_t stream);
+
+/* Sets the time limit of every bounded pipeline wait in the kernels launched
+ * after this call, in nanoseconds, for the whole process; 0 restores the
+ * default of 2 s. Returns the previous limit. A wait that exceeds the limit
+ * makes its kernel record PE_ERR_DEVICE_TIMEOUT in the status word, finish
+ * the copies and tensor-core operations it has in flight (each such drain
+ * wait is bounded by 2 s whatever this limit), free its tensor memory and
+ * exit, leaving the call's outputs incomplete; the context stays usable. A
+ * diagnostic control: a limit far below a kernel's normal waits turns a valid
+ * call into a reported timeout, which is how the timeout path is tested. */
+uint64_t pe_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -23,8 +23,11 @@ from .binding import (  # noqa: F401
     pe_packed_attention_bwd_local,
     pe_packed_attention_fwd,
     pe_packed_attention_fwd_local,
+    pe_packed_attention_fwd_noalloc,
     pe_read_device_status,
+    pe_read_noalloc_status,
     pe_rope_packed,
     pe_scatter_padded,
+    pe_set_wait_limit_ns,
     pe_upload_packed,
 )

@@ -28,7 +28,8 @@ EXPORTED = (
     "pe_packed_attention_bwd_local", "pe_read_device_status", "pe_attention_kernel",
     "pe_rows_workspace_size", "pe_pack_document_ids", "pe_flatten_packed_metadata",
     "pe_packed_positions", "pe_rope_packed", "pe_layernorm", "pe_geglu", "pe_upload_packed",
-    "pe_download_padded",
+    "pe_download_padded", "pe_packed_attention_fwd_noalloc", "pe_read_noalloc_status",
+    "pe_set_wait_limit_ns",
 )
 
 _lib = None
@@ -105,6 +106,13 @@ def load_library(path: str = LIB_PATH):
     lib.pe_attention_kernel.restype = c.c_char_p
     lib.pe_read_device_status.argtypes = [vp, vp]
     lib.pe_read_device_status.restype = c.c_int
+    lib.pe_read_noalloc_status.argtypes = [vp]
+    lib.pe_read_noalloc_status.restype = c.c_int
+    lib.pe_set_wait_limit_ns.argtypes = [c.c_uint64]
+    lib.pe_set_wait_limit_ns.restype = c.c_uint64
+    lib.pe_packed_attention_fwd_noalloc.argtypes = [c.c_int, i32, i64, i32, i32, i32, vp, vp, vp,
+                                                    vp, c.c_float, c.c_int, vp, vp, vp]
+    lib.pe_packed_attention_fwd_noalloc.restype = c.c_int
     _lib = lib
     return lib
 
@@ -235,8 +243,13 @@ def pe_upload_packed(padded_host: torch.Tensor, lengths_host, out: torch.Tensor)
     b, s = int(padded_host.shape[0]), int(padded_host.shape[1])
     if lengths.shape != (b,):
         raise ValueError("one length per grid row")
-    out = _cuda(out, "out")
     row_bytes = padded_host.element_size() * math.prod(tuple(padded_host.shape[2:]))
+    # Checked before anything is enqueued: every copy writes L_i rows into out.
+    if out.dtype != padded_host.dtype or not out.is_contiguous() or out.numel() != int(
+            lengths.sum()) * (row_bytes // padded_host.element_size()):
+        raise ValueError("out must be contiguous and hold sum(L) rows of the grid's row shape "
+                         "and dtype")
+    out = _cuda(out, "out")
     _check("pe_upload_packed",
            lib.pe_upload_packed(_ptr(padded_host), lengths.ctypes.data, b, s, row_bytes,
                                 _ptr(out), _stream(out.device)))
@@ -256,11 +269,12 @@ def pe_download_padded(packed: torch.Tensor, lengths_host, out_host: torch.Tenso
     b, s = int(out_host.shape[0]), int(out_host.shape[1])
     if lengths.shape != (b,):
         raise ValueError("one length per grid row")
-    packed = _cuda(packed, "packed")
     row_bytes = out_host.element_size() * math.prod(tuple(out_host.shape[2:]))
-    if packed.dtype != out_host.dtype or packed.numel() != int(lengths.sum()) * (
-            row_bytes // out_host.element_size()):
-        raise ValueError("packed must hold sum(L) rows of the grid's row shape and dtype")
+    if packed.dtype != out_host.dtype or not packed.is_contiguous() or packed.numel() != int(
+            lengths.sum()) * (row_bytes // out_host.element_size()):
+        raise ValueError("packed must be contiguous and hold sum(L) rows of the grid's row "
+                         "shape and dtype")
+    packed = _cuda(packed, "packed")
     _check("pe_download_padded",
            lib.pe_download_padded(_ptr(packed), lengths.ctypes.data, b, s, row_bytes,
                                   _ptr(out_host), _stream(packed.device)))
@@ -396,9 +410,49 @@ def pe_attention_kernel(dtype: torch.dtype, head_dim: int, query_is_first_token:
 
 
 def pe_read_device_status(workspace: torch.Tensor) -> int:
-    """Device-side status left in an attention workspace (0 = every wait completed)."""
+    """Device-side status left in an attention workspace (0 = the layout passed
+    its check and every pipeline wait completed)."""
     lib = load_library()
     return int(lib.pe_read_device_status(_ptr(workspace), _stream(workspace.device)))
+
+
+def pe_set_wait_limit_ns(ns: int) -> int:
+    """Process-wide limit of the kernels' bounded pipeline waits (0 = the
+    default 2 s); returns the previous limit."""
+    return int(load_library().pe_set_wait_limit_ns(int(ns)))
+
+
+def pe_packed_attention_fwd_noalloc(q, k, v, cu_seqlens, max_seq_len: int,
+                                    scale: float | None = None,
+                                    query_is_first_token: bool = False, need_lse: bool = False,
+                                    out=None, lse=None):
+    """The forward without a workspace: the library's static device array holds
+    its scratch. Returns (out, lse or None)."""
+    lib = load_library()
+    q, k, v = _cuda(q, "q"), _cuda(k, "k"), _cuda(v, "v")
+    cu_seqlens = _cuda(cu_seqlens, "cu_seqlens")
+    n, h, d = k.shape
+    b = int(cu_seqlens.numel()) - 1
+    nq = b if query_is_first_token else n
+    if tuple(q.shape) != (nq, h, d) or v.shape != k.shape or q.dtype != k.dtype:
+        raise ValueError(f"shape/dtype mismatch: q {tuple(q.shape)} k {tuple(k.shape)}")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if need_lse and lse is None:
+        lse = torch.empty((h, nq), dtype=torch.float32, device=q.device)
+    _check("pe_packed_attention_fwd_noalloc",
+           lib.pe_packed_attention_fwd_noalloc(
+               _dtype_code(q.dtype), b, n, h, d, int(max_seq_len), _ptr(q), _ptr(k), _ptr(v),
+               _ptr(cu_seqlens), scale, int(bool(query_is_first_token)), _ptr(out), _ptr(lse),
+               _stream(q.device)))
+    return out, lse
+
+
+def pe_read_noalloc_status(device=None) -> int:
+    """Device-side status of the last allocation-free forward on the device."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    return int(load_library().pe_read_noalloc_status(_stream(dev)))
 
 
 # --------------------------------------------------------------------------- layer tail

@@ -2,9 +2,18 @@
 // dispatch to the kernel families. Every check runs before any launch.
 #include <math.h>
 
+#include <atomic>
+
 #include "pe_kernels.cuh"
 
 namespace pe {
+
+namespace {
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -104,7 +113,7 @@ extern "C" const char* pe_status_string(int status) {
   }
 }
 
-extern "C" int pe_abi_version(void) { return 2; }
+extern "C" int pe_abi_version(void) { return 3; }
 
 extern "C" size_t pe_attention_workspace_size(pe_dtype dtype, int32_t B, int64_t N,
                                               int32_t H, int32_t D, int32_t S,
@@ -136,18 +145,24 @@ extern "C" pe_status pe_packed_attention_fwd_local(
   if (query_is_first_token && !first_token_supported(D)) return PE_ERR_UNSUPPORTED;
   if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
   const Window win = make_window(window_left, window_right, S);
-  PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
-  if (B == 0) return PE_OK;
-  const TilePlan plan = plan_view(workspace, B);
-  // Streaming first-token form (whole token rows, equal token chunks per CTA)
-  // when the row shape allows it and the workspace holds its chunk partials.
-  if (query_is_first_token && first_token_stream_supported(dtype, H, D) &&
-      workspace_bytes >= plan_bytes(B) + first_token_stream_partial_bytes(N, H, D)) {
-    float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
-    return fwd_first_token_stream(dtype, D, q, k, v, cu_seqlens, B, H, N, S, scale, win, out,
-                                  lse, part, static_cast<DeviceStatus*>(workspace), stream);
+  DeviceStatus* status = static_cast<DeviceStatus*>(workspace);
+  const LayoutCheck chk = {S, N, status};
+  if (B == 0) {
+    PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
+    return PE_OK;
   }
+  const TilePlan plan = plan_view(workspace, B);
   if (query_is_first_token) {
+    // No tile plan: the layout check writes the status word (its reset).
+    PE_TRY(launch_layout_check(cu_seqlens, B, chk, stream));
+    // Streaming form (whole token rows, equal token chunks per CTA) when the
+    // row shape allows it and the workspace holds its chunk partials.
+    if (first_token_stream_supported(dtype, H, D) &&
+        workspace_bytes >= plan_bytes(B) + first_token_stream_partial_bytes(N, H, D)) {
+      float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
+      return fwd_first_token_stream(dtype, D, q, k, v, cu_seqlens, B, H, N, S, scale, win, out,
+                                    lse, part, status, stream);
+    }
     // Otherwise one CTA per (sequence, head), split over key chunks when
     // sequences are long on average (more than two chunks) and the workspace
     // has room for those chunk partials.
@@ -157,16 +172,16 @@ extern "C" pe_status pe_packed_attention_fwd_local(
         workspace_bytes >= plan_bytes(B) + part_bytes)
       part = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
     return fwd_first_token(dtype, D, q, k, v, cu_seqlens, B, H, S, scale, win, out, lse, part,
-                           plan, stream);
+                           status, stream);
   }
+  PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (dtype == PE_BF16 && D == 64) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(),
                             sm103_fwd_pair_heads_rows(win), sm103_fwd_quad_heads_rows(win), plan,
-                            nullptr, stream));
-    return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan,
-                     static_cast<DeviceStatus*>(workspace), stream);
+                            chk, stream));
+    return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan, status, stream);
   }
-  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_item(), 0, 0, plan, nullptr, stream));
+  PE_TRY(launch_tile_plan(cu_seqlens, B, H, simt_rows_per_item(), 0, 0, plan, chk, stream));
   return fwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, scale, win, out, lse, N, plan, stream);
 }
 
@@ -207,14 +222,16 @@ extern "C" pe_status pe_packed_attention_bwd_local(
   PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (B == 0) return PE_OK;
   TilePlan plan = plan_view(workspace, B);
+  DeviceStatus* status = static_cast<DeviceStatus*>(workspace);
+  const LayoutCheck chk = {S, N, status};
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
   if (dtype == PE_BF16 && D == 64 && !query_is_first_token) {
     PE_TRY(bwd_preprocess(dtype, D, out, dout, N, H, delta, stream));
     return bwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, lse, dout, delta, dq, dk, dv,
-                     plan, static_cast<DeviceStatus*>(workspace), stream);
+                     plan, chk, stream);
   }
   return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, win, out,
-                  lse, dout, dq, dk, dv, delta, plan, stream);
+                  lse, dout, dq, dk, dv, delta, plan, chk, stream);
 }
 
 extern "C" pe_status pe_packed_attention_bwd(pe_dtype dtype, int32_t B, int64_t N, int32_t H,
@@ -239,6 +256,10 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
   if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
   if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64";
   return "simt_ffma";
+}
+
+extern "C" uint64_t pe_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitLimitNs : ns);
 }
 
 extern "C" pe_status pe_read_device_status(const void* workspace, pe_stream_t stream_) {

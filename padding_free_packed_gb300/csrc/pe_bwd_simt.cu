@@ -102,7 +102,7 @@ pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
                    const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,
                    int first_token, Window win, const void* out, const float* lse,
                    const void* dout, void* dq, void* dk, void* dv, float* delta, TilePlan plan,
-                   cudaStream_t stream) {
+                   LayoutCheck check, cudaStream_t stream) {
   BwdArgs a;
   a.q = q; a.k = k; a.v = v; a.dout = dout;
   a.lse = lse; a.delta = delta;
@@ -112,6 +112,7 @@ pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
   a.first_token = first_token;
   a.win = win;
   a.plan = plan;
+  a.check = check;
   // Delta.
   int64_t blocks = ceil_div(Nq * H, 8);
   const int64_t cap = (int64_t)device_sm_count() * 8;

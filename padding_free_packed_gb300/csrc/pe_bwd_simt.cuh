@@ -122,6 +122,7 @@ struct BwdArgs {
   int first_token;
   Window win;
   TilePlan plan;
+  LayoutCheck check;  // for the tile plans (host side only)
 };
 
 // Visibility of key position kp from the query at position rp (local attention).
@@ -351,7 +352,7 @@ pe_status launch_passes(const BwdArgs& a, TilePlan plan, int32_t B, cudaStream_t
     int per_sm = 0;
     PE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem));
     if (per_sm < 1) return PE_ERR_UNSUPPORTED;
-    PE_TRY(launch_tile_plan(a.cu, B, a.H, kB, 0, 0, plan, nullptr, stream));
+    PE_TRY(launch_tile_plan(a.cu, B, a.H, kB, 0, 0, plan, a.check, stream));
     kernel<<<device_sm_count() * per_sm, kThreads, smem, stream>>>(a);
     PE_CUDA_TRY(cudaGetLastError());
   }
@@ -362,7 +363,7 @@ pe_status launch_passes(const BwdArgs& a, TilePlan plan, int32_t B, cudaStream_t
     int per_sm = 0;
     PE_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem));
     if (per_sm < 1) return PE_ERR_UNSUPPORTED;
-    PE_TRY(launch_tile_plan(a.cu, B, a.H, a.first_token ? 0x7fffffff : kB, 0, 0, plan, nullptr,
+    PE_TRY(launch_tile_plan(a.cu, B, a.H, a.first_token ? 0x7fffffff : kB, 0, 0, plan, a.check,
                             stream));
     kernel<<<device_sm_count() * per_sm, kThreads, smem, stream>>>(a);
     PE_CUDA_TRY(cudaGetLastError());

@@ -87,7 +87,7 @@ struct alignas(1024) Smem {
   uint64_t drain[4];
   Item items[2];
   uint32_t tmem_base;
-  int abort_flag;
+  WaitGuard guard;
 };
 
 struct BwdParams {
@@ -103,6 +103,7 @@ struct BwdParams {
   TilePlan plan;
   Window win;
   DeviceStatus* status;
+  uint64_t wait_limit_ns;   // bounded-wait limit of this launch
 };
 
 // The nblk streaming blocks of 128 rows of the item block `blk` of a sequence
@@ -143,7 +144,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const uint32_t raw_addr = smem_u32(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* abort_flag = &S.abort_flag;
+  volatile WaitGuard* abort_flag = &S.guard;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -163,7 +164,8 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     mbar_init(smem_u32(&S.o_full), kAccWarps);
     mbar_init(smem_u32(&S.o_free), 8);
     for (int w = 0; w < 4; ++w) mbar_init(smem_u32(&S.drain[w]), 1);
-    S.abort_flag = 0;
+    S.guard.abort = 0;
+    S.guard.limit_ns = p.wait_limit_ns;
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -639,7 +641,8 @@ pe_status make_map_bwd(CUtensorMap* map, const void* base, int64_t N, int32_t H,
 }
 
 template <bool kKeyPass>
-pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, cudaStream_t stream) {
+pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, LayoutCheck check,
+                      cudaStream_t stream) {
   auto kernel = prm.win.active() ? bwd_sm103_kernel<kKeyPass, true>
                                  : bwd_sm103_kernel<kKeyPass, false>;
   const size_t smem = sizeof(Smem) + 1024;
@@ -652,7 +655,7 @@ pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, cudaStrea
   if (static_cast<uint32_t>(attr.numRegs) * kThreads < 2u * 128u * (kRegsLow + kRegsHigh))
     return PE_ERR_UNSUPPORTED;
   PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, prm.pair_heads_rows, 0, prm.plan,
-                          nullptr, stream));
+                          check, stream));
   kernel<<<device_sm_count(), kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6],
                                                         m[7], prm);
   PE_CUDA_TRY(cudaGetLastError());
@@ -665,7 +668,7 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     int32_t H, int64_t N, float scale, Window win, const float* lse,
                     const void* dout,
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
-                    DeviceStatus* status, cudaStream_t stream) {
+                    LayoutCheck check, cudaStream_t stream) {
   PE_TRY(get_encoder_bwd());
   // q, k, v, dO with 128-row boxes, then with 64-row boxes (two-head items).
   CUtensorMap maps[8];
@@ -683,13 +686,14 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.lse = lse;
   prm.delta = delta;
   prm.plan = plan;
-  prm.status = status;
+  prm.status = check.status;
+  prm.wait_limit_ns = wait_limit_ns();
   prm.out1 = static_cast<__nv_bfloat16*>(dk);
   prm.out2 = static_cast<__nv_bfloat16*>(dv);
-  PE_TRY(launch_pass<true>(maps, prm, stream));
+  PE_TRY(launch_pass<true>(maps, prm, check, stream));
   prm.out1 = static_cast<__nv_bfloat16*>(dq);
   prm.out2 = nullptr;
-  return launch_pass<false>(maps, prm, stream);
+  return launch_pass<false>(maps, prm, check, stream);
 }
 
 }  // namespace pe

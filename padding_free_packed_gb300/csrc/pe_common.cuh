@@ -53,7 +53,8 @@ __device__ __forceinline__ float ex2(float x) {
 // Device-side status word at the head of every attention workspace.
 struct DeviceStatus {
   int32_t code;       // pe_status
-  int32_t detail;     // where the wait gave up (role id), for diagnostics
+  int32_t detail;     // diagnostics: where a wait gave up (role id), or the
+                      // first sequence of a layout that failed its check
   int32_t pad[2];
 };
 
@@ -138,14 +139,40 @@ __device__ __forceinline__ void plan_decode(const int32_t* __restrict__ order,
   local = t - (lo > 0 ? __ldg(tile_end + lo - 1) : 0);
 }
 
+// What a caller's cu_seqlens must satisfy before any kernel reads through it:
+// cu[0] = 0, cu[B] = N and 1 <= cu[i+1] - cu[i] <= S for every i (so every
+// entry lies in [0, N] and every sequence is non-empty). A violation is
+// recorded in `status` (PE_ERR_BAD_LENGTH for a length, PE_ERR_INVALID_ARG for
+// an end; detail = the first offending sequence, or -1 for an end) and no
+// attention kernel of the call reads q, k or v.
+struct LayoutCheck {
+  int32_t max_seq_len;
+  int64_t num_tokens;
+  DeviceStatus* status;
+};
+
 // Launches the plan kernel: tiles of sequence i = heads * ceil(L_i / rows_per_tile),
 // or ceil(heads / 4) when L_i <= quad_heads_rows and ceil(heads / 2) when
 // L_i <= pair_heads_rows (kernels that run four or two heads of such a sequence
-// in one work item; 0 turns either off).
+// in one work item; 0 turns either off). The kernel first checks the layout
+// (LayoutCheck); when the check fails, or when the status word already holds an
+// error (an earlier pass of the same call), the plan has no tiles, so the
+// persistent kernels that consume it claim no work.
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
                            int32_t rows_per_tile, int32_t pair_heads_rows,
-                           int32_t quad_heads_rows, TilePlan plan, DeviceStatus* status,
+                           int32_t quad_heads_rows, TilePlan plan, LayoutCheck check,
                            cudaStream_t stream);
+
+// The same check for calls without a tile plan (first-token queries): writes
+// the whole status word (code 0 when the layout is valid), so it also serves as
+// the call's reset of that word. Kernels launched after it read the code at
+// entry and return when it is not PE_OK.
+pe_status launch_layout_check(const int32_t* cu_seqlens, int32_t B, LayoutCheck check,
+                              cudaStream_t stream);
+
+// Limit of every bounded pipeline wait in the kernels launched from now on
+// (pe_set_wait_limit_ns; 2 s by default).
+uint64_t wait_limit_ns();
 
 // First-token queries split each sequence's keys into chunks of this many keys
 // (one CTA each) when sequences are long (see the forward entry point); chunk

@@ -97,6 +97,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kStThreads) : "memory");
 }
+// The same barrier (another id) that also returns the OR of `x` over the
+// consumer threads, so that they all take the same branch after it.
+__device__ __forceinline__ bool consumers_sync_or(bool x) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 2, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(x ? 1u : 0u), "n"(kStThreads)
+      : "memory");
+  return r != 0;
+}
 
 // Largest i in [0, B) with cu[i] <= t (cu[0] = 0 <= t), found by the whole
 // warp: each round probes 32 evenly spaced entries and keeps the interval the
@@ -147,7 +159,7 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
                           const T* __restrict__ v, const int32_t* __restrict__ cu, int32_t B,
                           int64_t N, int32_t chunk, float scale_log2, int32_t key_limit,
                           T* __restrict__ out, float* __restrict__ lse, float* __restrict__ part,
-                          DeviceStatus* status) {
+                          DeviceStatus* status, uint64_t wait_limit_ns) {
   using Sh = StShape<T, D, VPL>;
   constexpr int EPV = Sh::kEPV, LPH = Sh::kLPH, ROW = Sh::kRow, H = Sh::kH, R = Sh::kRows;
   extern __shared__ __align__(128) unsigned char st_smem[];
@@ -157,7 +169,8 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
   float* s_m = s_o + kStWarps * ROW;                           // [warps][H]
   float* s_l = s_m + kStWarps * H;                             // [warps][H]
   __shared__ __align__(8) uint64_t full[kStStages], empty[kStStages];
-  __shared__ volatile int abort_flag;
+  __shared__ WaitGuard guard;
+  __shared__ int32_t entry_code;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t c0 = (int64_t)blockIdx.x * chunk;
   const int64_t c1 = min(N, c0 + chunk);
@@ -166,10 +179,15 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), kStWarps);
     }
-    abort_flag = 0;
+    guard.abort = 0;
+    guard.limit_ns = wait_limit_ns;
+    // Read once for the whole CTA: other CTAs may record a timeout meanwhile.
+    entry_code = *reinterpret_cast<volatile int32_t*>(&status->code);
     fence_mbarrier_init();
   }
   __syncthreads();
+  if (entry_code != PE_OK) return;  // the layout failed its check: read nothing
+  volatile WaitGuard* abort_flag = &guard;
   const int32_t first = find_sequence(cu, B, (int32_t)c0, lane);
 
   if (warp == kStWarps) {
@@ -182,7 +200,7 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
       const Segment sg = segment_of(cu, i, a, c1, key_limit);
       for (int64_t r0 = sg.a; r0 < sg.vis_end; r0 += R, ++g) {
         const int s = g % kStStages;
-        if (!mbar_wait(smem_u32(&empty[s]), ((g / kStStages) & 1) ^ 1, &abort_flag, status,
+        if (!mbar_wait(smem_u32(&empty[s]), ((g / kStStages) & 1) ^ 1, abort_flag, status,
                        kSiteStProducer)) {
           ok = false;
           break;
@@ -204,6 +222,10 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
   }
 
   // -------------------------------------------------------------- consumers
+  // A wait that gives up ends this warp's stage loop; the consumers then meet
+  // at the merge barrier, which tells all of them whether any gave up, and
+  // leave together without writing anything (so no warp is left waiting at a
+  // barrier that a departed warp would never reach).
   uint32_t g = 0;  // stages consumed
   int32_t i = first;
   for (int64_t a = c0; a < c1; ++i) {
@@ -217,6 +239,7 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
 #pragma unroll
       for (int e = 0; e < EPV; ++e) qv[u][e] *= scale_log2;
     }
+    bool failed = false;
     float m[VPL], l[VPL], o[VPL][EPV];
 #pragma unroll
     for (int u = 0; u < VPL; ++u) {
@@ -227,11 +250,12 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
     }
     for (int64_t r0 = sg.a; r0 < sg.vis_end; r0 += R, ++g) {
       const int s = g % kStStages;
-      // Every consumer warp waits for and releases every stage, so all of them
-      // pass or all of them give up at the same stage.
-      if (!warp_wait(smem_u32(&full[s]), (g / kStStages) & 1, &abort_flag, status,
-                     kSiteStConsumer))
-        return;
+      // Every consumer warp waits for and releases every stage.
+      if (!warp_wait(smem_u32(&full[s]), (g / kStStages) & 1, abort_flag, status,
+                     kSiteStConsumer)) {
+        failed = true;
+        break;
+      }
       const int nr = (int)min((int64_t)R, sg.vis_end - r0);
       const T* kst = ks + s * Sh::kStageElems;
       const T* vst = vs + s * Sh::kStageElems;
@@ -278,7 +302,7 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
         s_l[warp * H + h] = l[u];
       }
     }
-    consumers_sync();
+    if (consumers_sync_or(failed)) return;
     const int64_t s0 = sg.s0, e1 = sg.e1;
     const bool whole = s0 >= c0 && e1 <= c1;
     const int slot = s0 < c0 ? 0 : 1;
@@ -320,7 +344,10 @@ template <typename T, int D>
 __global__ void first_token_stream_merge_kernel(const float* __restrict__ part,
                                                 const int32_t* __restrict__ cu, int32_t B,
                                                 int32_t H, int32_t chunk, int32_t key_limit,
-                                                T* __restrict__ out, float* __restrict__ lse) {
+                                                T* __restrict__ out, float* __restrict__ lse,
+                                                const DeviceStatus* __restrict__ status) {
+  // An invalid layout or a streaming kernel that gave up: nothing to combine.
+  if (status->code != PE_OK) return;
   constexpr int kU = 16;
   static_assert(D % 32 == 0, "whole columns per lane");
   const int lane = threadIdx.x & 31;
@@ -397,13 +424,14 @@ pe_status launch_stream(const void* q, const void* k, const void* v, const int32
   const int64_t blocks = ceil_div(N, chunk);
   kernel<<<(unsigned)blocks, kStBlock, Sh::kSmem, stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, N,
-      chunk, scale * kLog2e, key_limit, static_cast<T*>(out), lse, part, status);
+      chunk, scale * kLog2e, key_limit, static_cast<T*>(out), lse, part, status,
+      wait_limit_ns());
   PE_CUDA_TRY(cudaGetLastError());
   int64_t mblocks = ceil_div((int64_t)B * H, 8);
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (mblocks > cap) mblocks = cap;
   first_token_stream_merge_kernel<T, D><<<(unsigned)mblocks, 256, 0, stream>>>(
-      part, cu, B, H, chunk, key_limit, static_cast<T*>(out), lse);
+      part, cu, B, H, chunk, key_limit, static_cast<T*>(out), lse, status);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -51,7 +51,11 @@ __global__ void __launch_bounds__(kFtThreads)
 fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                        const int32_t* __restrict__ cu, int32_t B, int32_t H, float scale_log2,
                        int32_t key_limit, T* __restrict__ out, float* __restrict__ lse,
-                       int32_t nsplit, int32_t chunk, float* __restrict__ part) {
+                       int32_t nsplit, int32_t chunk, float* __restrict__ part,
+                       const DeviceStatus* __restrict__ status) {
+  // A layout that failed its check (nothing else writes the word while this
+  // kernel runs, so every thread reads the same code).
+  if (status->code != PE_OK) return;
   using S = FtShape<T, D>;
   constexpr int EPL = S::kEPL, LPK = S::kLPK, G = S::kGroups;
   constexpr int kWarps = kFtThreads / 32;
@@ -159,7 +163,9 @@ fwd_first_token_kernel(const T* __restrict__ q, const T* __restrict__ k, const T
 template <typename T, int D>
 __global__ void first_token_merge_kernel(const float* __restrict__ part, int32_t B, int32_t H,
                                          int32_t nsplit, T* __restrict__ out,
-                                         float* __restrict__ lse) {
+                                         float* __restrict__ lse,
+                                         const DeviceStatus* __restrict__ status) {
+  if (status->code != PE_OK) return;
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t ih = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -188,7 +194,7 @@ __global__ void first_token_merge_kernel(const float* __restrict__ part, int32_t
 template <typename T, int D>
 pe_status launch_first(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                        int32_t H, int32_t S, float scale, Window win, void* out, float* lse,
-                       float* part, cudaStream_t stream) {
+                       float* part, const DeviceStatus* status, cudaStream_t stream) {
   // With a window the query sees at most right + 1 keys.
   const int32_t key_limit = win.right == kUnbounded ? S : min(S, win.right + 1);
   // Without room for chunk partials every sequence is a single chunk.
@@ -199,13 +205,13 @@ pe_status launch_first(const void* q, const void* k, const void* v, const int32_
   fwd_first_token_kernel<T, D><<<(unsigned)blocks, kFtThreads, 0, stream>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, H,
       scale * kLog2e, key_limit, static_cast<T*>(out), lse, nsplit,
-      nsplit == 1 ? key_limit : kFirstTokenChunk, part);
+      nsplit == 1 ? key_limit : kFirstTokenChunk, part, status);
   PE_CUDA_TRY(cudaGetLastError());
   if (nsplit > 1) {
     int64_t mblocks = ceil_div((int64_t)B * H, 8);
     if (mblocks > cap) mblocks = cap;
     first_token_merge_kernel<T, D><<<(unsigned)mblocks, 256, 0, stream>>>(
-        part, B, H, nsplit, static_cast<T*>(out), lse);
+        part, B, H, nsplit, static_cast<T*>(out), lse, status);
     PE_CUDA_TRY(cudaGetLastError());
   }
   return PE_OK;
@@ -214,10 +220,12 @@ pe_status launch_first(const void* q, const void* k, const void* v, const int32_
 template <typename T>
 pe_status dispatch_first(int D, const void* q, const void* k, const void* v, const int32_t* cu,
                          int32_t B, int32_t H, int32_t S, float scale, Window win, void* out,
-                         float* lse, float* part, cudaStream_t stream) {
+                         float* lse, float* part, const DeviceStatus* status,
+                         cudaStream_t stream) {
   switch (D) {
-#define PE_CASE(d) \
-  case d: return launch_first<T, d>(q, k, v, cu, B, H, S, scale, win, out, lse, part, stream);
+#define PE_CASE(d)                                                                            \
+  case d:                                                                                     \
+    return launch_first<T, d>(q, k, v, cu, B, H, S, scale, win, out, lse, part, status, stream);
     PE_CASE(8) PE_CASE(16) PE_CASE(32) PE_CASE(64) PE_CASE(128)
 #undef PE_CASE
     default: return PE_ERR_UNSUPPORTED;
@@ -240,12 +248,13 @@ bool first_token_supported(int D) { return D == 8 || D == 16 || D == 32 || D == 
 
 pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                           const int32_t* cu, int32_t B, int32_t H, int32_t S, float scale,
-                          Window win, void* out, float* lse, float* part, TilePlan /*plan*/,
-                          cudaStream_t stream) {
+                          Window win, void* out, float* lse, float* part,
+                          const DeviceStatus* status, cudaStream_t stream) {
   if (dtype == PE_FP32)
-    return dispatch_first<float>(D, q, k, v, cu, B, H, S, scale, win, out, lse, part, stream);
+    return dispatch_first<float>(D, q, k, v, cu, B, H, S, scale, win, out, lse, part, status,
+                                 stream);
   return dispatch_first<__nv_bfloat16>(D, q, k, v, cu, B, H, S, scale, win, out, lse, part,
-                                       stream);
+                                       status, stream);
 }
 
 }  // namespace pe

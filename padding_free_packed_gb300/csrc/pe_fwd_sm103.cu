@@ -95,7 +95,7 @@ struct alignas(1024) Smem {
   uint64_t drain[kIssueWarps];
   Item items[2];
   uint32_t tmem_base;
-  int abort_flag;
+  WaitGuard guard;
 };
 
 struct FwdParams {
@@ -110,6 +110,7 @@ struct FwdParams {
   TilePlan plan;
   Window win;
   DeviceStatus* status;
+  uint64_t wait_limit_ns;   // bounded-wait limit of this launch
 };
 
 // Where a wait gave up (recorded in the status word's detail field).
@@ -212,7 +213,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const uint32_t raw_addr = smem_u32(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* abort_flag = &S.abort_flag;
+  volatile WaitGuard* abort_flag = &S.guard;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -233,7 +234,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(smem_u32(&S.v_empty[s]), 2);       // each PV issuer, once per block
     }
     for (int w = 0; w < kIssueWarps; ++w) mbar_init(smem_u32(&S.drain[w]), 1);
-    S.abort_flag = 0;
+    S.guard.abort = 0;
+    S.guard.limit_ns = p.wait_limit_ns;
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -723,6 +725,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.plan = plan;
   prm.win = win;
   prm.status = status;
+  prm.wait_limit_ns = wait_limit_ns();
   kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mq64, mk64, mv64, prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;

@@ -14,16 +14,20 @@ pe_status fwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const vo
 // First-token query (one query row per sequence).
 bool first_token_supported(int D);
 // With a window the query at position 0 sees keys 0 .. win.right.
+// Returns at once on the device when `status` holds an error (a layout that
+// failed its check).
 pe_status fwd_first_token(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                           const int32_t* cu, int32_t B, int32_t H, int32_t S, float scale,
-                          Window win, void* out, float* lse, float* part, TilePlan plan,
-                          cudaStream_t stream);
+                          Window win, void* out, float* lse, float* part,
+                          const DeviceStatus* status, cudaStream_t stream);
 
 // First-token query, streaming form: chunks of whole token rows per CTA (all
 // heads); sequences that cross chunk edges leave partial states that a second
 // kernel merges. Needs first_token_stream_partial_bytes() of scratch in
 // `part`; a pipeline wait that gives up records PE_ERR_DEVICE_TIMEOUT in
-// `status`. Returns PE_ERR_UNSUPPORTED for shapes it does not take.
+// `status`, and both kernels return at entry when `status` already holds an
+// error (a layout that failed its check). Returns PE_ERR_UNSUPPORTED for
+// shapes it does not take.
 bool first_token_stream_supported(pe_dtype dtype, int32_t H, int32_t D);
 int32_t first_token_stream_chunk(int64_t N);
 size_t first_token_stream_partial_bytes(int64_t N, int32_t H, int32_t D);
@@ -37,7 +41,7 @@ pe_status fwd_first_token_stream(pe_dtype dtype, int32_t D, const void* q, const
 pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,
                    int first_token, Window win, const void* out, const float* lse, const void* dout,
-                   void* dq, void* dk, void* dv, float* delta, TilePlan plan,
+                   void* dq, void* dk, void* dv, float* delta, TilePlan plan, LayoutCheck check,
                    cudaStream_t stream);
 
 // Tensor-core forward, bf16, head_dim 64 (sm_103a). Work items are pairs of
@@ -62,6 +66,6 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     int32_t H, int64_t N, float scale, Window win, const float* lse,
                     const void* dout,
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
-                    DeviceStatus* status, cudaStream_t stream);
+                    LayoutCheck check, cudaStream_t stream);
 
 }  // namespace pe

@@ -12,7 +12,8 @@
 // without them (one CTA per sequence and head).
 //
 // Set-up: the first call on a device, with that device current, looks up the
-// array's device address with cudaGetSymbolAddress and caches it; make that
+// array's device address with cudaGetSymbolAddress and caches it for the life
+// of the process (the cache does not survive cudaDeviceReset); make that
 // first call before any stream capture. No call allocates memory. The array
 // is shared by every call on a device and keeps the last call's contents; the
 // forward clears the parts that must start at zero (the status word and the
@@ -68,4 +69,13 @@ extern "C" pe_status pe_packed_attention_fwd_noalloc(
   return pe_packed_attention_fwd(dtype, num_sequences, num_tokens, num_heads, head_dim,
                                  max_seq_len, q, k, v, cu_seqlens, scale, query_is_first_token,
                                  out, lse, scratch, kNoAllocScratchBytes, stream);
+}
+
+// The device status word of the last allocation-free call on the current
+// device lives at the head of the array, where the caller cannot address it.
+extern "C" pe_status pe_read_noalloc_status(pe_stream_t stream) {
+  void* scratch = nullptr;
+  pe_status st = scratch_for_current_device(&scratch);
+  if (st != PE_OK) return st;
+  return pe_read_device_status(scratch, stream);
 }

@@ -176,6 +176,43 @@ pe_status launch_scatter(const void* packed, const int32_t* cu, int32_t B, int32
 }
 
 // ---------------------------------------------------------------------------
+// Layout check of a caller's cu_seqlens (one CTA of kScanThreads threads):
+// cu[0] = 0, cu[B] = N, 1 <= cu[i+1] - cu[i] <= S. Reads only cu[0 .. B].
+// Returns PE_OK or the error code, the same in every thread; *detail gets the
+// first sequence whose length is out of range, or -1 for an end.
+// ---------------------------------------------------------------------------
+__device__ int32_t check_layout_cta(const int32_t* __restrict__ cu, int32_t B,
+                                    const LayoutCheck& chk, int32_t* detail) {
+  __shared__ int32_t bad_seq;
+  __shared__ int32_t bad_end;
+  if (threadIdx.x == 0) {
+    bad_seq = 0x7fffffff;
+    bad_end = (__ldg(cu) != 0 || (int64_t)__ldg(cu + B) != chk.num_tokens) ? 1 : 0;
+  }
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < B; i += blockDim.x) {
+    const int64_t len = (int64_t)__ldg(cu + i + 1) - __ldg(cu + i);
+    if (len < 1 || len > chk.max_seq_len) atomicMin(&bad_seq, (int32_t)i);
+  }
+  __syncthreads();
+  const int32_t seq = bad_seq, end = bad_end;
+  __syncthreads();  // the shared flags may be reused by a later call in this CTA
+  *detail = seq != 0x7fffffff ? seq : -1;
+  if (seq != 0x7fffffff) return PE_ERR_BAD_LENGTH;
+  return end ? PE_ERR_INVALID_ARG : PE_OK;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+layout_check_kernel(const int32_t* __restrict__ cu, int32_t B, LayoutCheck chk) {
+  int32_t detail;
+  const int32_t code = check_layout_cta(cu, B, chk, &detail);
+  if (threadIdx.x == 0) {
+    chk.status->code = code;
+    chk.status->detail = code == PE_OK ? 0 : detail;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Tile plan: counting sort of sequences by tile length (longest first), then
 // the inclusive prefix of tiles in that order. One CTA; no host read.
 // ---------------------------------------------------------------------------
@@ -184,10 +221,26 @@ constexpr int kPlanBins = 2048;
 __global__ void __launch_bounds__(kScanThreads)
 tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32_t rows_per_tile,
                  int32_t pair_heads_rows, int32_t quad_heads_rows, TilePlan plan,
-                 DeviceStatus* status) {
+                 LayoutCheck chk) {
   __shared__ int32_t start[kPlanBins];
   __shared__ long long warp_sums[32];
   const int tid = threadIdx.x;
+  // An invalid layout (or an error already recorded by an earlier pass of the
+  // same call) leaves a plan without tiles: nothing below reads through cu.
+  {
+    int32_t detail;
+    const int32_t prior = *reinterpret_cast<volatile int32_t*>(&chk.status->code);
+    const int32_t code = check_layout_cta(cu, B, chk, &detail);
+    if (code != PE_OK || prior != PE_OK) {
+      if (tid == 0) {
+        if (code != PE_OK && atomicCAS(&chk.status->code, (int)PE_OK, code) == PE_OK)
+          chk.status->detail = detail;
+        *plan.total_tiles = 0;
+        *plan.counter = 0;
+      }
+      return;
+    }
+  }
   for (int k = tid; k < kPlanBins; k += kScanThreads) start[k] = 0;
   __syncthreads();
   for (int64_t i = tid; i < B; i += kScanThreads) {
@@ -238,12 +291,20 @@ tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32
 
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
                            int32_t rows_per_tile, int32_t pair_heads_rows,
-                           int32_t quad_heads_rows, TilePlan plan, DeviceStatus* /*status*/,
+                           int32_t quad_heads_rows, TilePlan plan, LayoutCheck check,
                            cudaStream_t stream) {
   static_assert(kPlanBins == 2 * kScanThreads, "plan scan covers two bins per thread");
+  if (!check.status) return PE_ERR_INVALID_ARG;
   tile_plan_kernel<<<1, kScanThreads, 0, stream>>>(cu_seqlens, B, heads, rows_per_tile,
-                                                   pair_heads_rows, quad_heads_rows, plan,
-                                                   nullptr);
+                                                   pair_heads_rows, quad_heads_rows, plan, check);
+  PE_CUDA_TRY(cudaGetLastError());
+  return PE_OK;
+}
+
+pe_status launch_layout_check(const int32_t* cu_seqlens, int32_t B, LayoutCheck check,
+                              cudaStream_t stream) {
+  if (!check.status) return PE_ERR_INVALID_ARG;
+  layout_check_kernel<<<1, kScanThreads, 0, stream>>>(cu_seqlens, B, check);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -11,8 +11,18 @@
 namespace pe {
 namespace sm103 {
 
-// A wait that has not completed after this long marks the launch as failed.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// While draining after an abort, a wait for the CTA's own copies or MMAs gives
+// up after this long (the pipeline waits use the launch's own limit).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
+
+// Per-CTA abort state in shared memory, shared by every bounded wait of the
+// CTA: the flag raised by the first wait that gives up, and the launch's wait
+// limit in nanoseconds (pe_set_wait_limit_ns; 2 s by default).
+struct WaitGuard {
+  int abort;
+  int pad;
+  uint64_t limit_ns;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,22 +67,40 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same phase completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this poll with test_wait: a failed try_wait suspends the thread
+// for a hardware-chosen time that can exceed a short limit many times over.
+constexpr uint64_t kPollBelowNs = 1000000ull;
+
 // Waits for the phase of parity `parity` to complete. Gives up (returns false)
-// when another thread of the CTA has aborted, or after kWaitLimitNs, in which
-// case it raises the CTA's abort flag and records a timeout status.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          DeviceStatus* status, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
+// when another thread of the CTA has aborted, or once the guard's limit has
+// passed, in which case it raises the CTA's abort flag and records a timeout
+// status. Both checks run after every failed attempt (a failed try_wait has
+// already suspended the thread for a while).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile WaitGuard* guard, DeviceStatus* status,
+                                          int where) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const bool poll = guard->limit_ns < kPollBelowNs;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        report_timeout(status, where);
-        return false;
-      }
+  for (;;) {
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (guard->abort) return false;
+    if (globaltimer() - t0 >= guard->limit_ns) {
+      guard->abort = 1;
+      report_timeout(status, where);
+      return false;
     }
   }
 }
@@ -81,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 __device__ __forceinline__ bool mbar_drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (globaltimer() - t0 > kDrainLimitNs) return false;
   return true;
 }
 
@@ -179,9 +207,10 @@ __device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
 
 // A wait taken by all 32 lanes of a warp that succeeds only if it succeeds in
 // every lane, so warp-collective operations after it never run on a partial warp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          DeviceStatus* status, int where) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, status, where);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
+                                          volatile WaitGuard* guard, DeviceStatus* status,
+                                          int where) {
+  const bool ok = mbar_wait(bar, parity, guard, status, where);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.pe_abi_version() == 2
+    assert lib.pe_abi_version() == 3
     for code in range(8):
         assert lib.pe_status_string(code)
     assert lib.pe_status_string(0) == b"ok"
@@ -102,6 +102,36 @@ def test_host_copies_check_lengths_before_any_copy(lib):
         assert fn(16, bad, 2, 4, 0, 16, None) == 1
         assert fn(16, None, 2, 4, 32, 16, None) == 1
         assert fn(16, bad, 0, 4, 32, 16, None) == 0   # nothing to move
+
+
+def test_wait_limit_round_trip(lib):
+    """pe_set_wait_limit_ns returns the previous limit; 0 restores the 2 s default."""
+    first = lib.pe_set_wait_limit_ns(5000)
+    try:
+        assert first == 2_000_000_000
+        assert lib.pe_set_wait_limit_ns(0) == 5000
+        assert lib.pe_set_wait_limit_ns(0) == 2_000_000_000
+    finally:
+        lib.pe_set_wait_limit_ns(0)
+
+
+@pytest.mark.parametrize("call", ["upload", "download"])
+def test_host_copy_bindings_check_the_device_buffer_first(lib, call):
+    """The bindings of the per-sequence host copies refuse a device buffer that
+    does not hold exactly sum(L) rows of the grid's row shape and dtype before
+    any copy is enqueued (the buffers here are host tensors: the size check
+    comes first, so nothing reaches the library)."""
+    import torch
+    from padding_free_packed_gb300 import binding
+    grid = torch.zeros(3, 8, 2, 4)
+    lengths = [8, 1, 5]
+    for wrong in (torch.zeros(13, 2, 4), torch.zeros(15, 2, 4),
+                  torch.zeros(14, 2, 4, dtype=torch.float64), torch.zeros(14, 4, 2).transpose(1, 2)):
+        with pytest.raises(ValueError, match="sum\\(L\\) rows"):
+            if call == "upload":
+                binding.pe_upload_packed(grid, lengths, wrong)
+            else:
+                binding.pe_download_padded(wrong, lengths, grid)
 
 
 def test_no_gpu_means_unsupported(lib):

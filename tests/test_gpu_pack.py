@@ -146,11 +146,12 @@ def test_host_grids_upload_gather_and_scatter(dtype, row):
 
 def test_upload_rejects_bad_lengths():
     grid = torch.zeros((2, 4, 8), dtype=torch.float32).pin_memory()
-    out = torch.empty((9, 8), device=DEV)
+    # (out holds sum(L) rows, so the binding's size check passes and the
+    # library's length check answers.)
     with pytest.raises(pe.PackedAttentionError):
-        pe.pe_upload_packed(grid, [5, 4], out=out)      # 5 > max_seq_len
+        pe.pe_upload_packed(grid, [5, 4], out=torch.empty((9, 8), device=DEV))  # 5 > max_seq_len
     with pytest.raises(pe.PackedAttentionError):
-        pe.pe_upload_packed(grid, [0, 4], out=out)
+        pe.pe_upload_packed(grid, [0, 4], out=torch.empty((4, 8), device=DEV))
 
 
 @pytest.mark.parametrize("dtype,row", [(torch.bfloat16, (4, 64)), (torch.float32, (3, 5))])

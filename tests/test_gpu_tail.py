@@ -80,8 +80,9 @@ def test_layernorm_matches_oracle(dtype, c, with_bias, with_residual):
                           residual=None if r is None else r.to(DEV))
     if with_residual:
         y, h = res
-        assert torch.equal(h.cpu(), x + r)          # the sum as stored, in the I/O dtype
-        ref = oracle.layernorm(h.cpu(), w, b, 1e-5)
+        hx = x + r                                  # the sum as stored, in the I/O dtype
+        assert torch.equal(h.cpu(), hx)
+        ref = oracle.layernorm(hx, w, b, 1e-5)
     else:
         y = res
         ref = oracle.layernorm(x, w, b, 1e-5)

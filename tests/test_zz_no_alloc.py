@@ -6,8 +6,12 @@ loop that cannot afford cudaMalloc's implicit synchronisation): its scratch is
 a fixed device array inside libpe. This test calls it through the C ABI twice
 in a row (so the second call starts from the first call's leftover scratch)
 and compares each result with pe_packed_attention_fwd's, within the parity
-tolerance the other GPU tests use. It lives in its own file, collected last,
-and needs nothing that other tests set up.
+tolerance the other GPU tests use, and reads the device status of each call
+with pe_read_noalloc_status (the status word sits in the library's array,
+where the caller cannot address it). One first-token case is large enough
+that its partial softmax states do not fit in the array, so the call takes
+the documented fallback (one CTA per sequence and head). It lives in its own
+file, collected last, and needs nothing that other tests set up.
 """
 
 import ctypes
@@ -35,13 +39,28 @@ def _noalloc():
     return fn
 
 
-@pytest.mark.parametrize("dtype,d,first_token", [(torch.bfloat16, 64, False),
-                                                 (torch.float32, 64, False),
-                                                 (torch.bfloat16, 64, True)])
-def test_noalloc_matches_regular_forward_on_two_calls(dtype, d, first_token):
+def _status(stream):
+    lib = pe.load_library()
+    lib.pe_read_noalloc_status.argtypes = [ctypes.c_void_p]
+    lib.pe_read_noalloc_status.restype = ctypes.c_int
+    return lib.pe_read_noalloc_status(stream)
+
+
+SHORT = [300, 1, 129, 1000, 64, 257]
+# 24 sequences of ~1k tokens with 16 heads x 64: the streaming first-token
+# kernel's partial states (two per 64-token chunk, 16 x 66 fp32 each) need
+# ~4.4 MiB, more than the 512 KiB array holds.
+LONG = [1024 + 37 * i for i in range(24)]
+
+
+@pytest.mark.parametrize("dtype,d,heads,first_token,lengths",
+                         [(torch.bfloat16, 64, 4, False, SHORT),
+                          (torch.float32, 64, 4, False, SHORT),
+                          (torch.bfloat16, 64, 4, True, SHORT),
+                          (torch.bfloat16, 64, 16, True, LONG)])
+def test_noalloc_matches_regular_forward_on_two_calls(dtype, d, heads, first_token, lengths):
     fn = _noalloc()
-    lengths = [300, 1, 129, 1000, 64, 257]
-    x = workloads.make_custom(lengths, 4, d, dtype, seed=41)
+    x = workloads.make_custom(lengths, heads, d, dtype, seed=41)
     s = max(lengths)
     cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)).to(DEV)
     q, k, v = x.q.to(DEV), x.k.to(DEV), x.v.to(DEV)
@@ -55,9 +74,11 @@ def test_noalloc_matches_regular_forward_on_two_calls(dtype, d, first_token):
     for call in range(2):
         out = torch.full_like(q, float("nan"))
         lse = torch.full_like(ref_lse, float("nan"))
-        rc = fn(code, len(lengths), k.shape[0], 4, d, s, q.data_ptr(), k.data_ptr(), v.data_ptr(),
-                cu.data_ptr(), 0.125, int(first_token), out.data_ptr(), lse.data_ptr(), stream)
+        rc = fn(code, len(lengths), k.shape[0], heads, d, s, q.data_ptr(), k.data_ptr(),
+                v.data_ptr(), cu.data_ptr(), 0.125, int(first_token), out.data_ptr(),
+                lse.data_ptr(), stream)
         assert rc == 0, f"call {call}: status {rc}"
+        assert _status(stream) == 0, f"call {call}: device status"
         torch.cuda.synchronize()
         check(out, ref, tag, f"no-alloc call {call}")
         np.testing.assert_allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=0, atol=1e-4)
