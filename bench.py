@@ -162,7 +162,8 @@ def committed_traffic(kernel_name: str, source_file: str, config: str):
 
 
 KERNEL_SOURCES = {"tcgen05_bf16_d64": "pe_fwd_sm103.cu", "simt_ffma": "pe_fwd_simt.cu",
-                  "first_token_gemv": "pe_first_token.cu"}
+                  "first_token_gemv": "pe_first_token.cu",
+                  "tcgen05_f32_d64": "pe_fwd_sm103_f32.cu"}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -178,6 +179,12 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     pe.load_library()
     wl = workloads.WORKLOADS[args.workload]
+    if args.dtype and args.dtype != wl.dtype:
+        if not args.packed:
+            raise SystemExit("--dtype needs --packed")
+        import dataclasses
+        wl = dataclasses.replace(wl, dtype=args.dtype,
+                                 description=f"{wl.description}, as {args.dtype}")
     # Weak scaling: every rank draws its own batch of the same workload.
     train = wl.backward or args.backward
     rows_layout = args.layout == "rows"
@@ -228,9 +235,19 @@ def run_ours(args, rank, world):
                if args.packed and args.first_token else None)
     stream = torch.cuda.current_stream(dev)
     fwd_events, bwd_events = [], []
+    # One workspace per direction for every call (all attention calls run on
+    # one stream); their status words are read once after the timed region.
+    n_seq = int(len(lengths))
+    ws_fwd = torch.empty(max(16, pe.attention_workspace_bytes(
+        wl.torch_dtype, n_seq, n_tokens, h, d, s, args.first_token, False)),
+        dtype=torch.uint8, device=dev)
+    ws_bwd = torch.empty(max(16, pe.attention_workspace_bytes(
+        wl.torch_dtype, n_seq, n_tokens, h, d, s, False, True)),
+        dtype=torch.uint8, device=dev) if train else None
 
     # Full attention, or local attention with the --window bounds.
     def attention_fwd(*a, **kw):
+        kw["workspace"] = ws_fwd
         if window is None:
             return pe.pe_packed_attention_fwd(*a, **kw)
         q_, k_, v_, cu_, s_, scale_ = a
@@ -239,8 +256,9 @@ def run_ours(args, rank, world):
 
     def attention_bwd(*a):
         if window is None:
-            return pe.pe_packed_attention_bwd(*a)
-        return pe.pe_packed_attention_bwd_local(*a[:8], window[0], window[1], a[8])
+            return pe.pe_packed_attention_bwd(*a, workspace=ws_bwd)
+        return pe.pe_packed_attention_bwd_local(*a[:8], window[0], window[1], a[8],
+                                                workspace=ws_bwd)
 
     def timed(record, events, fn):
         if not record:
@@ -289,7 +307,9 @@ def run_ours(args, rank, world):
     # Padded steps: pack scan+fill, 3 gathers, plan+attention, scatter; training
     # adds the dO gather, the backward (delta, plan, key pass, plan, query pass)
     # and 3 scatters. Packed steps: plan+attention (+ the 5 backward launches).
-    if args.packed:
+    if args.packed and args.first_token:   # layout check, streaming kernel, merge
+        launches_per_step = 3
+    elif args.packed:
         launches_per_step = 2 + (5 if train else 0)
     elif rows_layout:   # mask count, scan, fill, 3 gathers, plan + attention (+ dO gather, backward)
         launches_per_step = 3 + 3 + 2 + ((1 + 5) if train else 0)
@@ -312,6 +332,11 @@ def run_ours(args, rank, world):
         end.record(stream)
         barrier()
     elapsed_ms = start.elapsed_time(end)
+    # What the kernels found (layout check, bounded waits): 0 when every call
+    # of the timed region completed normally.
+    device_status = {"forward": pe.pe_read_device_status(ws_fwd)}
+    if train:
+        device_status["backward"] = pe.pe_read_device_status(ws_bwd)
     fwd_ms = sum(a.elapsed_time(b) for a, b in fwd_events) / len(fwd_events)
     bwd_ms = sum(a.elapsed_time(b) for a, b in bwd_events) / len(bwd_events) if train else 0.0
     if world > 1:
@@ -411,7 +436,12 @@ def run_ours(args, rank, world):
         dom_kernel, dom_flops, dom_ms = bwd_kernel, bwd_flops, bwd_ms
     else:
         dom_kernel, dom_flops, dom_ms = kernel, fwd_flops, fwd_ms
-    if dom_kernel.startswith("tcgen05"):
+    if dom_kernel == "tcgen05_f32_d64":
+        # fp32 operands split into bf16 hi + lo: three bf16 products per fp32
+        # product, so the ceiling for the useful flops is a third of bf16's.
+        bound, peak, unit = "tensor", float(peaks["bf16_tflops"]) / 3.0, "TFLOP/s"
+        peak_note = f"dense bf16 burst / 3 (three bf16 products per fp32 product), {peaks_src}"
+    elif dom_kernel.startswith("tcgen05"):
         bound, peak, unit = "tensor", float(peaks["bf16_tflops"]), "TFLOP/s"
         peak_note = f"dense bf16 burst, {peaks_src}"
     elif dom_kernel == "first_token_gemv":
@@ -440,7 +470,8 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": {"workload": args.workload + (f"[:{args.sequences}]" if args.sequences else ""),
+        "config": {"workload": args.workload + (f"[:{args.sequences}]" if args.sequences else "")
+                   + (f" as {args.dtype}" if args.dtype else ""),
                    "description": wl.description,
                    "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
                    "heads": h, "head_dim": d, "max_seq_len": s,
@@ -475,9 +506,11 @@ def run_ours(args, rank, world):
         "roofline_kernel": dom_kernel,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
-                     "frac_of_sustained": (achieved / float(peaks["bf16_tflops_sustained"])
+                     "frac_of_sustained": (achieved / (float(peaks["bf16_tflops_sustained"]) * peak
+                                                      / float(peaks["bf16_tflops"]))
                                            if bound == "tensor" else None)},
         "gpu_launches": launches_per_step * args.steps,
+        "device_status": device_status,
         "clocks": clocks.summary(),
         "e2e": e2e,
     }
@@ -763,6 +796,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="longdoc_bf16")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--dtype", choices=["bf16", "fp32"], default=None,
+                    help="with --packed: the workload's shapes in another dtype")
     ap.add_argument("--sequences", type=int, default=None,
                     help="keep only the first K sequences of the workload (profiling cases)")
     ap.add_argument("--packed", action="store_true",
@@ -812,6 +847,11 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    # A kernel that reported a problem (a malformed layout, a pipeline wait
+    # that gave up) makes the measurement invalid: fail the run.
+    if any(v != 0 for v in line.get("device_status", {}).values()):
+        raise SystemExit(f"device status {line['device_status']}: the timed calls did not "
+                         "complete normally")
 
 
 if __name__ == "__main__":

@@ -204,7 +204,8 @@ def test_unsupported_arguments_raise():
 
 def test_bf16_d64_runs_on_tensor_cores_and_reports_clean_status():
     assert pe.pe_attention_kernel(torch.bfloat16, 64) == "tcgen05_bf16_d64"
-    assert pe.pe_attention_kernel(torch.float32, 64) == "simt_ffma"
+    assert pe.pe_attention_kernel(torch.float32, 64) == "tcgen05_f32_d64"
+    assert pe.pe_attention_kernel(torch.float32, 32) == "simt_ffma"
     assert pe.pe_attention_kernel(torch.bfloat16, 64, query_is_first_token=True) == \
         "first_token_gemv"
     # Lengths chosen so work items hit every case of the 256-row query pair:
