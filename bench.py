@@ -138,21 +138,32 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- traffic
 
-def committed_traffic(kernel_name: str, source_file: str, config: str):
+def source_sha1(files) -> str:
+    """sha1 of the concatenated kernel sources (the kernel's .cu file and the
+    csrc headers whose code it inlines)."""
+    h = hashlib.sha1()
+    for name in files:
+        path = os.path.join(ROOT, "padding_free_packed_gb300", "csrc", name)
+        if not os.path.exists(path):
+            return ""
+        h.update(open(path, "rb").read())
+    return h.hexdigest()
+
+
+def committed_traffic(kernel_name: str, source_files, config: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its sha1 is recorded in the summary) and for the
-    same workload and mode (`config`, e.g. "longdoc_bf16" or
+    the current kernel sources (their sha1 is recorded in the summary) and for
+    the same workload and mode (`config`, e.g. "longdoc_bf16" or
     "graph_fp32 first-token")."""
     path = os.path.join(ROOT, "profiles", f"{kernel_name}_traffic.txt")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or not source_files:
         return None
     fields = {}
     with open(path) as fh:
         for line in fh:
             key, _, value = line.partition(":")
             fields[key.strip()] = value.strip()
-    src = os.path.join(ROOT, "padding_free_packed_gb300", "csrc", source_file)
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest() if os.path.exists(src) else ""
+    sha = source_sha1(source_files)
     if fields.get("source_sha1") != sha or fields.get("config") != config:
         return None
     try:
@@ -161,9 +172,11 @@ def committed_traffic(kernel_name: str, source_file: str, config: str):
         return None
 
 
-KERNEL_SOURCES = {"tcgen05_bf16_d64": "pe_fwd_sm103.cu", "simt_ffma": "pe_fwd_simt.cu",
-                  "first_token_gemv": "pe_first_token.cu",
-                  "tcgen05_f32_d64": "pe_fwd_sm103_f32.cu"}
+_HEADERS = ["pe_common.cuh", "pe_sm103.cuh"]
+KERNEL_SOURCES = {"tcgen05_bf16_d64": ["pe_fwd_sm103.cu"] + _HEADERS,
+                  "simt_ffma": ["pe_fwd_simt.cu", "pe_fwd_simt.cuh", "pe_common.cuh"],
+                  "first_token_gemv": ["pe_first_token.cu"] + _HEADERS,
+                  "tcgen05_f32_d64": ["pe_fwd_sm103_f32.cu"] + _HEADERS}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -464,7 +477,7 @@ def run_ours(args, rank, world):
                       + (f" window {window[0]} {window[1]}" if window else "")
                       + (" backward" if train and dom_kernel == bwd_kernel else "")
                       + (f" seed {args.seed + rank}" if args.seed + rank else ""))
-    traffic = committed_traffic(dom_kernel, KERNEL_SOURCES.get(dom_kernel, ""), traffic_config)
+    traffic = committed_traffic(dom_kernel, KERNEL_SOURCES.get(dom_kernel), traffic_config)
     value = world * flops / (ms_per_step * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
