@@ -83,11 +83,15 @@ struct Item {
   int32_t multi;
 };
 constexpr uint32_t kHalfTileBytes = kTileBytes / 2;  // 64 rows
+// Output staging: one 128-byte row per softmax thread, rows 144 bytes apart so
+// that a warp's 16-byte shared stores fall in distinct bank groups.
+constexpr uint32_t kStagePitch = kD * 2 + 16;
 
 struct alignas(1024) Smem {
   __nv_bfloat16 q[2][kRows * kD];
   __nv_bfloat16 k[kStages][kRows * kD];
   __nv_bfloat16 v[kStages][kRows * kD];
+  alignas(16) uint8_t ostage[2][kRows * kStagePitch];   // epilogue rows on their way to HBM
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
@@ -630,7 +634,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (pos < len && head < p.H) {  // (a repeated head's rows are not stored)
         const int64_t tok = static_cast<int64_t>(start) + pos;
         const float inv = 1.f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + head) * kD);
+        // The row goes through shared memory to one bulk copy: 16-byte stores
+        // of 32 rows at a time straight to HBM stall the warp, a copy does not.
+        uint8_t* stage = S.ostage[t] + row * kStagePitch;
+        bulk_wait_read();               // this thread's previous row has left the stage
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint32_t* src = o[g >> 2] + (g & 3) * 8;
@@ -639,12 +646,16 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
           w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
           w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
-          dst[g] = w;
+          reinterpret_cast<uint4*>(stage)[g] = w;
         }
+        fence_proxy_async_smem();
+        bulk_store(p.out + (tok * p.H + head) * kD, smem_u32(stage), kD * 2);
+        bulk_commit();
         if (p.lse) p.lse[static_cast<int64_t>(head) * p.lse_stride + tok] =
             (m + __log2f(l)) * kLn2;
       }
     }
+    bulk_wait_all();                    // every row is written before the CTA retires
   }
 
   tc_fence_before();
