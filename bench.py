@@ -176,7 +176,8 @@ _HEADERS = ["pe_common.cuh", "pe_sm103.cuh"]
 KERNEL_SOURCES = {"tcgen05_bf16_d64": ["pe_fwd_sm103.cu"] + _HEADERS,
                   "simt_ffma": ["pe_fwd_simt.cu", "pe_fwd_simt.cuh", "pe_common.cuh"],
                   "first_token_gemv": ["pe_first_token.cu"] + _HEADERS,
-                  "tcgen05_f32_d64": ["pe_fwd_sm103_f32.cu"] + _HEADERS}
+                  "tcgen05_f32_d64": ["pe_fwd_sm103_f32.cu"] + _HEADERS,
+                  "tcgen05_bf16_d128": ["pe_fwd_sm103_d128.cu"] + _HEADERS}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -192,12 +193,14 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     pe.load_library()
     wl = workloads.WORKLOADS[args.workload]
-    if args.dtype and args.dtype != wl.dtype:
+    if (args.dtype and args.dtype != wl.dtype) or args.heads or args.head_dim:
         if not args.packed:
-            raise SystemExit("--dtype needs --packed")
+            raise SystemExit("--dtype, --heads and --head-dim need --packed")
         import dataclasses
-        wl = dataclasses.replace(wl, dtype=args.dtype,
-                                 description=f"{wl.description}, as {args.dtype}")
+        dt = args.dtype or wl.dtype
+        h_, d_ = args.heads or wl.num_heads, args.head_dim or wl.head_dim
+        wl = dataclasses.replace(wl, dtype=dt, num_heads=h_, head_dim=d_,
+                                 description=f"{wl.description}, as {h_}x{d_} {dt}")
     # Weak scaling: every rank draws its own batch of the same workload.
     train = wl.backward or args.backward
     rows_layout = args.layout == "rows"
@@ -484,7 +487,8 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": args.workload + (f"[:{args.sequences}]" if args.sequences else "")
-                   + (f" as {args.dtype}" if args.dtype else ""),
+                   + (f" as {wl.num_heads}x{wl.head_dim} {wl.dtype}"
+                      if (args.dtype or args.heads or args.head_dim) else ""),
                    "description": wl.description,
                    "num_sequences": int(len(lengths)), "num_tokens": n_tokens,
                    "heads": h, "head_dim": d, "max_seq_len": s,
@@ -810,7 +814,11 @@ def main():
     ap.add_argument("--workload", default="longdoc_bf16")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--dtype", choices=["bf16", "fp32"], default=None,
-                    help="with --packed: the workload's shapes in another dtype")
+                    help="with --packed: the workload's lengths in another dtype")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="with --packed: the workload's lengths with another head count")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="with --packed: the workload's lengths with another head_dim")
     ap.add_argument("--sequences", type=int, default=None,
                     help="keep only the first K sequences of the workload (profiling cases)")
     ap.add_argument("--packed", action="store_true",

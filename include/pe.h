@@ -242,8 +242,10 @@ pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t
  *   are left as they were. Only the num_sequences + 1 entries are read.
  * scale: finite and > 0 (1/sqrt(D) is the pages' default).
  * head_dim: a multiple of 8 (the module docstring's "Constraints" require
- *   it for the aligned kernels), at most 128; bf16 with head_dim 64 runs on the
- *   tcgen05 tensor cores.
+ *   it for the aligned kernels), at most 128. Full attention runs on the
+ *   tcgen05 tensor cores for bf16 with head_dim 64 or 128 and for fp32 with
+ *   head_dim 64 (fp32 operands split into bf16 hi and lo parts, three
+ *   products each, fp32 accumulation); other shapes run on the CUDA cores.
  * All tensor pointers 16-byte aligned.
  * workspace: device, >= pe_attention_workspace_size(...) bytes. Its first 4
  *   bytes receive a device-side status (PE_OK, PE_ERR_BAD_LENGTH or
@@ -363,10 +365,10 @@ pe_status pe_geglu(pe_dtype dtype, const void* x, int64_t num_tokens, int32_t fe
                    pe_stream_t stream);
 
 /* Name of the kernel family that pe_packed_attention_fwd (backward = 0) or
- * pe_packed_attention_bwd (backward = 1) runs for these arguments on an sm_103a
- * device: "tcgen05_bf16_d64", "simt_ffma", "first_token_gemv",
- * "simt_ffma_bwd", "tcgen05_bf16_d64_bwd", or "unsupported". A static
- * string; never NULL. */
+ * pe_packed_attention_bwd (backward = 1) runs for these arguments (full
+ * attention) on an sm_103a device: "tcgen05_bf16_d64", "tcgen05_bf16_d128",
+ * "tcgen05_f32_d64", "simt_ffma", "first_token_gemv", "simt_ffma_bwd",
+ * "tcgen05_bf16_d64_bwd", or "unsupported". A static string; never NULL. */
 const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_first_token,
                                 int backward);
 

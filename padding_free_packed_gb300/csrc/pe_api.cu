@@ -181,6 +181,12 @@ extern "C" pe_status pe_packed_attention_fwd_local(
                             chk, stream));
     return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan, status, stream);
   }
+  if (dtype == PE_BF16 && D == 128 && !win.active()) {
+    PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_d128_fwd_rows_per_item(),
+                            sm103_d128_fwd_pair_heads_rows(), sm103_d128_fwd_quad_heads_rows(),
+                            plan, chk, stream));
+    return fwd_sm103_d128(q, k, v, cu_seqlens, B, H, N, scale, out, lse, plan, status, stream);
+  }
   if (dtype == PE_FP32 && D == 64 && !win.active()) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_f32_fwd_rows_per_item(),
                             sm103_f32_fwd_pair_heads_rows(), sm103_f32_fwd_quad_heads_rows(),
@@ -261,6 +267,7 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
                                                                    : "simt_ffma_bwd";
   if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
   if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64";
+  if (dtype == PE_BF16 && D == 128) return "tcgen05_bf16_d128";
   if (dtype == PE_FP32 && D == 64) return "tcgen05_f32_d64";
   return "simt_ffma";
 }

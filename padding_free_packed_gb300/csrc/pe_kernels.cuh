@@ -66,6 +66,16 @@ pe_status fwd_sm103_f32(const void* q, const void* k, const void* v, const int32
                         int32_t B, int32_t H, int64_t N, float scale, void* out, float* lse,
                         TilePlan plan, DeviceStatus* status, cudaStream_t stream);
 
+// Tensor-core forward, bf16, head_dim 128, full attention (sm_103a): P written
+// over the first half of its tile's score columns. Same work items as the
+// head_dim-64 kernel.
+int sm103_d128_fwd_rows_per_item();
+int sm103_d128_fwd_pair_heads_rows();
+int sm103_d128_fwd_quad_heads_rows();
+pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int32_t* cu,
+                         int32_t B, int32_t H, int64_t N, float scale, void* out, float* lse,
+                         TilePlan plan, DeviceStatus* status, cudaStream_t stream);
+
 // Delta[h, r] = dO_r . O_r (bf16, head_dim 64) into [H, Nq] fp32.
 pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dout, int64_t Nq,
                          int32_t H, float* delta, cudaStream_t stream);
