@@ -83,15 +83,15 @@ struct Item {
   int32_t multi;
 };
 constexpr uint32_t kHalfTileBytes = kTileBytes / 2;  // 64 rows
-// Output staging: one 128-byte row per softmax thread, rows 144 bytes apart so
-// that a warp's 16-byte shared stores fall in distinct bank groups.
-constexpr uint32_t kStagePitch = kD * 2 + 16;
+// Output staging: the 32 rows of a softmax warp (4 KiB), 128-byte swizzled,
+// written to HBM by one TMA store.
+constexpr uint32_t kStageWarpBytes = 32 * kD * 2;
 
 struct alignas(1024) Smem {
   __nv_bfloat16 q[2][kRows * kD];
   __nv_bfloat16 k[kStages][kRows * kD];
   __nv_bfloat16 v[kStages][kRows * kD];
-  alignas(16) uint8_t ostage[2][kRows * kStagePitch];   // epilogue rows on their way to HBM
+  alignas(1024) uint8_t ostage[8][kStageWarpBytes];   // per softmax warp, on the way to HBM
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
@@ -212,7 +212,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_q64,
                  const __grid_constant__ CUtensorMap tm_k64,
-                 const __grid_constant__ CUtensorMap tm_v64, const FwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_v64,
+                 const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -631,13 +632,18 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_ld32(lane_base + col_o(t) + 32, o[1]);
       tmem_wait_ld(o[0]);
       tmem_wait_ld(o[1]);
-      if (pos < len && head < p.H) {  // (a repeated head's rows are not stored)
-        const int64_t tok = static_cast<int64_t>(start) + pos;
-        const float inv = 1.f / l;
-        // The row goes through shared memory to one bulk copy: 16-byte stores
-        // of 32 rows at a time straight to HBM stall the warp, a copy does not.
-        uint8_t* stage = S.ostage[t] + row * kStagePitch;
-        bulk_wait_read();               // this thread's previous row has left the stage
+      // A warp's 32 rows are 32 consecutive tokens of one head: when all of
+      // them are real they go through shared memory to one TMA store (the
+      // copy engine moves 4 KiB, no 16-byte stores of 32 rows at a time from
+      // the warp); the partial warp at a sequence's end stores its rows itself.
+      const int32_t pos0 = pos - lane;                  // warp-uniform
+      const bool real = pos < len && head < p.H;        // (a repeated head's rows are not stored)
+      const float inv = 1.f / l;
+      const int64_t tok = static_cast<int64_t>(start) + pos;
+      if (head < p.H && len - pos0 >= 32) {
+        uint8_t* stage = S.ostage[warp - 4];
+        if (lane == 0) bulk_wait_read();                // the previous store has left the stage
+        __syncwarp();
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const uint32_t* src = o[g >> 2] + (g & 3) * 8;
@@ -646,14 +652,29 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
           w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
           w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
-          reinterpret_cast<uint4*>(stage)[g] = w;
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((g ^ (lane & 7)) << 4)) = w;
         }
         fence_proxy_async_smem();
-        bulk_store(p.out + (tok * p.H + head) * kD, smem_u32(stage), kD * 2);
-        bulk_commit();
-        if (p.lse) p.lse[static_cast<int64_t>(head) * p.lse_stride + tok] =
-            (m + __log2f(l)) * kLn2;
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tm_o, smem_u32(stage), head * kD, start + pos0);
+          bulk_commit();
+        }
+      } else if (real) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + head) * kD);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t* src = o[g >> 2] + (g & 3) * 8;
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+          dst[g] = w;
+        }
       }
+      if (real && p.lse) p.lse[static_cast<int64_t>(head) * p.lse_stride + tok] =
+          (m + __log2f(l)) * kLn2;
     }
     bulk_wait_all();                    // every row is written before the CTA retires
   }
@@ -682,7 +703,8 @@ pe_status get_encoder() {
   return PE_OK;
 }
 
-// [N, H*64] bf16 rows; boxes of box_rows rows x 64 columns (one head), 128-byte swizzle.
+// [N, H*64] bf16 rows; boxes of box_rows rows x 64 columns (one head), 128-byte
+// swizzle (loads of q, k, v; stores of 32-row output boxes).
 pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H,
                    uint32_t box_rows = kRows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * kD, static_cast<cuuint64_t>(N)};
@@ -706,7 +728,8 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
                     TilePlan plan, DeviceStatus* status, cudaStream_t stream) {
   PE_TRY(get_encoder());
-  CUtensorMap mq, mk, mv, mq64, mk64, mv64;
+  CUtensorMap mq, mk, mv, mq64, mk64, mv64, mo;
+  PE_TRY(make_map(&mo, out, N, H, 32));
   PE_TRY(make_map(&mq, q, N, H));
   PE_TRY(make_map(&mk, k, N, H));
   PE_TRY(make_map(&mv, v, N, H));
@@ -737,7 +760,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.win = win;
   prm.status = status;
   prm.wait_limit_ns = wait_limit_ns();
-  kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mq64, mk64, mv64, prm);
+  kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mq64, mk64, mv64, mo, prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }
