@@ -74,10 +74,15 @@ struct Item {
 };
 constexpr uint32_t kHalfTileBytes = kTileBytes / 2;  // 64 rows
 
+// Output staging: the 32 rows x 32 columns of each accumulator that an
+// elementwise warp writes (2 KiB each, 64-byte swizzled), stored by TMA.
+constexpr uint32_t kStageAccBytes = 32 * 32 * 2;
+
 struct alignas(1024) Smem {
   __nv_bfloat16 st[2][kRows * kD];             // stationary tiles
   __nv_bfloat16 u[kStages][2][kRows * kD];     // streaming tile pairs
   float vec[kStages][2][kRows];                // key pass: -lse*log2e and -Delta per query column
+  alignas(1024) uint8_t ostage[8][2 * kStageAccBytes];  // per elementwise warp: acc1, acc2
   uint64_t item_full[2], item_empty[2];
   uint64_t st_full, st_empty;
   uint64_t u_full[kStages], u_empty[kStages];
@@ -137,7 +142,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_q64,
                  const __grid_constant__ CUtensorMap tm_k64,
                  const __grid_constant__ CUtensorMap tm_v64,
-                 const __grid_constant__ CUtensorMap tm_do64, const BwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_do64,
+                 const __grid_constant__ CUtensorMap tm_o1,
+                 const __grid_constant__ CUtensorMap tm_o2, const BwdParams p) {
   constexpr int kAccWarps = kKeyPass ? 2 : 1;
   constexpr int kUseWarps = 2 + kAccWarps;     // warps reading each streaming pair
   extern __shared__ uint8_t smem_raw[];
@@ -571,11 +578,45 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (lane == 0) mbar_arrive(smem_u32(&S.o_free));
       const int32_t pos_r = it.dual ? (row & 63) : r0 + row;
       const int32_t head_r = it.dual ? it.head + (row >> 6) : it.head;
-      if (pos_r < len) {
+      // key pass: acc1 = dV (unscaled), acc2 = dK (times scale); query pass: acc1 = dQ * scale.
+      const float s1 = kKeyPass ? 1.f : p.scale, s2 = p.scale;
+      // A warp's 32 rows are 32 consecutive tokens of one head: when all are
+      // real, its 32 columns of each accumulator go through a 64-byte-swizzled
+      // stage to one TMA store; the partial warp at a sequence's end stores its
+      // rows itself.
+      const int32_t pos0 = pos_r - lane;               // warp-uniform
+      if (len - pos0 >= 32) {
+        uint8_t* stage = S.ostage[warp - 8];
+        if (lane == 0) bulk_wait_read();               // the previous stores have left the stage
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t off = lane * 64 + ((g ^ ((lane >> 1) & 3)) << 4);
+          uint4 wv;
+          wv.x = pack_bf16x2(__uint_as_float(a1[8 * g + 0]) * s1, __uint_as_float(a1[8 * g + 1]) * s1);
+          wv.y = pack_bf16x2(__uint_as_float(a1[8 * g + 2]) * s1, __uint_as_float(a1[8 * g + 3]) * s1);
+          wv.z = pack_bf16x2(__uint_as_float(a1[8 * g + 4]) * s1, __uint_as_float(a1[8 * g + 5]) * s1);
+          wv.w = pack_bf16x2(__uint_as_float(a1[8 * g + 6]) * s1, __uint_as_float(a1[8 * g + 7]) * s1);
+          *reinterpret_cast<uint4*>(stage + off) = wv;
+          if (kKeyPass) {
+            wv.x = pack_bf16x2(__uint_as_float(a2[8 * g + 0]) * s2, __uint_as_float(a2[8 * g + 1]) * s2);
+            wv.y = pack_bf16x2(__uint_as_float(a2[8 * g + 2]) * s2, __uint_as_float(a2[8 * g + 3]) * s2);
+            wv.z = pack_bf16x2(__uint_as_float(a2[8 * g + 4]) * s2, __uint_as_float(a2[8 * g + 5]) * s2);
+            wv.w = pack_bf16x2(__uint_as_float(a2[8 * g + 6]) * s2, __uint_as_float(a2[8 * g + 7]) * s2);
+            *reinterpret_cast<uint4*>(stage + kStageAccBytes + off) = wv;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t x = head_r * kD + 32 * h, y = start + pos0;
+          tma_store_2d(kKeyPass ? &tm_o2 : &tm_o1, smem_u32(stage), x, y);
+          if (kKeyPass) tma_store_2d(&tm_o1, smem_u32(stage) + kStageAccBytes, x, y);
+          bulk_commit();
+        }
+      } else if (pos_r < len) {
         const int64_t tok = static_cast<int64_t>(start) + pos_r;
         const int64_t off = (tok * p.H + head_r) * kD + 32 * h;
-        // key pass: acc1 = dV (unscaled), acc2 = dK (times scale); query pass: acc1 = dQ * scale.
-        const float s1 = kKeyPass ? 1.f : p.scale;
         uint4* d1 = reinterpret_cast<uint4*>((kKeyPass ? p.out2 : p.out1) + off);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -588,7 +629,6 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         if (kKeyPass) {
           uint4* d2 = reinterpret_cast<uint4*>(p.out1 + off);
-          const float s2 = p.scale;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             uint4 wv;
@@ -601,6 +641,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
       }
     }
+    bulk_wait_all();                                   // every row is written before the CTA retires
   }
 
   tc_fence_before();
@@ -640,9 +681,27 @@ pe_status make_map_bwd(CUtensorMap* map, const void* base, int64_t N, int32_t H,
   return r == CUDA_SUCCESS ? PE_OK : PE_ERR_CUDA;
 }
 
+// [N, H*64] bf16 gradient rows; stores of 32 rows x 32 columns (half a head),
+// 64-byte swizzle.
+pe_status make_map_out(CUtensorMap* map, void* base, int64_t N, int32_t H) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * kD, static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * kD * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r = g_encode_bwd(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+                            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PE_OK : PE_ERR_CUDA;
+}
+
 template <bool kKeyPass>
 pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, LayoutCheck check,
                       cudaStream_t stream) {
+  // Output maps: key pass dK (out1) and dV (out2), query pass dQ (out1).
+  CUtensorMap mo1, mo2;
+  PE_TRY(make_map_out(&mo1, prm.out1, prm.Nq, prm.H));
+  PE_TRY(make_map_out(&mo2, kKeyPass ? prm.out2 : prm.out1, prm.Nq, prm.H));
   auto kernel = prm.win.active() ? bwd_sm103_kernel<kKeyPass, true>
                                  : bwd_sm103_kernel<kKeyPass, false>;
   const size_t smem = sizeof(Smem) + 1024;
@@ -657,7 +716,7 @@ pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, LayoutChe
   PE_TRY(launch_tile_plan(prm.cu, prm.B, prm.H, kRows, prm.pair_heads_rows, 0, prm.plan,
                           check, stream));
   kernel<<<device_sm_count(), kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6],
-                                                        m[7], prm);
+                                                        m[7], mo1, mo2, prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }
