@@ -52,6 +52,9 @@ constexpr uint32_t kHalfColBytes = kRows * 64 * 2;   // one 64-column box of 128
 constexpr uint32_t kTileBytes = 2 * kHalfColBytes;   // 32 KiB
 constexpr uint32_t kHalfRowBytes = kHalfColBytes / 2;  // 64 rows of one 64-column box
 constexpr int kPairRows = 2 * kRows;
+// Output staging: 32 rows x 64 columns of a softmax warp (4 KiB, 128-byte
+// swizzled), one 64-column half of its rows at a time, written by TMA.
+constexpr uint32_t kStageWarpBytes = 32 * 64 * 2;
 
 __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }   // P over its first 64
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
@@ -67,6 +70,7 @@ struct alignas(1024) Smem {
   __nv_bfloat16 q[2][kRows * kD];
   __nv_bfloat16 k[kStages][kRows * kD];
   __nv_bfloat16 v[kStages][kRows * kD];
+  alignas(1024) uint8_t ostage[8][kStageWarpBytes];
   uint64_t item_full[2], item_empty[2];
   uint64_t q_full, q_empty;
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
@@ -76,6 +80,8 @@ struct alignas(1024) Smem {
   uint32_t tmem_base;
   WaitGuard guard;
 };
+
+static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory exceeds the per-CTA limit");
 
 struct FwdParams {
   const int32_t* cu;
@@ -155,7 +161,8 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q64,
                       const __grid_constant__ CUtensorMap tm_k64,
-                      const __grid_constant__ CUtensorMap tm_v64, const FwdParams p) {
+                      const __grid_constant__ CUtensorMap tm_v64,
+                      const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -505,31 +512,54 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         break;
       ++o_cnt;
       tc_fence_after();
+      // A warp's 32 rows are 32 consecutive tokens of one head: when all are
+      // real, each 64-column half goes through the warp's 4 KiB stage to one
+      // TMA store; the partial warp at a sequence's end stores its rows itself.
       const bool store = pos < len && head < p.H;
+      const bool full = head < p.H && len - (pos - lane) >= 32;   // warp-uniform
       const int64_t tok = static_cast<int64_t>(start) + pos;
       const float inv = 1.f / l;
+      uint8_t* stage = S.ostage[warp - 4];
       uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * p.H + head) * kD);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + col_o(t) + 32 * h, o);
-        tmem_wait_ld(o);
-        if (store) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[2][32];
+        tmem_ld32(lane_base + col_o(t) + 64 * c, o[0]);
+        tmem_ld32(lane_base + col_o(t) + 64 * c + 32, o[1]);
+        tmem_wait_ld(o[0]);
+        tmem_wait_ld(o[1]);
+        if (full) {
+          if (lane == 0) bulk_wait_read();   // the previous half has left the stage
+          __syncwarp();
+        }
+        if (full || store) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint32_t* src = o + 8 * g;
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t* src = o[g >> 2] + (g & 3) * 8;
             uint4 w;
             w.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
             w.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
             w.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
             w.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
-            dst[4 * h + g] = w;
+            if (full)
+              *reinterpret_cast<uint4*>(stage + lane * 128 + ((g ^ (lane & 7)) << 4)) = w;
+            else
+              dst[8 * c + g] = w;
+          }
+        }
+        if (full) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_o, smem_u32(stage), head * kD + 64 * c, start + (pos - lane));
+            bulk_commit();
           }
         }
       }
       if (store && p.lse) p.lse[static_cast<int64_t>(head) * p.lse_stride + tok] =
           (m + __log2f(l)) * kLn2;
     }
+    bulk_wait_all();                    // every row is written before the CTA retires
   }
 
   tc_fence_before();
@@ -581,7 +611,8 @@ pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int3
                          int32_t B, int32_t H, int64_t N, float scale, void* out, float* lse,
                          TilePlan plan, DeviceStatus* status, cudaStream_t stream) {
   PE_TRY(get_encoder_d128());
-  CUtensorMap mq, mk, mv, mq64, mk64, mv64;
+  CUtensorMap mq, mk, mv, mq64, mk64, mv64, mo;
+  PE_TRY(make_map_d128(&mo, out, N, H, 32));
   PE_TRY(make_map_d128(&mq, q, N, H, kRows));
   PE_TRY(make_map_d128(&mk, k, N, H, kRows));
   PE_TRY(make_map_d128(&mv, v, N, H, kRows));
@@ -610,7 +641,7 @@ pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int3
   prm.status = status;
   prm.wait_limit_ns = wait_limit_ns();
   fwd_sm103_d128_kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mq64, mk64,
-                                                                       mv64, prm);
+                                                                       mv64, mo, prm);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }
