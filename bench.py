@@ -476,6 +476,8 @@ def run_ours(args, rank, world):
     else:
         achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     traffic_config = (args.workload + (f"[:{args.sequences}]" if args.sequences else "")
+                      + (f" as {wl.num_heads}x{wl.head_dim} {wl.dtype}"
+                         if (args.dtype or args.heads or args.head_dim) else "")
                       + (" first-token" if args.first_token else "")
                       + (f" window {window[0]} {window[1]}" if window else "")
                       + (" backward" if train and dom_kernel == bwd_kernel else "")
