@@ -175,7 +175,8 @@ def committed_traffic(kernel_name: str, source_files, config: str):
 _HEADERS = ["pe_common.cuh", "pe_sm103.cuh"]
 KERNEL_SOURCES = {"tcgen05_bf16_d64": ["pe_fwd_sm103.cu"] + _HEADERS,
                   "simt_ffma": ["pe_fwd_simt.cu", "pe_fwd_simt.cuh", "pe_common.cuh"],
-                  "first_token_gemv": ["pe_first_token.cu"] + _HEADERS,
+                  "first_token_gemv": ["pe_first_token.cu", "pe_token_stream.cuh"] + _HEADERS,
+                  "first_token_bwd": ["pe_first_token_bwd.cu", "pe_token_stream.cuh"] + _HEADERS,
                   "tcgen05_f32_d64": ["pe_fwd_sm103_f32.cu"] + _HEADERS,
                   "tcgen05_bf16_d128": ["pe_fwd_sm103_d128.cu"] + _HEADERS}
 
@@ -230,13 +231,14 @@ def run_ours(args, rank, world):
     if args.first_token:
         if not args.packed:
             raise SystemExit("--first-token needs --packed")
-        train = False
+        train = args.backward   # a workload's own backward step is for full attention
     window = tuple(args.window) if args.window else None
     fwd_flops = real_flops(lengths, h, d, first_token=args.first_token, window=window)
     bwd_flops = 2.5 * fwd_flops if train else 0.0   # 10 sum L^2 H d: five GEMM-shaped products
     flops = fwd_flops + bwd_flops
     kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token)
-    bwd_kernel = pe.pe_attention_kernel(wl.torch_dtype, d, backward=True) if train else None
+    bwd_kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token,
+                                        backward=True) if train else None
 
     # The per-step layout metadata: lengths, or the packed rows' mask.
     meta_host = row_ids if rows_layout else lengths
@@ -249,6 +251,8 @@ def run_ours(args, rank, world):
     packed_cu = pe.pe_pack_sequences(lengths_d, s)[1] if args.packed else None
     q_first = (dev_grids[0][packed_cu[:-1].long()].contiguous()
                if args.packed and args.first_token else None)
+    do_first = (dev_grids[3][packed_cu[:-1].long()].contiguous()
+                if args.packed and args.first_token and train else None)
     stream = torch.cuda.current_stream(dev)
     fwd_events, bwd_events = [], []
     # One workspace per direction for every call (all attention calls run on
@@ -258,7 +262,7 @@ def run_ours(args, rank, world):
         wl.torch_dtype, n_seq, n_tokens, h, d, s, args.first_token, False)),
         dtype=torch.uint8, device=dev)
     ws_bwd = torch.empty(max(16, pe.attention_workspace_bytes(
-        wl.torch_dtype, n_seq, n_tokens, h, d, s, False, True)),
+        wl.torch_dtype, n_seq, n_tokens, h, d, s, args.first_token, True)),
         dtype=torch.uint8, device=dev) if train else None
 
     # Full attention, or local attention with the --window bounds.
@@ -271,10 +275,11 @@ def run_ours(args, rank, world):
                                                 scale_, **kw)
 
     def attention_bwd(*a):
+        ft = bool(args.first_token)
         if window is None:
-            return pe.pe_packed_attention_bwd(*a, workspace=ws_bwd)
+            return pe.pe_packed_attention_bwd(*a, query_is_first_token=ft, workspace=ws_bwd)
         return pe.pe_packed_attention_bwd_local(*a[:8], window[0], window[1], a[8],
-                                                workspace=ws_bwd)
+                                                query_is_first_token=ft, workspace=ws_bwd)
 
     def timed(record, events, fn):
         if not record:
@@ -294,8 +299,11 @@ def run_ours(args, rank, world):
             cu = packed_cu
             q, k, v = grids[:3]
             if args.first_token:
-                out, _ = timed(record, fwd_events, lambda: attention_fwd(
-                    q_first, k, v, cu, s, wl.scale, query_is_first_token=True))
+                out, lse = timed(record, fwd_events, lambda: attention_fwd(
+                    q_first, k, v, cu, s, wl.scale, query_is_first_token=True, need_lse=train))
+                if train:
+                    timed(record, bwd_events, lambda: attention_bwd(
+                        do_first, q_first, k, v, out, lse, cu, s, wl.scale))
                 return n_tokens
         elif rows_layout:
             flat, cu, n = pe.pe_pack_document_ids(lengths_t)
@@ -323,8 +331,8 @@ def run_ours(args, rank, world):
     # Padded steps: pack scan+fill, 3 gathers, plan+attention, scatter; training
     # adds the dO gather, the backward (delta, plan, key pass, plan, query pass)
     # and 3 scatters. Packed steps: plan+attention (+ the 5 backward launches).
-    if args.packed and args.first_token:   # layout check, streaming kernel, merge
-        launches_per_step = 3
+    if args.packed and args.first_token:   # layout check, streaming kernel, merge (each way)
+        launches_per_step = 3 + (3 if train else 0)
     elif args.packed:
         launches_per_step = 2 + (5 if train else 0)
     elif rows_layout:   # mask count, scan, fill, 3 gathers, plan + attention (+ dO gather, backward)
@@ -460,7 +468,7 @@ def run_ours(args, rank, world):
     elif dom_kernel.startswith("tcgen05"):
         bound, peak, unit = "tensor", float(peaks["bf16_tflops"]), "TFLOP/s"
         peak_note = f"dense bf16 burst, {peaks_src}"
-    elif dom_kernel == "first_token_gemv":
+    elif dom_kernel in ("first_token_gemv", "first_token_bwd"):
         bound, peak, unit = "hbm", float(peaks["hbm_gbs"]), "GB/s"
         peak_note = f"HBM copy, {peaks_src}"
     else:
@@ -469,9 +477,14 @@ def run_ours(args, rank, world):
         bound, peak, unit = "alu", ffma, "TFLOP/s"
         peak_note = "FFMA: SMs x 128 lanes x 2 flop x max SM clock"
     if bound == "hbm":
-        # k and v read once, q read and the output written once per sequence and head.
         esize = 4 if wl.dtype == "fp32" else 2
-        hbm_bytes = (2 * n_tokens + 2 * len(lengths)) * h * d * esize
+        if dom_kernel == "first_token_bwd":
+            # k, v read and dk, dv written once; q, dO, out read and dq written
+            # once per sequence and head; lse read.
+            hbm_bytes = (4 * n_tokens + 4 * len(lengths)) * h * d * esize + 4 * h * len(lengths)
+        else:
+            # k and v read once, q read and the output written once per sequence and head.
+            hbm_bytes = (2 * n_tokens + 2 * len(lengths)) * h * d * esize
         achieved = hbm_bytes / (dom_ms * 1e-3) / 1e9
     else:
         achieved = dom_flops / (dom_ms * 1e-3) / 1e12

@@ -123,6 +123,8 @@ extern "C" size_t pe_attention_workspace_size(pe_dtype dtype, int32_t B, int64_t
   if (query_is_first_token && !backward)
     bytes += first_token_stream_supported(dtype, H, D) ? first_token_stream_partial_bytes(N, H, D)
                                                        : first_token_partial_bytes(B, H, D, S);
+  if (query_is_first_token && backward && first_token_bwd_stream_supported(dtype, H, D))
+    bytes += first_token_bwd_stream_partial_bytes(N, H, D);
   return bytes;
 }
 
@@ -231,11 +233,20 @@ extern "C" pe_status pe_packed_attention_bwd_local(
                          attention_ws_bytes(B, N, H, query_is_first_token, 1)));
   if (!device_is_sm103()) return PE_ERR_UNSUPPORTED;
   const Window win = make_window(window_left, window_right, S);
+  DeviceStatus* status = static_cast<DeviceStatus*>(workspace);
+  const LayoutCheck chk = {S, N, status};
+  const size_t base_bytes = attention_ws_bytes(B, N, H, query_is_first_token, 1);
+  if (B > 0 && query_is_first_token && first_token_bwd_stream_supported(dtype, H, D) &&
+      workspace_bytes >= base_bytes + first_token_bwd_stream_partial_bytes(N, H, D)) {
+    // Streaming form: the layout check writes the status word (its reset).
+    PE_TRY(launch_layout_check(cu_seqlens, B, chk, stream));
+    float* part = reinterpret_cast<float*>(static_cast<char*>(workspace) + base_bytes);
+    return bwd_first_token_stream(dtype, D, q, k, v, out, dout, lse, cu_seqlens, B, H, N, S,
+                                  scale, win, dq, dk, dv, part, status, stream);
+  }
   PE_CUDA_TRY(cudaMemsetAsync(workspace, 0, sizeof(DeviceStatus), stream));
   if (B == 0) return PE_OK;
   TilePlan plan = plan_view(workspace, B);
-  DeviceStatus* status = static_cast<DeviceStatus*>(workspace);
-  const LayoutCheck chk = {S, N, status};
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan_bytes(B));
   if (dtype == PE_BF16 && D == 64 && !query_is_first_token) {
     PE_TRY(bwd_preprocess(dtype, D, out, dout, N, H, delta, stream));
@@ -262,9 +273,11 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
                                           int backward) {
   if ((dtype != PE_BF16 && dtype != PE_FP32) || D < 8 || D % 8 != 0 || D > kMaxHeadDim)
     return "unsupported";
-  if (backward)
-    return (dtype == PE_BF16 && D == 64 && !query_is_first_token) ? "tcgen05_bf16_d64_bwd"
-                                                                   : "simt_ffma_bwd";
+  if (backward) {
+    if (query_is_first_token)
+      return (D == 32 || D == 64 || D == 128) ? "first_token_bwd" : "simt_ffma_bwd";
+    return (dtype == PE_BF16 && D == 64) ? "tcgen05_bf16_d64_bwd" : "simt_ffma_bwd";
+  }
   if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
   if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64";
   if (dtype == PE_BF16 && D == 128) return "tcgen05_bf16_d128";

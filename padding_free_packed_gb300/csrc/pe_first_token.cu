@@ -1,24 +1,15 @@
-// First-token query, streaming form.
+// First-token query, streaming forward.
 //
 // In first-token mode every sequence has one query row (its first token), so
 // the forward is a matrix-vector product per (sequence, head) whose cost is
 // reading k and v once (page "Source code for gigl.nn.packed_attention",
-// function `packed_attention`, `query_is_first_token`). The packed buffers are
-// token-major [N, H, D]: one token's keys for all heads are one contiguous row
-// of H*D elements. This kernel streams those rows in order instead of reading
-// one head's 2*D-byte slices at an H*D stride:
+// function `packed_attention`, `query_is_first_token`). The kernel streams
+// whole token rows through the ring of pe_token_stream.cuh (equal token
+// chunks, one CTA each, a producer thread and four consumer warps):
 //
-//  * the token range [0, N) is cut into equal chunks, one CTA each and as
-//    many as fit on the GPU at once (never shorter than 64 tokens), so every
-//    CTA moves the same number of bytes whatever the mix of sequence lengths;
-//  * a CTA walks the sequences that overlap its chunk. One producer thread
-//    streams their visible k and v rows into a five-stage shared-memory ring
-//    with bulk asynchronous copies (cp.async.bulk, completion counted in bytes
-//    on an mbarrier per stage), running ahead across sequence boundaries; four
-//    consumer warps read each row with 16-byte shared loads (each lane owns VPL
-//    vectors of a row, a head's D elements being LPH consecutive lanes), keep
-//    one online-softmax state per (lane, vector), release the stage, and at
-//    each sequence's end merge their states in shared memory;
+//  * the consumers keep one online-softmax state per (lane, vector), release
+//    each stage, and at each sequence's end merge their states in shared
+//    memory;
 //  * a sequence that lies inside one chunk is finished there (output, lse); a
 //    sequence that crosses chunk edges leaves one partial state (m, l, o[D]
 //    per head) in every chunk it touches (slot 1 in its first chunk, slot 0
@@ -30,127 +21,32 @@
 // and a head's row slice spans a power of two of lanes (D in {32, 64, 128});
 // other shapes run the per-(sequence, head) kernel in pe_fwd_simt.cu.
 #include "pe_kernels.cuh"
-#include "pe_sm103.cuh"
+#include "pe_token_stream.cuh"
 
 namespace pe {
 namespace {
 
-using namespace sm103;
+using namespace stream;
 
-constexpr int kStWarps = 4;                     // consumer warps
-constexpr int kStThreads = kStWarps * 32;       // consumer threads
-constexpr int kStBlock = kStThreads + 32;       // + one producer warp
-constexpr int kStStages = 5;
-constexpr int kStStageBytes = 8192;             // of k (and as much of v) per stage
+constexpr int kStWarps = stream::kWarps;
+constexpr int kStThreads = stream::kThreads;
+constexpr int kStBlock = stream::kBlock;
+constexpr int kStStages = stream::kStages;
 constexpr int32_t kStMaxChunks = 16384;
 enum StWaitSite { kSiteStProducer = 21, kSiteStConsumer = 22 };
 
 template <typename T, int D, int VPL>
-struct StShape {
-  static constexpr int kEPV = 16 / (int)sizeof(T);  // elements per 16-byte vector
-  static constexpr int kLPH = D / kEPV;              // lanes per head
-  static constexpr int kRow = 32 * VPL * kEPV;       // elements of one token row (H * D)
-  static constexpr int kRowBytes = kRow * (int)sizeof(T);
-  static constexpr int kH = kRow / D;                // heads
-  static constexpr int kRows = kStStageBytes / kRowBytes > 0 ? kStStageBytes / kRowBytes : 1;
-  static constexpr int kStageElems = kRows * kRow;   // of k (or v) per stage
+struct StShape : Shape<T, D, VPL> {
   static constexpr int kMinBlocks = VPL <= 6 ? 2 : 1;
-  static constexpr size_t kSmem = (size_t)kStStages * 2 * kStageElems * sizeof(T) +
-                                  (size_t)kStWarps * (kRow + 2 * kH) * sizeof(float);
-  static_assert(32 % kLPH == 0 && kLPH >= 1, "a head must span a power of two of lanes");
-  static_assert(kRowBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+  static constexpr size_t kSmem =
+      Shape<T, D, VPL>::kRingBytes +
+      (size_t)kStWarps * (Shape<T, D, VPL>::kRow + 2 * Shape<T, D, VPL>::kH) * sizeof(float);
 };
-
-template <typename T>
-__device__ __forceinline__ void unpack16(const uint4& r, float (&x)[16 / sizeof(T)]) {
-  if constexpr (sizeof(T) == 4) {
-    x[0] = __uint_as_float(r.x);
-    x[1] = __uint_as_float(r.y);
-    x[2] = __uint_as_float(r.z);
-    x[3] = __uint_as_float(r.w);
-  } else {
-    // bf16 element 2j is the low half of word j; a bf16 is the top half of an fp32.
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = __uint_as_float(w[j] << 16);
-      x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-    }
-  }
-}
-
-__device__ __forceinline__ uint4 load16(const void* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
-// global to shared memory, counted on the mbarrier `bar`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Barrier of the consumer warps only (the producer warp never joins it).
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kStThreads) : "memory");
-}
-// The same barrier (another id) that also returns the OR of `x` over the
-// consumer threads, so that they all take the same branch after it.
-__device__ __forceinline__ bool consumers_sync_or(bool x) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 2, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(x ? 1u : 0u), "n"(kStThreads)
-      : "memory");
-  return r != 0;
-}
-
-// Largest i in [0, B) with cu[i] <= t (cu[0] = 0 <= t), found by the whole
-// warp: each round probes 32 evenly spaced entries and keeps the interval the
-// last true probe opens.
-__device__ __forceinline__ int32_t find_sequence(const int32_t* __restrict__ cu, int32_t B,
-                                                 int32_t t, int lane) {
-  int32_t lo = 0, hi = B;  // answer in [lo, hi)
-  while (hi - lo > 32) {
-    const int32_t step = (hi - lo + 31) / 32;
-    const int32_t idx = lo + lane * step;
-    const bool le = idx < hi && __ldg(cu + idx) <= t;
-    const int n = __popc(__ballot_sync(0xffffffffu, le));  // >= 1: cu[lo] <= t
-    lo += (n - 1) * step;
-    hi = min(hi, lo + step);
-  }
-  const int32_t idx = lo + lane;
-  const bool le = idx < hi && __ldg(cu + idx) <= t;
-  return lo + __popc(__ballot_sync(0xffffffffu, le)) - 1;
-}
 
 // Partial state of (chunk c, slot, head h): m, l, o[D].
 template <int D>
 __device__ __forceinline__ float* partial_state(float* part, int64_t c, int slot, int H, int h) {
   return part + ((c * 2 + slot) * H + h) * (D + 2);
-}
-
-// The visible rows of one sequence inside a chunk: [a, vis_end) of sequence i,
-// whose keys seen by its query are [s0, e1).
-struct Segment {
-  int64_t s0, e1, a, vis_end, next;
-};
-
-__device__ __forceinline__ Segment segment_of(const int32_t* __restrict__ cu, int32_t i,
-                                              int64_t a, int64_t c1, int32_t key_limit) {
-  Segment g;
-  g.s0 = __ldg(cu + i);
-  const int64_t s1 = __ldg(cu + i + 1);
-  g.next = min(s1, c1);
-  g.e1 = min(s1, g.s0 + key_limit);
-  g.a = a;
-  g.vis_end = min(g.next, g.e1);
-  return g;
 }
 
 template <typename T, int D, int VPL>
@@ -191,33 +87,9 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
   const int32_t first = find_sequence(cu, B, (int32_t)c0, lane);
 
   if (warp == kStWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane != 0) return;
-    uint32_t g = 0;           // stages issued
-    bool ok = true;
-    int32_t i = first;
-    for (int64_t a = c0; ok && a < c1; ++i) {
-      const Segment sg = segment_of(cu, i, a, c1, key_limit);
-      for (int64_t r0 = sg.a; r0 < sg.vis_end; r0 += R, ++g) {
-        const int s = g % kStStages;
-        if (!mbar_wait(smem_u32(&empty[s]), ((g / kStStages) & 1) ^ 1, abort_flag, status,
-                       kSiteStProducer)) {
-          ok = false;
-          break;
-        }
-        const uint32_t bytes = (uint32_t)(min((int64_t)R, sg.vis_end - r0) * Sh::kRowBytes);
-        mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * bytes);
-        bulk_load(smem_u32(ks + s * Sh::kStageElems), k + r0 * ROW, bytes, smem_u32(&full[s]));
-        bulk_load(smem_u32(vs + s * Sh::kStageElems), v + r0 * ROW, bytes, smem_u32(&full[s]));
-      }
-      a = sg.next;
-    }
-    if (!ok) {
-      // Copies still in flight land in this CTA's shared memory: wait for them
-      // (bounded) before the CTA can retire.
-      for (uint32_t j = g > kStStages ? g - kStStages : 0; j < g; ++j)
-        mbar_drain_wait(smem_u32(&full[j % kStStages]), (j / kStStages) & 1);
-    }
+    if (lane == 0)
+      produce_rows<Sh>(k, v, cu, first, c0, c1, key_limit, ks, vs, full, empty, abort_flag,
+                       status, kSiteStProducer);
     return;
   }
 
@@ -472,10 +344,8 @@ pe_status dispatch_d(int D, int vpl, const void* q, const void* k, const void* v
 }
 
 int stream_vectors_per_lane(pe_dtype dtype, int32_t H, int32_t D) {
-  const int64_t row_bytes = (int64_t)H * D * (dtype == PE_FP32 ? 4 : 2);
-  if (row_bytes % 512 != 0) return 0;
-  const int64_t vpl = row_bytes / 512;
-  return vpl >= 1 && vpl <= 8 ? (int)vpl : 0;
+  const int vpl = vectors_per_lane(dtype, H, D);
+  return vpl >= 1 && vpl <= 8 ? vpl : 0;
 }
 
 }  // namespace

@@ -37,6 +37,20 @@ pe_status fwd_first_token_stream(pe_dtype dtype, int32_t D, const void* q, const
                                  float* lse, float* part, DeviceStatus* status,
                                  cudaStream_t stream);
 
+// First-token query, streaming backward: the same chunks of whole token rows;
+// dk and dv rows are written as they stream, and dq sums of sequences that
+// cross chunk edges are added in chunk order by a second kernel. Delta = dO.O
+// is formed in the kernel. Needs first_token_bwd_stream_partial_bytes() of
+// scratch in `part`; waits and status as in the forward above.
+bool first_token_bwd_stream_supported(pe_dtype dtype, int32_t H, int32_t D);
+size_t first_token_bwd_stream_partial_bytes(int64_t N, int32_t H, int32_t D);
+pe_status bwd_first_token_stream(pe_dtype dtype, int32_t D, const void* q, const void* k,
+                                 const void* v, const void* out, const void* dout,
+                                 const float* lse, const int32_t* cu, int32_t B, int32_t H,
+                                 int64_t N, int32_t S, float scale, Window win, void* dq,
+                                 void* dk, void* dv, float* part, DeviceStatus* status,
+                                 cudaStream_t stream);
+
 // CUDA-core backward; delta is [H, Nq] fp32 scratch.
 pe_status bwd_simt(pe_dtype dtype, int D, const void* q, const void* k, const void* v,
                    const int32_t* cu, int32_t B, int32_t H, int64_t Nq, float scale,
