@@ -76,6 +76,10 @@ def _load():
                                                 ctypes.c_double, ctypes.c_int, i64, i64, dp, dp,
                                                 dp, ctypes.c_int]
         lib.orc_attention_bwd_local.restype = ctypes.c_int
+        lib.orc_attention_bwd_saved.argtypes = [dp, dp, dp, dp, dp, i32p, i64, i64, i64,
+                                                ctypes.c_double, ctypes.c_int, i64, i64, dp, dp,
+                                                dp, ctypes.c_int]
+        lib.orc_attention_bwd_saved.restype = ctypes.c_int
         lib.orc_pack_document_ids.argtypes = [i32p, i64, i64, i64p, i32p, i64p, i64p]
         lib.orc_pack_document_ids.restype = ctypes.c_int
         lib.orc_flatten_packed_metadata.argtypes = [i64p, i32p, i64, i64, i64, i64p, i32p, i64p,
@@ -259,8 +263,15 @@ def attention_fwd_rows(q, k, v, cu_seqlens, scale: float, first_token: bool,
 
 
 def attention_bwd(q, k, v, dout, cu_seqlens, scale: float, first_token: bool = False,
-                  threads: int | None = None, window: tuple[int, int] = (-1, -1)):
-    """Analytic gradients. Returns (dq, dk, dv) in fp64."""
+                  threads: int | None = None, window: tuple[int, int] = (-1, -1),
+                  out=None):
+    """Analytic gradients. Returns (dq, dk, dv) in fp64.
+
+    out: the forward output as the backward op receives it (shaped like q).
+    When given, Delta = dO . out is formed from it as saved (a bf16 output is
+    the exact one rounded), the backward op of page "Source code for
+    gigl.nn.packed_attention" taking the saved output; None forms Delta from
+    the exact fp64 output."""
     lib = _load()
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
@@ -269,8 +280,14 @@ def attention_bwd(q, k, v, dout, cu_seqlens, scale: float, first_token: bool = F
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    rc = lib.orc_attention_bwd_local(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
+    saved = None
+    if out is not None:
+        saved = _f64(out)
+        if saved.shape != q.shape:
+            raise ValueError(f"out shape {saved.shape} != q shape {q.shape}")
+    rc = lib.orc_attention_bwd_saved(_ptr(q, ctypes.c_double), _ptr(k, ctypes.c_double),
                                _ptr(v, ctypes.c_double), _ptr(dout, ctypes.c_double),
+                               None if saved is None else _ptr(saved, ctypes.c_double),
                                _ptr(cu, ctypes.c_int32), b, h, d, float(scale),
                                int(bool(first_token)), int(window[0]), int(window[1]),
                                _ptr(dq, ctypes.c_double),

@@ -427,6 +427,10 @@ int orc_attention_fwd_rows(const double* q, const double* k, const double* v,
 /*   dk_j += scale * dS_rj q_r                                                */
 /*   dv_j += P_rj dO_r                                                        */
 /* Every (sequence, head) writes a disjoint slice of dq, dk, dv.              */
+/* The backward op of page "Source code for gigl.nn.packed_attention"         */
+/* (gigl::varlen_attention_backward) takes the forward's saved output; when   */
+/* that output is given (out != NULL), Dlt_r = dO_r . out_r uses it as saved  */
+/* (in bf16 it is O_r rounded), otherwise the exact O_r above.                */
 /* ------------------------------------------------------------------------- */
 typedef struct {
   const double *q, *k, *v, *dout;
@@ -436,6 +440,7 @@ typedef struct {
   int first_token;
   int64_t wl, wr;
   double *dq, *dk, *dv;
+  const double* out; /* saved output [Nq][H][D] or NULL */
 } orc_bwd_ctx;
 
 static void orc_bwd_task(void* vctx, int64_t item, double* scratch) {
@@ -474,8 +479,9 @@ static void orc_bwd_task(void* vctx, int64_t item, double* scratch) {
       for (int64_t j = 0; j < len; ++j) acc += p[j] * c->v[((start + j) * H + h) * D + c2];
       orow[c2] = acc;
     }
+    const double* ov = c->out ? c->out + (qrow * H + h) * D : orow;
     double delta = 0.0;
-    for (int64_t c2 = 0; c2 < D; ++c2) delta += gv[c2] * orow[c2];
+    for (int64_t c2 = 0; c2 < D; ++c2) delta += gv[c2] * ov[c2];
     double* dqv = c->dq + (qrow * H + h) * D;
     for (int64_t c2 = 0; c2 < D; ++c2) dqv[c2] = 0.0;
     for (int64_t j = 0; j < len; ++j) {
@@ -495,11 +501,11 @@ static void orc_bwd_task(void* vctx, int64_t item, double* scratch) {
   }
 }
 
-int orc_attention_bwd_local(const double* q, const double* k, const double* v,
-                            const double* dout, const int32_t* cu, int64_t B, int64_t H,
-                            int64_t D, double scale, int first_token, int64_t window_left,
-                            int64_t window_right, double* dq, double* dk, double* dv,
-                            int nthreads) {
+int orc_attention_bwd_saved(const double* q, const double* k, const double* v,
+                            const double* dout, const double* out, const int32_t* cu,
+                            int64_t B, int64_t H, int64_t D, double scale, int first_token,
+                            int64_t window_left, int64_t window_right, double* dq, double* dk,
+                            double* dv, int nthreads) {
   int64_t max_len = 0;
   for (int64_t i = 0; i < B; ++i) {
     int64_t len = (int64_t)cu[i + 1] - cu[i];
@@ -507,8 +513,17 @@ int orc_attention_bwd_local(const double* q, const double* k, const double* v,
     if (len > max_len) max_len = len;
   }
   orc_bwd_ctx ctx = {q, k, v, dout, cu, B, H, D, scale, first_token, window_left,
-                     window_right, dq, dk, dv};
+                     window_right, dq, dk, dv, out};
   return orc_run(orc_bwd_task, &ctx, B * H, (size_t)(max_len + D), nthreads);
+}
+
+int orc_attention_bwd_local(const double* q, const double* k, const double* v,
+                            const double* dout, const int32_t* cu, int64_t B, int64_t H,
+                            int64_t D, double scale, int first_token, int64_t window_left,
+                            int64_t window_right, double* dq, double* dk, double* dv,
+                            int nthreads) {
+  return orc_attention_bwd_saved(q, k, v, dout, NULL, cu, B, H, D, scale, first_token,
+                                 window_left, window_right, dq, dk, dv, nthreads);
 }
 
 int orc_attention_bwd(const double* q, const double* k, const double* v, const double* dout,

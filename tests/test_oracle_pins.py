@@ -324,6 +324,47 @@ def test_backward_invariants():
         np.testing.assert_allclose(dv[rows].sum(0), dout[rows].sum(0), atol=1e-12)
 
 
+@pytest.mark.parametrize("first_token", [False, True])
+def test_backward_with_saved_output(first_token):
+    """The backward op takes the forward's saved output, and Delta = dO . O is
+    formed from it. Given the exact output, the gradients are the exact ones;
+    a perturbation E of the saved output moves only the Delta term, by brute
+    force on a tiny case: dq_r -= scale (dO_r . E_r) sum_j P_rj k_j,
+    dk_j -= scale sum_r P_rj (dO_r . E_r) q_r, dv unchanged."""
+    lengths, s, q, k, v = _random_case(72, b_max=5, s_max=9)
+    _, cu, _ = oracle.pack_sequences(lengths, s)
+    rng = np.random.default_rng(73)
+    first = cu[:-1].astype(np.int64)
+    qq = q[first] if first_token else q
+    dout = rng.standard_normal(qq.shape)
+    scale = 0.4
+    out, _ = oracle.attention_fwd(q, k, v, cu, s, scale)
+    out = out[first] if first_token else out
+    exact = oracle.attention_bwd(qq, k, v, dout, cu, scale, first_token=first_token)
+    same = oracle.attention_bwd(qq, k, v, dout, cu, scale, first_token=first_token, out=out)
+    for a, b in zip(exact, same):
+        np.testing.assert_allclose(b, a, atol=1e-12)
+    pert = rng.standard_normal(out.shape) * 1e-2
+    moved = oracle.attention_bwd(qq, k, v, dout, cu, scale, first_token=first_token,
+                                 out=out + pert)
+    want_dq, want_dk = exact[0].copy(), exact[1].copy()
+    for i in range(len(lengths)):
+        a, b = int(cu[i]), int(cu[i + 1])
+        rows = [i] if first_token else list(range(a, b))
+        for r in rows:
+            for h in range(k.shape[1]):
+                logits = scale * np.array([qq[r, h] @ k[j, h] for j in range(a, b)])
+                p = np.exp(logits - logits.max())
+                p /= p.sum()
+                e = float(dout[r, h] @ pert[r, h])
+                want_dq[r, h] -= scale * e * sum(p[t] * k[a + t, h] for t in range(b - a))
+                for t in range(b - a):
+                    want_dk[a + t, h] -= scale * p[t] * e * qq[r, h]
+    np.testing.assert_allclose(moved[0], want_dq, atol=1e-12)
+    np.testing.assert_allclose(moved[1], want_dk, atol=1e-12)
+    np.testing.assert_allclose(moved[2], exact[2], atol=1e-12)
+
+
 # --------------------------------------------------------------------------- local attention
 # Reading of the packed-encoders README's "local-64" mode and FlashAttention's
 # sliding-window pruning: the key at position j is visible from the query at
