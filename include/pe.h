@@ -259,6 +259,14 @@ pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t
  *   otherwise, with max_seq_len > 1024, each (sequence, head) is split into
  *   1024-key chunks. A workspace without that room (but large enough
  *   otherwise) is accepted and runs one CTA per sequence and head.
+ *   For a first-token backward (backward = 1) the reported size likewise
+ *   includes room for per-chunk dq sums when the token row is 512, 1024, ...
+ *   bytes with at most 32 elements per 32-lane slice (bf16 rows up to 2048
+ *   bytes, fp32 rows up to 4096) and head_dim is 32, 64 or 128: the token
+ *   range is then cut into equal chunks, dk and dv rows are written as k and
+ *   v stream through, and sequences crossing chunk edges have their dq sums
+ *   added in chunk order. Without that room the backward runs per sequence
+ *   and head on the CUDA cores.
  * ------------------------------------------------------------------------ */
 size_t pe_attention_workspace_size(pe_dtype dtype, int32_t num_sequences, int64_t num_tokens,
                                    int32_t num_heads, int32_t head_dim, int32_t max_seq_len,
@@ -278,7 +286,8 @@ pe_status pe_packed_attention_fwd(pe_dtype dtype, int32_t num_sequences, int64_t
  *   Delta_r = dO_r . O_r,  dS = P o (dO v^T - Delta),
  *   dq = scale dS k,  dk = scale dS^T q,  dv = P^T dO.
  * Arguments as in the forward; out and lse are that forward's results for
- * the same inputs; dout, dq are shaped like q; dk, dv like k. Every element
+ * the same inputs; dout, dq are shaped like q; dk, dv like k. Delta is formed
+ * from out as passed (a bf16 out is the exact output rounded). Every element
  * of dq, dk, dv is written. The result is bitwise deterministic run to run
  * (no floating-point atomics).
  * ------------------------------------------------------------------------ */
@@ -368,7 +377,10 @@ pe_status pe_geglu(pe_dtype dtype, const void* x, int64_t num_tokens, int32_t fe
  * pe_packed_attention_bwd (backward = 1) runs for these arguments (full
  * attention) on an sm_103a device: "tcgen05_bf16_d64", "tcgen05_bf16_d128",
  * "tcgen05_f32_d64", "simt_ffma", "first_token_gemv", "simt_ffma_bwd",
- * "tcgen05_bf16_d64_bwd", or "unsupported". A static string; never NULL. */
+ * "tcgen05_bf16_d64_bwd", "first_token_bwd", or "unsupported". The two
+ * first-token families cover both of their forms (streaming whole token rows
+ * when the row shape and workspace allow it, per sequence and head
+ * otherwise). A static string; never NULL. */
 const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_first_token,
                                 int backward);
 
