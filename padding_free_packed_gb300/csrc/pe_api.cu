@@ -180,7 +180,7 @@ extern "C" pe_status pe_packed_attention_fwd_local(
   if (dtype == PE_BF16 && D == 64) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_fwd_rows_per_item(),
                             sm103_fwd_pair_heads_rows(win), sm103_fwd_quad_heads_rows(win), plan,
-                            chk, stream));
+                            chk, stream, sm103_fwd_pair_odd_tails(win)));
     return fwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, out, lse, plan, status, stream);
   }
   if (dtype == PE_BF16 && D == 128 && !win.active()) {

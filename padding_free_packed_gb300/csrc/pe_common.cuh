@@ -157,11 +157,15 @@ struct LayoutCheck {
 // in one work item; 0 turns either off). The kernel first checks the layout
 // (LayoutCheck); when the check fails, or when the status word already holds an
 // error (an earlier pass of the same call), the plan has no tiles, so the
-// persistent kernels that consume it claim no work.
+// persistent kernels that consume it claim no work. With pair_odd_tails, a
+// longer sequence whose last item would hold only one of its two half-tiles
+// (ceil(L_i / (rows_per_tile / 2)) odd) has those last half-tiles of two heads
+// share one item: heads * (ceil(L_i / rows_per_tile) - 1) + ceil(heads / 2)
+// tiles.
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
                            int32_t rows_per_tile, int32_t pair_heads_rows,
                            int32_t quad_heads_rows, TilePlan plan, LayoutCheck check,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int32_t pair_odd_tails = 0);
 
 // The same check for calls without a tile plan (first-token queries): writes
 // the whole status word (code 0 when the layout is valid), so it also serves as

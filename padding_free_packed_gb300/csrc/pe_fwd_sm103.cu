@@ -30,7 +30,11 @@
 // head h + t against its own K/V block, and both softmax warpgroups work. A
 // sequence of at most 64 tokens packs two heads into each tile as well (rows
 // 0-63 one head, rows 64-127 the next, loaded as 64-row boxes; each row masks
-// the other head's half of the key columns), so an item takes four heads. With local attention (a window of key positions
+// the other head's half of the key columns), so an item takes four heads. A
+// longer sequence with an odd number of 128-row blocks would end each head
+// with an item of one tile; without a window those last tiles of two heads
+// share an item instead, each tile against its own head's key blocks (which
+// alternate in the K/V ring). With local attention (a window of key positions
 // around each query position) an item visits only the key blocks its rows can
 // see, and the softmax masks each row to its window. Keys past the sequence end are masked to -inf;
 // query rows past it are computed but never stored. TMA zero-fills rows
@@ -75,9 +79,12 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return 384u + 64u * t; }
 constexpr uint32_t kTmemCols = 512;
 
 // Heads of a work item: one (kOneHead), one per tile (kHeadPerTile: tile t runs
-// head + t), or two per tile (kTwoHeadsPerTile: tile t runs head + 2t in rows
-// 0-63 and head + 2t + 1 in rows 64-127).
-enum : int32_t { kOneHead = 0, kHeadPerTile = 1, kTwoHeadsPerTile = 2 };
+// head + t), two per tile (kTwoHeadsPerTile: tile t runs head + 2t in rows
+// 0-63 and head + 2t + 1 in rows 64-127), or the last query tiles of two heads
+// of a longer sequence whose last pair would hold only one tile (kTailPair:
+// tile t runs head + t over query rows pair*256 .., against key blocks of its
+// own head, which alternate with the other tile's in the K/V ring).
+enum : int32_t { kOneHead = 0, kHeadPerTile = 1, kTwoHeadsPerTile = 2, kTailPair = 3 };
 struct Item {
   int32_t seq, head, pair;
   int32_t multi;
@@ -107,6 +114,7 @@ struct FwdParams {
   int32_t B, H;
   int32_t pair_heads_rows;  // sequences up to this long run a head per tile (0: never)
   int32_t quad_heads_rows;  // ... and up to this long two heads per tile (0: never)
+  int32_t pair_odd_tails;   // longer sequences with an odd block count end in kTailPair items
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -121,20 +129,24 @@ struct FwdParams {
 enum WaitSite { kSiteProducer = 1, kSiteMma = 2, kSiteSoftmax = 3 };
 
 // The key blocks of an item: nkv blocks of 128 keys starting at key position
-// kb0, and the blocks [lo[t], hi[t]] that query tile t uses. Without a window
-// that is the whole sequence for both tiles. With one, the blocks start at the
-// first key of the item's window band (TMA rows need no alignment) and each
-// tile uses only the blocks its own rows can see.
+// kb0, and the blocks lo[t], lo[t] + step, ..., hi[t] that query tile t uses.
+// Without a window that is the whole sequence for both tiles. With one, the
+// blocks start at the first key of the item's window band (TMA rows need no
+// alignment) and each tile uses only the blocks its own rows can see. A
+// kTailPair item alternates the two heads' blocks (step 2).
 struct ItemRange {
   int32_t kb0, nkv, lo0, hi0, lo1, hi1;   // (lo0, hi0) for tile 0, (lo1, hi1) for tile 1
+  int32_t step;
   __device__ int32_t lo(int t) const { return t ? lo1 : lo0; }
   __device__ int32_t hi(int t) const { return t ? hi1 : hi0; }
-  __device__ bool uses(int t, int32_t j) const { return j >= lo(t) && j <= hi(t); }
+  __device__ bool uses(int t, int32_t j) const {
+    return j >= lo(t) && j <= hi(t) && (step == 1 || ((j - lo(t)) & 1) == 0);
+  }
 };
 
 // Query tiles of an item.
 __device__ __forceinline__ int item_tiles(const FwdParams& p, const Item& it, int32_t len) {
-  if (it.multi == kHeadPerTile) return 2;
+  if (it.multi == kHeadPerTile || it.multi == kTailPair) return 2;
   if (it.multi == kTwoHeadsPerTile) return p.H - it.head > 2 ? 2 : 1;
   return len - it.pair * kPairRows > kRows ? 2 : 1;
 }
@@ -143,6 +155,18 @@ template <bool kLocal>
 __device__ __forceinline__ ItemRange item_range(const FwdParams& p, int32_t len, int32_t r0,
                                                 int32_t multi, int ntiles) {
   ItemRange ir;
+  ir.step = 1;
+  if (multi == kTailPair) {  // block j: keys 128*(j/2) .. of tile (j & 1)'s head
+    const int32_t nb = (len + kRows - 1) / kRows;
+    ir.kb0 = 0;
+    ir.nkv = 2 * nb;
+    ir.lo0 = 0;
+    ir.hi0 = 2 * nb - 2;
+    ir.lo1 = 1;
+    ir.hi1 = 2 * nb - 1;
+    ir.step = 2;
+    return ir;
+  }
   if (multi != kOneHead) {  // block j holds the keys of tile j's heads and serves it only
     ir.kb0 = 0;
     ir.nkv = ntiles;
@@ -190,6 +214,20 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
     return;
   }
   const int32_t npairs = (len + kPairRows - 1) / kPairRows;
+  if (p.pair_odd_tails && (((len + kRows - 1) / kRows) & 1)) {
+    // The heads' full pairs first, then their last tiles two heads at a time.
+    const int32_t full = npairs - 1;
+    if (local < p.H * full) {
+      it.head = local / full;
+      it.pair = local - it.head * full;
+      it.multi = kOneHead;
+      return;
+    }
+    it.head = 2 * (local - p.H * full);
+    it.pair = full;
+    it.multi = it.head + 1 < p.H ? kTailPair : kOneHead;
+    return;
+  }
   it.head = local / npairs;
   it.pair = local - it.head * npairs;
   it.multi = kOneHead;
@@ -307,6 +345,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               for (int hh = 0; hh < 2; ++hh)
                 tma_load_2d(smem_u32(S.q[tt]) + hh * kHalfTileBytes, &tm_q64, smem_u32(&S.q_full),
                             packed_head(p, it, tt, hh) * kD, start);
+            } else if (it.multi == kTailPair) {  // both tiles: rows r0.., heads head + tt
+              tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full), x + tt * kD,
+                          start + r0);
             } else {
               tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full),
                           it.multi ? x + tt * kD : x, it.multi ? start : start + r0 + tt * kRows);
@@ -321,8 +362,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               break;
             }
             const bool packed = it.multi == kTwoHeadsPerTile;
-            const int32_t kx = it.multi ? x + j * kD : x;
-            const int32_t ky = it.multi ? start : start + ir.kb0 + j * kRows;
+            const bool tail = it.multi == kTailPair;
+            const int32_t kx = tail ? x + (j & 1) * kD : (it.multi ? x + j * kD : x);
+            const int32_t ky = tail ? start + (j >> 1) * kRows
+                                    : (it.multi ? start : start + ir.kb0 + j * kRows);
             mbar_arrive_expect_tx(smem_u32(&S.k_full[s]), kTileBytes);
             if (packed) {
               for (int hh = 0; hh < 2; ++hh)
@@ -500,7 +543,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int ntiles = item_tiles(p, it, len);
       if (t >= ntiles) continue;                 // this tile of the item is empty
       const bool packed = it.multi == kTwoHeadsPerTile;
-      const int32_t r0 = it.multi ? 0 : it.pair * kPairRows + t * kRows;
+      const int32_t r0 = it.multi == kTailPair ? it.pair * kPairRows
+                         : (it.multi ? 0 : it.pair * kPairRows + t * kRows);
       const int32_t head = packed ? it.head + 2 * t + (quarter >> 1)
                                   : (it.multi ? it.head + t : it.head);
       const int32_t pos = packed ? (row & 63) : r0 + row;   // this row's query position
@@ -511,7 +555,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int32_t vis_hi = kLocal ? window_hi(p.win, r0 + row, len) : len - 1;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int32_t j = ir.lo(t); j <= ir.hi(t); ++j) {
+      for (int32_t j = ir.lo(t); j <= ir.hi(t); j += ir.step) {
         const bool first_blk = j == ir.lo(t);
         if (!warp_wait(smem_u32(&S.s_full[t]), s_cnt & 1, abort_flag, p.status, kSiteSoftmax)) {
           ok = false;
@@ -528,7 +572,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&S.s_free[t]));
-        const int32_t kb = it.multi ? 0 : ir.kb0 + j * kRows;  // key position of column coff
+        // Key position of column coff.
+        const int32_t kb = it.multi == kTailPair ? (j >> 1) * kRows
+                                                 : (it.multi ? 0 : ir.kb0 + j * kRows);
         const int32_t kv_valid = len - kb;         // > 0; columns at or past it are masked
         if (kLocal) {
           // Columns outside [vis_lo, vis_hi] (which also ends before len).
@@ -723,6 +769,7 @@ pe_status make_map(CUtensorMap* map, const void* base, int64_t N, int32_t H,
 int sm103_fwd_rows_per_item() { return kPairRows; }
 int sm103_fwd_pair_heads_rows(Window win) { return win.active() ? 0 : kRows; }
 int sm103_fwd_quad_heads_rows(Window win) { return win.active() ? 0 : kRows / 2; }
+int sm103_fwd_pair_odd_tails(Window win) { return win.active() ? 0 : 1; }
 
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
@@ -752,6 +799,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   prm.H = H;
   prm.pair_heads_rows = sm103_fwd_pair_heads_rows(win);
   prm.quad_heads_rows = sm103_fwd_quad_heads_rows(win);
+  prm.pair_odd_tails = sm103_fwd_pair_odd_tails(win);
   prm.scale_log2 = scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;

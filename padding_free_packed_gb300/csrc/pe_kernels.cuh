@@ -66,6 +66,10 @@ int sm103_fwd_rows_per_item();
 int sm103_fwd_pair_heads_rows(Window win);
 // ... and at most this many four heads (two per tile, 64 rows each).
 int sm103_fwd_quad_heads_rows(Window win);
+// 1 when a longer sequence with an odd number of 128-row blocks runs the last
+// query tiles of two heads in one item (the plan's pair_odd_tails); 0 with a
+// window.
+int sm103_fwd_pair_odd_tails(Window win);
 pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* cu, int32_t B,
                     int32_t H, int64_t N, float scale, Window win, void* out, float* lse,
                     TilePlan plan, DeviceStatus* status, cudaStream_t stream);

@@ -221,7 +221,7 @@ constexpr int kPlanBins = 2048;
 __global__ void __launch_bounds__(kScanThreads)
 tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32_t rows_per_tile,
                  int32_t pair_heads_rows, int32_t quad_heads_rows, TilePlan plan,
-                 LayoutCheck chk) {
+                 LayoutCheck chk, int32_t pair_odd_tails) {
   __shared__ int32_t start[kPlanBins];
   __shared__ long long warp_sums[32];
   const int tid = threadIdx.x;
@@ -272,9 +272,12 @@ tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32
     if (pos < B) {
       const int32_t i = plan.order[pos];
       const int32_t len = __ldg(cu + i + 1) - __ldg(cu + i);
+      const long long pairs = ceil_div(len, rows_per_tile);
+      const bool odd_tail = pair_odd_tails && (ceil_div(len, rows_per_tile / 2) & 1);
       tiles = len <= quad_heads_rows   ? (long long)(heads + 3) / 4
               : len <= pair_heads_rows ? (long long)(heads + 1) / 2
-                                       : (long long)heads * ceil_div(len, rows_per_tile);
+              : odd_tail               ? (long long)heads * (pairs - 1) + (heads + 1) / 2
+                                       : (long long)heads * pairs;
     }
     long long total;
     const long long incl = block_inclusive_scan(tiles, warp_sums, total);
@@ -292,11 +295,12 @@ tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32
 pe_status launch_tile_plan(const int32_t* cu_seqlens, int32_t B, int32_t heads,
                            int32_t rows_per_tile, int32_t pair_heads_rows,
                            int32_t quad_heads_rows, TilePlan plan, LayoutCheck check,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int32_t pair_odd_tails) {
   static_assert(kPlanBins == 2 * kScanThreads, "plan scan covers two bins per thread");
   if (!check.status) return PE_ERR_INVALID_ARG;
   tile_plan_kernel<<<1, kScanThreads, 0, stream>>>(cu_seqlens, B, heads, rows_per_tile,
-                                                   pair_heads_rows, quad_heads_rows, plan, check);
+                                                   pair_heads_rows, quad_heads_rows, plan, check,
+                                                   pair_odd_tails);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -264,3 +264,23 @@ def test_first_token_split_over_key_chunks(dtype):
                                          query_is_first_token=True, workspace=small)
     check(out2[torch.arange(len(lengths)).repeat_interleave(3), torch.from_numpy(heads).to(DEV)],
           ref, tag, "first-token single pass")
+
+
+@pytest.mark.parametrize("heads", [4, 5, 6])
+def test_odd_block_tails_share_items_across_heads(heads):
+    """A sequence of an odd number of 128-row blocks (above 128 tokens) ends in
+    one query tile per head; the tensor-core forward runs those last tiles of
+    two heads in one work item, each against its own head's keys (the last
+    head alone when the head count is odd). Lengths put the tail at every
+    offset in its block, next to even-block sequences."""
+    lengths = [257, 300, 383, 384, 640, 641, 700, 896, 1100, 1152, 129, 256, 512, 1000, 2000]
+    x = workloads.make_custom(lengths, heads, 64, torch.bfloat16, seed=37)
+    s = max(lengths)
+    cu, cu_d, q, k, v = _device_inputs(x)
+    ws = torch.empty(pe.attention_workspace_bytes(torch.bfloat16, len(lengths), q.shape[0], heads,
+                                                  64, s), dtype=torch.uint8, device=DEV)
+    out, lse = pe.pe_packed_attention_fwd(q, k, v, cu_d, s, 0.125, need_lse=True, workspace=ws)
+    assert pe.pe_read_device_status(ws) == 0
+    ref, ref_lse = oracle.attention_fwd(x.q, x.k, x.v, cu, s, 0.125)
+    check(out, ref, "bf16", f"odd-block tails, {heads} heads")
+    assert float(np.abs(to64(lse) - ref_lse).max()) <= 2e-3
