@@ -186,7 +186,7 @@ extern "C" pe_status pe_packed_attention_fwd_local(
   if (dtype == PE_BF16 && D == 128 && !win.active()) {
     PE_TRY(launch_tile_plan(cu_seqlens, B, H, sm103_d128_fwd_rows_per_item(),
                             sm103_d128_fwd_pair_heads_rows(), sm103_d128_fwd_quad_heads_rows(),
-                            plan, chk, stream));
+                            plan, chk, stream, sm103_d128_fwd_pair_odd_tails()));
     return fwd_sm103_d128(q, k, v, cu_seqlens, B, H, N, scale, out, lse, plan, status, stream);
   }
   if (dtype == PE_FP32 && D == 64 && !win.active()) {

@@ -60,7 +60,10 @@ __host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }   // P 
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 constexpr uint32_t kTmemCols = 512;
 
-enum : int32_t { kOneHead = 0, kHeadPerTile = 1, kTwoHeadsPerTile = 2 };
+// kTailPair: the last query tiles of two heads of a longer sequence with an
+// odd number of 128-row blocks; tile t runs head + t against its own head's
+// key blocks, which alternate with the other tile's in the K/V ring.
+enum : int32_t { kOneHead = 0, kHeadPerTile = 1, kTwoHeadsPerTile = 2, kTailPair = 3 };
 struct Item {
   int32_t seq, head, pair;
   int32_t multi;
@@ -88,6 +91,7 @@ struct FwdParams {
   int32_t B, H;
   int32_t pair_heads_rows;
   int32_t quad_heads_rows;
+  int32_t pair_odd_tails;
   float scale_log2;
   __nv_bfloat16* out;
   float* lse;
@@ -100,15 +104,24 @@ struct FwdParams {
 enum WaitSite { kSiteProducer = 41, kSiteMma = 42, kSiteSoftmax = 43 };
 
 __device__ __forceinline__ int item_tiles(const FwdParams& p, const Item& it, int32_t len) {
-  if (it.multi == kHeadPerTile) return 2;
+  if (it.multi == kHeadPerTile || it.multi == kTailPair) return 2;
   if (it.multi == kTwoHeadsPerTile) return p.H - it.head > 2 ? 2 : 1;
   return len - it.pair * kPairRows > kRows ? 2 : 1;
 }
 
 // Key blocks of an item: the whole sequence, or for multi-head items one block
-// per tile (block t holds tile t's heads and serves only tile t).
+// per tile (block t holds tile t's heads and serves only tile t), or for a
+// kTailPair item both heads' blocks alternating (block j: head + (j & 1), keys
+// 128 * (j / 2) ..).
 __device__ __forceinline__ int32_t item_blocks(const Item& it, int32_t len, int ntiles) {
+  if (it.multi == kTailPair) return 2 * ((len + kRows - 1) / kRows);
   return it.multi ? ntiles : (len + kRows - 1) / kRows;
+}
+
+// Blocks first(t), first(t) + step, ..., last(t) of the item serve tile t.
+__device__ __forceinline__ bool tile_uses(const Item& it, int t, int32_t j) {
+  if (it.multi == kTailPair) return (j & 1) == t;
+  return it.multi ? j == t : true;
 }
 
 __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item& it) {
@@ -128,6 +141,20 @@ __device__ __forceinline__ void decode_item(const FwdParams& p, int32_t t, Item&
     return;
   }
   const int32_t npairs = (len + kPairRows - 1) / kPairRows;
+  if (p.pair_odd_tails && (((len + kRows - 1) / kRows) & 1)) {
+    // The heads' full pairs first, then their last tiles two heads at a time.
+    const int32_t full = npairs - 1;
+    if (local < p.H * full) {
+      it.head = local / full;
+      it.pair = local - it.head * full;
+      it.multi = kOneHead;
+      return;
+    }
+    it.head = 2 * (local - p.H * full);
+    it.pair = full;
+    it.multi = it.head + 1 < p.H ? kTailPair : kOneHead;
+    return;
+  }
   it.head = local / npairs;
   it.pair = local - it.head * npairs;
   it.multi = kOneHead;
@@ -245,16 +272,19 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             break;
           }
           mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
+          const bool tail = it.multi == kTailPair;
           for (int tt = 0; tt < ntiles; ++tt)
             load_tile(smem_u32(S.q[tt]), &tm_q, &tm_q64, smem_u32(&S.q_full), packed,
-                      it.multi ? x + tt * kD : x, it.multi ? start : start + r0 + tt * kRows,
+                      it.multi ? x + tt * kD : x,
+                      tail ? start + r0 : (it.multi ? start : start + r0 + tt * kRows),
                       packed_head(p, it, tt, 0) * kD, packed_head(p, it, tt, 1) * kD);
           pending_q = item_no & 1;
           for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
             const int s = kv_no % kStages;
             const uint32_t ph = (kv_no / kStages) & 1;
-            const int32_t kx = it.multi ? x + j * kD : x;
-            const int32_t ky = it.multi ? start : start + j * kRows;
+            const int32_t kx = tail ? x + (j & 1) * kD : (it.multi ? x + j * kD : x);
+            const int32_t ky = tail ? start + (j >> 1) * kRows
+                                    : (it.multi ? start : start + j * kRows);
             const int32_t xa = packed_head(p, it, j, 0) * kD, xb = packed_head(p, it, j, 1) * kD;
             if (!mbar_wait(smem_u32(&S.k_empty[s]), ph ^ 1, abort_flag, p.status, kSiteProducer)) {
               ok = false;
@@ -313,7 +343,7 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
           const uint32_t k_addr = smem_u32(S.k[s]);
           for (int t = 0; t < ntiles; ++t) {
-            if (it.multi && j != t) continue;
+            if (!tile_uses(it, t, j)) continue;
             if (n_qk[t] > 0 && !warp_wait(smem_u32(&S.pv_done[t]), (n_qk[t] - 1) & 1, abort_flag,
                                           p.status, kSiteMma)) {
               ok = false;
@@ -356,7 +386,9 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int32_t len = __ldg(p.cu + it.seq + 1) - __ldg(p.cu + it.seq);
         const int ntiles = item_tiles(p, it, len);
         const int32_t nkv = item_blocks(it, len, ntiles);
-        const int32_t first = it.multi ? t : 0, last = it.multi ? t : nkv - 1;
+        const bool tail = it.multi == kTailPair;
+        const int32_t first = it.multi ? t : 0;
+        const int32_t last = tail ? nkv - 2 + t : (it.multi ? t : nkv - 1);
         for (int32_t j = 0; j < nkv; ++j) {
           const uint32_t c = kv_no + j;
           const int s = c % kStages;
@@ -365,7 +397,7 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ok = false;
             break;
           }
-          if (t >= ntiles || j < first || j > last) {
+          if (t >= ntiles || !tile_uses(it, t, j)) {
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&S.v_empty[s]));
             continue;
@@ -416,16 +448,18 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int ntiles = item_tiles(p, it, len);
       if (t >= ntiles) continue;
       const bool packed = it.multi == kTwoHeadsPerTile;
-      const int32_t r0 = it.multi ? 0 : it.pair * kPairRows + t * kRows;
+      const bool tail = it.multi == kTailPair;
+      const int32_t r0 = tail ? it.pair * kPairRows : (it.multi ? 0 : it.pair * kPairRows + t * kRows);
       const int32_t head = packed ? it.head + 2 * t + (quarter >> 1)
                                   : (it.multi ? it.head + t : it.head);
       const int32_t pos = packed ? (row & 63) : r0 + row;
       const int32_t coff = packed ? (quarter >> 1) * 64 : 0;
       const int32_t nkv = item_blocks(it, len, ntiles);
-      const int32_t first = it.multi ? t : 0, last = it.multi ? t : nkv - 1;
+      const int32_t first = it.multi ? t : 0;
+      const int32_t last = tail ? nkv - 2 + t : (it.multi ? t : nkv - 1);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int32_t j = first; j <= last; ++j) {
+      for (int32_t j = first; j <= last; j += tail ? 2 : 1) {
         const bool first_blk = j == first;
         if (!warp_wait(smem_u32(&S.s_full[t]), s_cnt & 1, abort_flag, p.status, kSiteSoftmax)) {
           ok = false;
@@ -438,7 +472,7 @@ fwd_sm103_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + col_s(t) + 32 * c, sr[c]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
-        const int32_t kb = it.multi ? 0 : j * kRows;
+        const int32_t kb = tail ? (j >> 1) * kRows : (it.multi ? 0 : j * kRows);
         const int32_t kv_valid = len - kb;
         if (kv_valid < kRows) {
 #pragma unroll
@@ -606,6 +640,7 @@ pe_status make_map_d128(CUtensorMap* map, const void* base, int64_t N, int32_t H
 int sm103_d128_fwd_rows_per_item() { return kPairRows; }
 int sm103_d128_fwd_pair_heads_rows() { return kRows; }
 int sm103_d128_fwd_quad_heads_rows() { return kRows / 2; }
+int sm103_d128_fwd_pair_odd_tails() { return 1; }
 
 pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int32_t* cu,
                          int32_t B, int32_t H, int64_t N, float scale, void* out, float* lse,
@@ -633,6 +668,7 @@ pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int3
   prm.H = H;
   prm.pair_heads_rows = sm103_d128_fwd_pair_heads_rows();
   prm.quad_heads_rows = sm103_d128_fwd_quad_heads_rows();
+  prm.pair_odd_tails = sm103_d128_fwd_pair_odd_tails();
   prm.scale_log2 = scale * kLog2e;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.lse = lse;

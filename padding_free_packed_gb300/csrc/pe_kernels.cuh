@@ -90,6 +90,7 @@ pe_status fwd_sm103_f32(const void* q, const void* k, const void* v, const int32
 int sm103_d128_fwd_rows_per_item();
 int sm103_d128_fwd_pair_heads_rows();
 int sm103_d128_fwd_quad_heads_rows();
+int sm103_d128_fwd_pair_odd_tails();   // as sm103_fwd_pair_odd_tails, full attention only
 pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int32_t* cu,
                          int32_t B, int32_t H, int64_t N, float scale, void* out, float* lse,
                          TilePlan plan, DeviceStatus* status, cudaStream_t stream);
