@@ -253,6 +253,11 @@ extern "C" pe_status pe_packed_attention_bwd_local(
     return bwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, lse, dout, delta, dq, dk, dv,
                      plan, chk, stream);
   }
+  if (dtype == PE_BF16 && D == 128 && !query_is_first_token && !win.active()) {
+    PE_TRY(bwd_preprocess(dtype, D, out, dout, N, H, delta, stream));
+    return bwd_sm103_d128(q, k, v, cu_seqlens, B, H, N, scale, lse, dout, delta, dq, dk, dv,
+                          plan, chk, stream);
+  }
   return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, win, out,
                   lse, dout, dq, dk, dv, delta, plan, chk, stream);
 }
@@ -276,7 +281,9 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
   if (backward) {
     if (query_is_first_token)
       return (D == 32 || D == 64 || D == 128) ? "first_token_bwd" : "simt_ffma_bwd";
-    return (dtype == PE_BF16 && D == 64) ? "tcgen05_bf16_d64_bwd" : "simt_ffma_bwd";
+    if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64_bwd";
+    if (dtype == PE_BF16 && D == 128) return "tcgen05_bf16_d128_bwd";
+    return "simt_ffma_bwd";
   }
   if (query_is_first_token) return first_token_supported(D) ? "first_token_gemv" : "unsupported";
   if (dtype == PE_BF16 && D == 64) return "tcgen05_bf16_d64";

@@ -49,22 +49,24 @@ __global__ void bwd_preprocess_kernel(const T* __restrict__ out, const T* __rest
 
 }  // namespace
 
-// Delta for bf16 rows of 64: 8 lanes per (row, head), each reading 16 bytes of
-// O and of dO, four rows per warp per step; the row loop is warp-uniform so
-// the group reduction always sees all 32 lanes.
-__global__ void bwd_preprocess_bf16_d64_kernel(const __nv_bfloat16* __restrict__ out,
-                                               const __nv_bfloat16* __restrict__ dout, int64_t Nq,
-                                               int32_t H, float* __restrict__ delta) {
-  const int lane = threadIdx.x & 31, group = lane >> 3, sub = lane & 7;
+// Delta for bf16 rows of D (64 or 128): D/8 lanes per (row, head), each
+// reading 16 bytes of O and of dO, 256/D rows per warp per step; the row loop
+// is warp-uniform so the group reduction always sees all 32 lanes.
+template <int D>
+__global__ void bwd_preprocess_bf16_kernel(const __nv_bfloat16* __restrict__ out,
+                                           const __nv_bfloat16* __restrict__ dout, int64_t Nq,
+                                           int32_t H, float* __restrict__ delta) {
+  constexpr int kLanes = D / 8, kRowsPerWarp = 32 / kLanes;
+  const int lane = threadIdx.x & 31, group = lane / kLanes, sub = lane % kLanes;
   const int64_t rows = Nq * H;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4;
-       base < rows; base += warps * 4) {
+  for (int64_t base = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerWarp;
+       base < rows; base += warps * kRowsPerWarp) {
     const int64_t w = base + group;
     float acc = 0.f;
     if (w < rows) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + w * 64) + sub);
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + w * 64) + sub);
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + w * D) + sub);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + w * D) + sub);
       const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
       const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
@@ -75,7 +77,7 @@ __global__ void bwd_preprocess_bf16_d64_kernel(const __nv_bfloat16* __restrict__
       }
     }
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    for (int off = 1; off < kLanes; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (w < rows && sub == 0) {
       const int64_t r = w / H;
       const int32_t h = (int32_t)(w - r * H);
@@ -86,14 +88,18 @@ __global__ void bwd_preprocess_bf16_d64_kernel(const __nv_bfloat16* __restrict__
 
 pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dout, int64_t Nq,
                          int32_t H, float* delta, cudaStream_t stream) {
-  int64_t blocks = ceil_div(Nq * H, 32);  // 8 warps x 4 rows per block
+  if (dtype != PE_BF16 || (D != 64 && D != 128)) return PE_ERR_UNSUPPORTED;
+  const int64_t rows_per_block = 8 * (256 / D);  // 8 warps
+  int64_t blocks = ceil_div(Nq * H, rows_per_block);
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks <= 0) return PE_OK;
-  if (dtype != PE_BF16 || D != 64) return PE_ERR_UNSUPPORTED;
-  bwd_preprocess_bf16_d64_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), Nq, H,
-      delta);
+  const auto* o = static_cast<const __nv_bfloat16*>(out);
+  const auto* g = static_cast<const __nv_bfloat16*>(dout);
+  if (D == 64)
+    bwd_preprocess_bf16_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(o, g, Nq, H, delta);
+  else
+    bwd_preprocess_bf16_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(o, g, Nq, H, delta);
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -95,7 +95,7 @@ pe_status fwd_sm103_d128(const void* q, const void* k, const void* v, const int3
                          int32_t B, int32_t H, int64_t N, float scale, void* out, float* lse,
                          TilePlan plan, DeviceStatus* status, cudaStream_t stream);
 
-// Delta[h, r] = dO_r . O_r (bf16, head_dim 64) into [H, Nq] fp32.
+// Delta[h, r] = dO_r . O_r (bf16, head_dim 64 or 128) into [H, Nq] fp32.
 pe_status bwd_preprocess(pe_dtype dtype, int D, const void* out, const void* dout, int64_t Nq,
                          int32_t H, float* delta, cudaStream_t stream);
 
@@ -106,5 +106,11 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     const void* dout,
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
                     LayoutCheck check, cudaStream_t stream);
+// The same two passes for head_dim 128, full attention; each key-pass item
+// accumulates one 64-column half of dK and dV.
+pe_status bwd_sm103_d128(const void* q, const void* k, const void* v, const int32_t* cu,
+                         int32_t B, int32_t H, int64_t N, float scale, const float* lse,
+                         const void* dout, const float* delta, void* dq, void* dk, void* dv,
+                         TilePlan plan, LayoutCheck check, cudaStream_t stream);
 
 }  // namespace pe
