@@ -243,9 +243,10 @@ pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t
  * scale: finite and > 0 (1/sqrt(D) is the pages' default).
  * head_dim: a multiple of 8 (the module docstring's "Constraints" require
  *   it for the aligned kernels), at most 128. Full attention runs on the
- *   tcgen05 tensor cores for bf16 with head_dim 64 or 128 and for fp32 with
- *   head_dim 64 (fp32 operands split into bf16 hi and lo parts, three
- *   products each, fp32 accumulation); other shapes run on the CUDA cores.
+ *   tcgen05 tensor cores for bf16 with head_dim 64 or 128 (forward and
+ *   backward) and for fp32 with head_dim 64 (forward; fp32 operands split
+ *   into bf16 hi and lo parts, three products each, fp32 accumulation);
+ *   other shapes run on the CUDA cores.
  * All tensor pointers 16-byte aligned.
  * workspace: device, >= pe_attention_workspace_size(...) bytes. Its first 4
  *   bytes receive a device-side status (PE_OK, PE_ERR_BAD_LENGTH or
