@@ -44,6 +44,16 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Programmatic dependent launch (a kernel launched with
+// launch_after_previous): griddep_wait blocks until the previous kernel in
+// the stream has completed and its writes are visible (at once for a kernel
+// launched without it); griddep_launch_dependents lets the next such kernel
+// be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -196,6 +206,26 @@ inline size_t first_token_partial_bytes(int32_t B, int32_t H, int32_t D, int32_t
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// Launches `kernel` so that it may be scheduled while the previous kernel in
+// the stream is still running (programmatic stream serialisation); the kernel
+// must call griddep_wait() before it reads anything that kernel wrote.
+template <typename... KArgs, typename... Args>
+pe_status launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, args...) != cudaSuccess) return PE_ERR_CUDA;
+  return PE_OK;
+}
 // True if the current device is compute capability 10.3.
 bool device_is_sm103();
 

@@ -70,6 +70,10 @@ first_token_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t c0 = (int64_t)blockIdx.x * chunk;
   const int64_t c1 = min(N, c0 + chunk);
+  // Launched behind the layout check: nothing it wrote (the status word) is
+  // read before it has finished. The merge kernel may be scheduled meanwhile.
+  griddep_wait();
+  griddep_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStStages; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -218,6 +222,7 @@ __global__ void first_token_stream_merge_kernel(const float* __restrict__ part,
                                                 int32_t H, int32_t chunk, int32_t key_limit,
                                                 T* __restrict__ out, float* __restrict__ lse,
                                                 const DeviceStatus* __restrict__ status) {
+  griddep_wait();  // launched behind the streaming kernel: its partials are complete
   // An invalid layout or a streaming kernel that gave up: nothing to combine.
   if (status->code != PE_OK) return;
   constexpr int kU = 16;
@@ -294,17 +299,18 @@ pe_status launch_stream(const void* q, const void* k, const void* v, const int32
   chunk = (int32_t)max((int64_t)chunk,
                        ceil_div(N, (int64_t)device_sm_count() * Sh::kMinBlocks));
   const int64_t blocks = ceil_div(N, chunk);
-  kernel<<<(unsigned)blocks, kStBlock, Sh::kSmem, stream>>>(
-      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), cu, B, N,
-      chunk, scale * kLog2e, key_limit, static_cast<T*>(out), lse, part, status,
-      wait_limit_ns());
-  PE_CUDA_TRY(cudaGetLastError());
+  PE_TRY(launch_after_previous(kernel, dim3((unsigned)blocks), dim3(kStBlock), Sh::kSmem, stream,
+                               static_cast<const T*>(q), static_cast<const T*>(k),
+                               static_cast<const T*>(v), cu, B, N, chunk, scale * kLog2e,
+                               key_limit, static_cast<T*>(out), lse, part, status,
+                               wait_limit_ns()));
   int64_t mblocks = ceil_div((int64_t)B * H, 8);
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (mblocks > cap) mblocks = cap;
-  first_token_stream_merge_kernel<T, D><<<(unsigned)mblocks, 256, 0, stream>>>(
-      part, cu, B, H, chunk, key_limit, static_cast<T*>(out), lse, status);
-  PE_CUDA_TRY(cudaGetLastError());
+  PE_TRY(launch_after_previous(first_token_stream_merge_kernel<T, D>, dim3((unsigned)mblocks),
+                               dim3(256), 0, stream, static_cast<const float*>(part), cu, B, H,
+                               chunk, key_limit, static_cast<T*>(out), lse,
+                               static_cast<const DeviceStatus*>(status)));
   return PE_OK;
 }
 

@@ -204,6 +204,7 @@ __device__ int32_t check_layout_cta(const int32_t* __restrict__ cu, int32_t B,
 
 __global__ void __launch_bounds__(kScanThreads)
 layout_check_kernel(const int32_t* __restrict__ cu, int32_t B, LayoutCheck chk) {
+  griddep_launch_dependents();  // the next kernel may be scheduled; it waits for this one
   int32_t detail;
   const int32_t code = check_layout_cta(cu, B, chk, &detail);
   if (threadIdx.x == 0) {
