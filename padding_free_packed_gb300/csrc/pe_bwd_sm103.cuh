@@ -215,6 +215,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = __shfl_sync(0xffffffffu, S.tmem_base, 0);
+  // Launched behind the tile plan: read it (and the status word) only once
+  // that kernel has finished.
+  griddep_wait();
   const int32_t total = *p.plan.total_tiles;
 
   // Every role walks the same item sequence through the two-slot ring.
@@ -785,8 +788,8 @@ pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, LayoutChe
   // The key pass counts each head once per half of the head dimension.
   PE_TRY(launch_tile_plan(prm.cu, prm.B, kKeyPass ? prm.H * Cfg<D>::kHalves : prm.H, kRows,
                           prm.pair_heads_rows, 0, prm.plan, check, stream));
-  kernel<<<device_sm_count(), kThreads, smem, stream>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6],
-                                                        m[7], mo1, mo2, prm);
+  PE_TRY(launch_after_previous(kernel, dim3(device_sm_count()), dim3(kThreads), smem, stream,
+                               m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], mo1, mo2, prm));
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -250,6 +250,9 @@ fwd_sm103_f32_kernel(const __grid_constant__ CUtensorMap tm_q,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = __shfl_sync(0xffffffffu, S.tmem_base, 0);
+  // Launched behind the tile plan: read it (and the status word) only once
+  // that kernel has finished.
+  griddep_wait();
   const int32_t total = *p.plan.total_tiles;
 
   if (warp < 4) {
@@ -755,8 +758,8 @@ pe_status fwd_sm103_f32(const void* q, const void* k, const void* v, const int32
   prm.plan = plan;
   prm.status = status;
   prm.wait_limit_ns = wait_limit_ns();
-  fwd_sm103_f32_kernel<<<device_sm_count(), kThreads, smem, stream>>>(mq, mk, mv, mq64, mk64,
-                                                                      mv64, prm);
+  PE_TRY(launch_after_previous(fwd_sm103_f32_kernel, dim3(device_sm_count()), dim3(kThreads),
+                               smem, stream, mq, mk, mv, mq64, mk64, mv64, prm));
   PE_CUDA_TRY(cudaGetLastError());
   return PE_OK;
 }

@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kScanThreads)
 tile_plan_kernel(const int32_t* __restrict__ cu, int32_t B, int32_t heads, int32_t rows_per_tile,
                  int32_t pair_heads_rows, int32_t quad_heads_rows, TilePlan plan,
                  LayoutCheck chk, int32_t pair_odd_tails) {
+  griddep_launch_dependents();  // the kernel that consumes the plan waits for it on the device
   __shared__ int32_t start[kPlanBins];
   __shared__ long long warp_sums[32];
   const int tid = threadIdx.x;
