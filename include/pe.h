@@ -262,8 +262,8 @@ pe_status pe_flatten_packed_metadata(const int64_t* token_indices, const int32_t
  *   otherwise) is accepted and runs one CTA per sequence and head.
  *   For a first-token backward (backward = 1) the reported size likewise
  *   includes room for per-chunk dq sums when the token row is 512, 1024, ...
- *   bytes with at most 32 elements per 32-lane slice (bf16 rows up to 2048
- *   bytes, fp32 rows up to 4096) and head_dim is 32, 64 or 128: the token
+ *   bytes (bf16 rows up to 3072 bytes, fp32 rows up to 4096) and head_dim
+ *   is 32, 64 or 128: the token
  *   range is then cut into equal chunks, dk and dv rows are written as k and
  *   v stream through, and sequences crossing chunk edges have their dq sums
  *   added in chunk order. Without that room the backward runs per sequence

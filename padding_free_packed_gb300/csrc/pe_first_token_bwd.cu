@@ -31,9 +31,10 @@
 // first_token_bwd_merge_kernel adds in chunk order. No atomics: the results
 // are bitwise reproducible.
 //
-// Supported when a token row is a whole number of 512-byte warp loads with at
-// most 32 elements per lane (bf16 rows up to 2048 bytes, fp32 rows up to 4096)
-// and D is 32, 64 or 128; other shapes run the CUDA-core backward.
+// Supported when a token row is a whole number of 512-byte warp loads (bf16
+// rows up to 3072 bytes, fp32 rows up to 4096: at most 48 and 32 elements per
+// lane, which the one-CTA-per-SM register budget holds without spilling) and
+// D is 32, 64 or 128; other shapes run the CUDA-core backward.
 #include "pe_kernels.cuh"
 #include "pe_token_stream.cuh"
 
@@ -52,7 +53,7 @@ struct BwdShape : Shape<T, D, VPL> {
   // 168 would spill.
   static constexpr int kMinBlocks = VPL * Base::kEPV <= 24 ? 2 : 1;
   static constexpr size_t kSmem = Base::kRingBytes + (size_t)kWarps * Base::kRow * sizeof(float);
-  static_assert(VPL * Base::kEPV <= 32, "at most 32 elements of a row per lane");
+  static_assert(VPL * Base::kEPV <= 48, "at most 48 elements of a row per lane");
 };
 
 template <typename T, int D, int VPL>
@@ -67,6 +68,7 @@ first_token_bwd_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
                               uint64_t wait_limit_ns) {
   using Sh = BwdShape<T, D, VPL>;
   constexpr int EPV = Sh::kEPV, LPH = Sh::kLPH, ROW = Sh::kRow, R = Sh::kRows;
+  constexpr int kUGroup = VPL < 4 ? VPL : 4;
   extern __shared__ __align__(128) unsigned char bw_smem[];
   T* ks = reinterpret_cast<T*>(bw_smem);                     // [stages][R][ROW]
   T* vs = ks + kStages * Sh::kStageElems;                    // [stages][R][ROW]
@@ -162,52 +164,63 @@ first_token_bwd_stream_kernel(const T* __restrict__ q, const T* __restrict__ k,
       const T* kst = ks + s * Sh::kStageElems;
       const T* vst = vs + s * Sh::kStageElems;
       for (int r = warp; r < nr; r += kWarps) {
-        float sc[VPL], dp[VPL];
-#pragma unroll
-        for (int u = 0; u < VPL; ++u) {
-          const int col = (u * 32 + lane) * EPV;
-          float kx[EPV], vx[EPV], qx[EPV], dx[EPV];
-          unpack16<T>(*reinterpret_cast<const uint4*>(kst + r * ROW + col), kx);
-          unpack16<T>(*reinterpret_cast<const uint4*>(vst + r * ROW + col), vx);
-          unpack16<T>(qp[u], qx);
-          unpack16<T>(dop[u], dx);
-          float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            s1 = fmaf(qx[e], kx[e], s1);
-            s2 = fmaf(dx[e], vx[e], s2);
-          }
-          sc[u] = s1;
-          dp[u] = s2;
-        }
-#pragma unroll
-        for (int x = 1; x < LPH; x <<= 1) {
-#pragma unroll
-          for (int u = 0; u < VPL; ++u) {
-            sc[u] += __shfl_xor_sync(0xffffffffu, sc[u], x);
-            dp[u] += __shfl_xor_sync(0xffffffffu, dp[u], x);
-          }
-        }
         T* dkr = dk + (r0 + r) * ROW;
         T* dvr = dv + (r0 + r) * ROW;
+        // The row's vectors in groups of at most four (each vector's heads
+        // reduce on their own), so that wide rows keep few values live
+        // across the reductions.
 #pragma unroll
-        for (int u = 0; u < VPL; ++u) {
-          const int col = (u * 32 + lane) * EPV;
-          const float p = ex2(fmaf(sc[u], scale_log2, -lse2[u]));
-          const float ds = p * (dp[u] - delta[u]);
-          const float dss = ds * scale;
-          float kx[EPV], qx[EPV], dx[EPV], gv[EPV], gk[EPV];
-          unpack16<T>(*reinterpret_cast<const uint4*>(kst + r * ROW + col), kx);
-          unpack16<T>(qp[u], qx);
-          unpack16<T>(dop[u], dx);
+        for (int ub = 0; ub < VPL; ub += kUGroup) {
+          float sc[kUGroup], dp[kUGroup];
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            gv[e] = p * dx[e];
-            gk[e] = dss * qx[e];
-            acc[u][e] = fmaf(ds, kx[e], acc[u][e]);
+          for (int uu = 0; uu < kUGroup; ++uu) {
+            const int u = ub + uu;
+            if (u >= VPL) break;
+            const int col = (u * 32 + lane) * EPV;
+            float kx[EPV], vx[EPV], qx[EPV], dx[EPV];
+            unpack16<T>(*reinterpret_cast<const uint4*>(kst + r * ROW + col), kx);
+            unpack16<T>(*reinterpret_cast<const uint4*>(vst + r * ROW + col), vx);
+            unpack16<T>(qp[u], qx);
+            unpack16<T>(dop[u], dx);
+            float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              s1 = fmaf(qx[e], kx[e], s1);
+              s2 = fmaf(dx[e], vx[e], s2);
+            }
+            sc[uu] = s1;
+            dp[uu] = s2;
           }
-          store16(dvr + col, pack16<T>(gv));
-          store16(dkr + col, pack16<T>(gk));
+#pragma unroll
+          for (int x = 1; x < LPH; x <<= 1) {
+#pragma unroll
+            for (int uu = 0; uu < kUGroup; ++uu) {
+              if (ub + uu >= VPL) break;
+              sc[uu] += __shfl_xor_sync(0xffffffffu, sc[uu], x);
+              dp[uu] += __shfl_xor_sync(0xffffffffu, dp[uu], x);
+            }
+          }
+#pragma unroll
+          for (int uu = 0; uu < kUGroup; ++uu) {
+            const int u = ub + uu;
+            if (u >= VPL) break;
+            const int col = (u * 32 + lane) * EPV;
+            const float p = ex2(fmaf(sc[uu], scale_log2, -lse2[u]));
+            const float ds = p * (dp[uu] - delta[u]);
+            const float dss = ds * scale;
+            float kx[EPV], qx[EPV], dx[EPV], gv[EPV], gk[EPV];
+            unpack16<T>(*reinterpret_cast<const uint4*>(kst + r * ROW + col), kx);
+            unpack16<T>(qp[u], qx);
+            unpack16<T>(dop[u], dx);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+              gv[e] = p * dx[e];
+              gk[e] = dss * qx[e];
+              acc[u][e] = fmaf(ds, kx[e], acc[u][e]);
+            }
+            store16(dvr + col, pack16<T>(gv));
+            store16(dkr + col, pack16<T>(gk));
+          }
         }
       }
       __syncwarp();
@@ -318,7 +331,7 @@ pe_status dispatch_vpl(int vpl, const void* q, const void* k, const void* v, con
                        int32_t H, int64_t N, int32_t chunk, float scale, int32_t key_limit,
                        void* dq, void* dk, void* dv, float* part, DeviceStatus* status,
                        cudaStream_t stream) {
-  constexpr int kMaxVpl = sizeof(T) == 4 ? 8 : 4;
+  constexpr int kMaxVpl = sizeof(T) == 4 ? 8 : 6;
   switch (vpl) {
 #define PE_CASE(n)                                                                          \
   case n:                                                                                   \
@@ -351,7 +364,7 @@ pe_status dispatch_d(int D, int vpl, const void* q, const void* k, const void* v
 
 int bwd_vectors_per_lane(pe_dtype dtype, int32_t H, int32_t D) {
   const int vpl = vectors_per_lane(dtype, H, D);
-  return vpl >= 1 && vpl <= (dtype == PE_FP32 ? 8 : 4) ? vpl : 0;
+  return vpl >= 1 && vpl <= (dtype == PE_FP32 ? 8 : 6) ? vpl : 0;
 }
 
 }  // namespace

@@ -90,9 +90,10 @@ def _tag(dtype):
     return "fp32" if dtype == torch.float32 else "bf16"
 
 
-# Row widths 512 .. 2048 bytes for bf16 and 512 .. 4096 bytes for fp32.
+# Row widths 512 .. 3072 bytes for bf16 and 512 .. 4096 bytes for fp32.
 SHAPES = [(torch.bfloat16, 4, 64), (torch.bfloat16, 8, 64), (torch.bfloat16, 12, 64),
           (torch.bfloat16, 16, 64), (torch.bfloat16, 8, 32), (torch.bfloat16, 8, 128),
+          (torch.bfloat16, 10, 128), (torch.bfloat16, 24, 64),
           (torch.float32, 2, 64), (torch.float32, 8, 64), (torch.float32, 12, 64),
           (torch.float32, 16, 64), (torch.float32, 14, 64), (torch.float32, 16, 32),
           (torch.float32, 4, 128), (torch.float32, 10, 64)]
@@ -149,6 +150,18 @@ def test_streaming_first_token_backward_fallback_and_determinism():
     c = _bwd(args, cu_d, s, scale, workspace=minimal)
     for name, gs, gc in zip(("dq", "dk", "dv"), a, c):
         check_grad(gc, to64(gs), "bf16", f"fallback {name}")
+
+
+def test_wide_bf16_rows_fall_back_and_match():
+    """bf16 rows of 4096 bytes (16 heads of 128) are wider than the streaming
+    backward takes: they run the CUDA-core backward, with the same results."""
+    scale = 1.0 / np.sqrt(128)
+    lengths = _mixed_lengths(17)[:60]
+    x, s, cu, cu_d, args = _case(lengths, 16, 128, torch.bfloat16, seed=96, scale=scale)
+    dq, dk, dv = _bwd(args, cu_d, s, scale)
+    rq, rk, rv = _oracle(x, cu, args, scale)
+    for name, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        check_grad(got, want, "bf16", f"16x128 fallback {name}")
 
 
 def test_streaming_first_token_backward_single_sequence_and_tiny():
