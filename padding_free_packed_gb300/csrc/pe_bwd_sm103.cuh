@@ -331,23 +331,9 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             ok = false;
             break;
           }
-          if (kKeyPass) {
-            // -lse*log2e and -Delta of the block's 128 queries; -inf / 0 past
-            // the sequence end, so those columns get P = 0.
-            // A two-head item's columns 0-63 are head `head`'s queries at
-            // positions 0-63, columns 64-127 head + 1's.
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int r = lane + 32 * u;
-              const int32_t pos = it.dual ? (r & 63) : org + i * kRows + r;
-              const int32_t hd = it.dual ? it.head + (r >> 6) : it.head / kHalves;
-              const int64_t idx = static_cast<int64_t>(hd) * p.Nq + start + pos;
-              const bool in = pos < len;
-              S.vec[s][0][r] = in ? -__ldg(p.lse + idx) * kLog2e : -INFINITY;
-              S.vec[s][1][r] = in ? -__ldg(p.delta + idx) : 0.f;
-            }
-          }
-          __syncwarp();
+          // The tiles first, then (key pass) the block's lse and Delta: the
+          // global loads of those then overlap the copy instead of delaying it.
+          // The stage completes on the copy's bytes and the 32 lanes' arrivals.
           if (lane == 0) {
             mbar_arrive_expect_tx(smem_u32(&S.u_full[s]), 2 * kTileBytes);
             if (it.dual) {
@@ -364,6 +350,22 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tma_load_2d(smem_u32(S.u[s][1]) + b * kBoxBytes, u_map1, smem_u32(&S.u_full[s]),
                             x + 64 * b, start + org + i * kRows);
               }
+            }
+          }
+          if (kKeyPass) {
+            // -lse*log2e and -Delta of the block's 128 queries; -inf / 0 past
+            // the sequence end, so those columns get P = 0.
+            // A two-head item's columns 0-63 are head `head`'s queries at
+            // positions 0-63, columns 64-127 head + 1's.
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int r = lane + 32 * u;
+              const int32_t pos = it.dual ? (r & 63) : org + i * kRows + r;
+              const int32_t hd = it.dual ? it.head + (r >> 6) : it.head / kHalves;
+              const int64_t idx = static_cast<int64_t>(hd) * p.Nq + start + pos;
+              const bool in = pos < len;
+              S.vec[s][0][r] = in ? -__ldg(p.lse + idx) * kLog2e : -INFINITY;
+              S.vec[s][1][r] = in ? -__ldg(p.delta + idx) : 0.f;
             }
           }
           if (kKeyPass) mbar_arrive(smem_u32(&S.u_full[s]));
