@@ -180,3 +180,50 @@ def test_first_token_workspace_holds_the_partial_states(lib, dtype, b, n, h, d, 
     assert got == _plan_bytes(b) + extra
     # Without the first-token flag only the plan is needed.
     assert lib.pe_attention_workspace_size(dtype, b, n, h, d, s, 0, 0) == _plan_bytes(b)
+
+
+def _bwd_stream_sums(n, h, d):
+    chunk = 64
+    while -(-n // chunk) > 16384:
+        chunk *= 2
+    return _round16(-(-n // chunk) * 2 * h * d * 4)
+
+
+@pytest.mark.parametrize("dtype,b,n,h,d,s,streaming", [
+    (0, 32, 169151, 16, 64, 8192, True),     # long documents: 2 KiB bf16 rows
+    (0, 32, 169151, 24, 64, 8192, True),     # 3 KiB bf16 rows: the widest bf16 rows streamed
+    (0, 32, 169151, 16, 128, 8192, False),   # 4 KiB bf16 rows: CUDA-core backward
+    (1, 1024, 90487, 8, 64, 256, True),      # graph workload: 2 KiB fp32 rows
+    (1, 1024, 90487, 16, 64, 256, True),     # 4 KiB fp32 rows
+    (1, 1024, 90487, 20, 64, 256, False),    # 5 KiB fp32 rows: too wide
+    (0, 600, 2_000_000, 4, 64, 8192, True),  # past 16384 chunks of 64: chunk 128
+    (0, 10, 40000, 3, 64, 5000, False),      # 384-byte rows
+    (0, 10, 40000, 16, 96, 5000, False),     # head_dim 96
+])
+def test_first_token_backward_workspace_holds_the_chunk_sums(lib, dtype, b, n, h, d, s,
+                                                              streaming):
+    """First-token backwards need the plan and Delta [H, B] fp32; the streaming
+    form adds per-chunk dq sums (two H*d fp32 slots per token chunk) when a
+    token row is 512-byte loads up to 3 KiB in bf16 or 4 KiB in fp32 and
+    head_dim is 32, 64 or 128."""
+    got = lib.pe_attention_workspace_size(dtype, b, n, h, d, s, 1, 1)
+    base = _plan_bytes(b) + _round16(4 * h * b)
+    assert got == base + (_bwd_stream_sums(n, h, d) if streaming else 0)
+
+
+def test_kernel_families(lib):
+    """The kernel family each (dtype, head_dim, mode, direction) runs."""
+    lib.pe_attention_kernel.restype = ctypes.c_char_p
+    fam = lambda *a: lib.pe_attention_kernel(*a).decode()
+    assert fam(0, 64, 0, 0) == "tcgen05_bf16_d64"
+    assert fam(0, 128, 0, 0) == "tcgen05_bf16_d128"
+    assert fam(1, 64, 0, 0) == "tcgen05_f32_d64"
+    assert fam(1, 32, 0, 0) == "simt_ffma"
+    assert fam(0, 64, 1, 0) == "first_token_gemv"
+    assert fam(0, 64, 0, 1) == "tcgen05_bf16_d64_bwd"
+    assert fam(0, 128, 0, 1) == "tcgen05_bf16_d128_bwd"
+    assert fam(1, 64, 0, 1) == "simt_ffma_bwd"
+    assert fam(0, 64, 1, 1) == "first_token_bwd"
+    assert fam(1, 128, 1, 1) == "first_token_bwd"
+    assert fam(0, 96, 1, 1) == "simt_ffma_bwd"
+    assert fam(0, 12, 0, 0) == "unsupported"
