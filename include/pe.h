@@ -378,12 +378,10 @@ pe_status pe_geglu(pe_dtype dtype, const void* x, int64_t num_tokens, int32_t fe
  * pe_packed_attention_bwd (backward = 1) runs for these arguments (full
  * attention) on an sm_103a device: "tcgen05_bf16_d64", "tcgen05_bf16_d128",
  * "tcgen05_f32_d64", "simt_ffma", "first_token_gemv", "simt_ffma_bwd",
- * "tcgen05_bf16_d64_bwd", "tcgen05_bf16_d128_bwd" (full attention; local
- * windows at head_dim 128 run "simt_ffma_bwd"), "first_token_bwd", or
- * "unsupported". The two
- * first-token families cover both of their forms (streaming whole token rows
- * when the row shape and workspace allow it, per sequence and head
- * otherwise). A static string; never NULL. */
+ * "tcgen05_bf16_d64_bwd", "tcgen05_bf16_d128_bwd", "first_token_bwd", or
+ * "unsupported". The two first-token families cover both of their forms
+ * (streaming whole token rows when the row shape and workspace allow it, per
+ * sequence and head otherwise). A static string; never NULL. */
 const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_first_token,
                                 int backward);
 

@@ -253,10 +253,10 @@ extern "C" pe_status pe_packed_attention_bwd_local(
     return bwd_sm103(q, k, v, cu_seqlens, B, H, N, scale, win, lse, dout, delta, dq, dk, dv,
                      plan, chk, stream);
   }
-  if (dtype == PE_BF16 && D == 128 && !query_is_first_token && !win.active()) {
+  if (dtype == PE_BF16 && D == 128 && !query_is_first_token) {
     PE_TRY(bwd_preprocess(dtype, D, out, dout, N, H, delta, stream));
-    return bwd_sm103_d128(q, k, v, cu_seqlens, B, H, N, scale, lse, dout, delta, dq, dk, dv,
-                          plan, chk, stream);
+    return bwd_sm103_d128(q, k, v, cu_seqlens, B, H, N, scale, win, lse, dout, delta, dq, dk,
+                          dv, plan, chk, stream);
   }
   return bwd_simt(dtype, D, q, k, v, cu_seqlens, B, H, nq, scale, query_is_first_token, win, out,
                   lse, dout, dq, dk, dv, delta, plan, chk, stream);

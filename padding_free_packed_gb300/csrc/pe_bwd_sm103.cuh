@@ -42,8 +42,8 @@
 // 64 columns of dV and dK (the plan counts two items per key block and head).
 // The query pass needs no P, so its dQ accumulator takes 128 columns
 // [384,512). Two streaming stages of 64 KiB, and the epilogues store their
-// rows directly (no staging), so shared memory stays within bounds. Full
-// attention only, and no two-head items.
+// rows directly (no staging), so shared memory stays within bounds. No
+// two-head items.
 // With local attention an item streams only the blocks inside the window band
 // (key pass: the queries that can see its keys; query pass: the keys its rows
 // can see) and the elementwise step zeroes P outside each row's window.
@@ -773,11 +773,8 @@ pe_status launch_pass(const CUtensorMap (&m)[8], const BwdParams& prm, LayoutChe
   CUtensorMap mo1, mo2;
   PE_TRY(make_map_out<D>(&mo1, prm.out1, prm.Nq, prm.H));
   PE_TRY(make_map_out<D>(&mo2, kKeyPass ? prm.out2 : prm.out1, prm.Nq, prm.H));
-  // Local attention: head_dim 64 only.
-  auto kernel = bwd_sm103_kernel<D, kKeyPass, false>;
-  if constexpr (D == 64) {
-    if (prm.win.active()) kernel = bwd_sm103_kernel<D, kKeyPass, true>;
-  }
+  auto kernel = prm.win.active() ? bwd_sm103_kernel<D, kKeyPass, true>
+                                 : bwd_sm103_kernel<D, kKeyPass, false>;
   const size_t smem = sizeof(Smem<D>) + 1024;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));

@@ -106,11 +106,12 @@ pe_status bwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
                     const void* dout,
                     const float* delta, void* dq, void* dk, void* dv, TilePlan plan,
                     LayoutCheck check, cudaStream_t stream);
-// The same two passes for head_dim 128, full attention; each key-pass item
+// The same two passes for head_dim 128 (full or local); each key-pass item
 // accumulates one 64-column half of dK and dV.
 pe_status bwd_sm103_d128(const void* q, const void* k, const void* v, const int32_t* cu,
-                         int32_t B, int32_t H, int64_t N, float scale, const float* lse,
-                         const void* dout, const float* delta, void* dq, void* dk, void* dv,
-                         TilePlan plan, LayoutCheck check, cudaStream_t stream);
+                         int32_t B, int32_t H, int64_t N, float scale, Window win,
+                         const float* lse, const void* dout, const float* delta, void* dq,
+                         void* dk, void* dv, TilePlan plan, LayoutCheck check,
+                         cudaStream_t stream);
 
 }  // namespace pe

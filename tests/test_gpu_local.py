@@ -87,7 +87,7 @@ def test_local_first_token_query(dtype, d, right):
 
 
 @pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 64), (torch.float32, 64),
-                                     (torch.float32, 32)])
+                                     (torch.float32, 32), (torch.bfloat16, 128)])
 @pytest.mark.parametrize("window", [(64, 64), (0, 0), (3, 150), (200, 1), (-1, 30)])
 @pytest.mark.parametrize("first_token", [False, True])
 def test_local_backward_matches_oracle(dtype, d, window, first_token):
@@ -103,9 +103,17 @@ def test_local_backward_matches_oracle(dtype, d, window, first_token):
     dq, dk, dv = pe.pe_packed_attention_bwd_local(do, q, k, v, out, lse, cu_d, s, window[0],
                                                   window[1], scale,
                                                   query_is_first_token=first_token)
-    rq, rk, rv = oracle.attention_bwd(q.cpu(), x.k, x.v, do.cpu(), cu, scale,
-                                      first_token=first_token, window=window)
     tag = "fp32" if dtype == torch.float32 else "bf16"
+    saved = None
+    if tag == "bf16" and first_token:
+        # First-token bf16 gradients against the oracle's own output rounded to
+        # bf16, as the backward op forms Delta from the saved output (a
+        # near-cancelled dS_j takes its sign from that rounding).
+        ref_out, _ = oracle.attention_fwd(q.cpu(), x.k, x.v, cu, s, scale, first_token=True,
+                                          window=window)
+        saved = torch.from_numpy(ref_out).to(torch.bfloat16)
+    rq, rk, rv = oracle.attention_bwd(q.cpu(), x.k, x.v, do.cpu(), cu, scale,
+                                      first_token=first_token, window=window, out=saved)
     for name, got, want in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         check_grad(got, want, tag, f"local {name} {window} first_token={first_token}")
 
