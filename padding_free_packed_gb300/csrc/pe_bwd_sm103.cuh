@@ -20,6 +20,10 @@
 //                then a ring of streaming tile pairs (Q_i, dO_i or K_j, V_j);
 //                in the key pass the warp also stages each block's lse and
 //                Delta columns in shared memory.
+//   warp 5       scheduler: claims work items from the longest-first plan and
+//                decodes them into the two-slot item ring ahead of the
+//                producer, so that the claim's atomic and the plan and
+//                cu_seqlens reads are off the producer's per-item chain.
 //   warps 1, 2   issue the two score-shaped products (warp 1 owns tensor memory).
 //   warps 3, 4   issue the accumulations (warp 4 only in the key pass). A single
 //                thread issues one tcgen05.mma per ~130 cycles, hence four issuers.
@@ -188,7 +192,7 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&S.item_full[i]), 1);
-      mbar_init(smem_u32(&S.item_empty[i]), 2 + kAccWarps + 8);
+      mbar_init(smem_u32(&S.item_empty[i]), 1 + 2 + kAccWarps + 8);  // producer, issuers, elementwise
       mbar_init(smem_u32(&S.t_full[i]), 1);
       mbar_init(smem_u32(&S.acc_done[i]), 1);
     }
@@ -257,43 +261,11 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int s = 0; s < kStages; ++s) pending_u[s] = -1;
       bool ok = true;
       for (uint32_t item_no = 0; ok; ++item_no) {
-        const int slot = item_no & 1;
-        if (!warp_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
-                       p.status, kSiteProducer)) {
+        Item it;
+        if (!read_item(item_no, it, kSiteProducer)) {
           ok = false;
           break;
         }
-        Item it;
-        if (lane == 0) {
-          const int32_t t = atomicAdd(p.plan.counter, 1);
-          if (t >= total) {
-            it.seq = -1;
-            it.head = it.blk = it.dual = 0;
-          } else {
-            int32_t seq, local;
-            plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
-            const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
-            it.seq = seq;
-            if (len <= p.pair_heads_rows) {  // local indexes pairs of heads
-              it.head = 2 * local;
-              it.blk = 0;
-              it.dual = it.head + 1 < p.H;
-            } else {
-              // With head_dim 128 the key pass's plan counts each head twice
-              // (two halves of the head dimension): it.head is head * 2 + half.
-              const int32_t nb = (len + kRows - 1) / kRows;
-              it.head = local / nb;
-              it.blk = local - it.head * nb;
-              it.dual = 0;
-            }
-          }
-          S.items[slot] = it;
-          mbar_arrive(smem_u32(&S.item_full[slot]));
-        }
-        it.seq = __shfl_sync(0xffffffffu, it.seq, 0);
-        it.head = __shfl_sync(0xffffffffu, it.head, 0);
-        it.blk = __shfl_sync(0xffffffffu, it.blk, 0);
-        it.dual = __shfl_sync(0xffffffffu, it.dual, 0);
         if (it.seq < 0) break;
         const int32_t start = __ldg(p.cu + it.seq);
         const int32_t len = __ldg(p.cu + it.seq + 1) - start;
@@ -418,6 +390,44 @@ bwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       }
       tc_commit_warp(smem_u32(&S.drain[w]));
       mbar_drain_wait(smem_u32(&S.drain[w]), 0);
+    } else if (warp == 5) {
+      // ------------------------------------------------------------ scheduler (whole warp)
+      for (uint32_t item_no = 0;; ++item_no) {
+        const int slot = item_no & 1;
+        if (!warp_wait(smem_u32(&S.item_empty[slot]), ((item_no >> 1) & 1) ^ 1, abort_flag,
+                       p.status, kSiteProducer))
+          break;
+        int32_t claimed = -1;
+        if (lane == 0) {
+          Item it;
+          const int32_t t = atomicAdd(p.plan.counter, 1);
+          if (t >= total) {
+            it.seq = -1;
+            it.head = it.blk = it.dual = 0;
+          } else {
+            int32_t seq, local;
+            plan_decode(p.plan.order, p.plan.tile_end, p.B, t, seq, local);
+            const int32_t len = __ldg(p.cu + seq + 1) - __ldg(p.cu + seq);
+            it.seq = seq;
+            if (len <= p.pair_heads_rows) {  // local indexes pairs of heads
+              it.head = 2 * local;
+              it.blk = 0;
+              it.dual = it.head + 1 < p.H;
+            } else {
+              // With head_dim 128 the key pass's plan counts each head twice
+              // (two halves of the head dimension): it.head is head * 2 + half.
+              const int32_t nb = (len + kRows - 1) / kRows;
+              it.head = local / nb;
+              it.blk = local - it.head * nb;
+              it.dual = 0;
+            }
+          }
+          S.items[slot] = it;
+          mbar_arrive(smem_u32(&S.item_full[slot]));
+          claimed = it.seq;
+        }
+        if (__shfl_sync(0xffffffffu, claimed, 0) < 0) break;
+      }
     } else if (warp == 3 || (kKeyPass && warp == 4)) {
       // ------------------------------------------------------------ accumulations
       // key pass: warp 3 dV += P^T dO_i, warp 4 dK += dS^T Q_i;
