@@ -178,7 +178,11 @@ KERNEL_SOURCES = {"tcgen05_bf16_d64": ["pe_fwd_sm103.cu"] + _HEADERS,
                   "first_token_gemv": ["pe_first_token.cu", "pe_token_stream.cuh"] + _HEADERS,
                   "first_token_bwd": ["pe_first_token_bwd.cu", "pe_token_stream.cuh"] + _HEADERS,
                   "tcgen05_f32_d64": ["pe_fwd_sm103_f32.cu"] + _HEADERS,
-                  "tcgen05_bf16_d128": ["pe_fwd_sm103_d128.cu"] + _HEADERS}
+                  "tcgen05_bf16_d128": ["pe_fwd_sm103_d128.cu"] + _HEADERS,
+                  "tcgen05_bf16_d64_bwd": ["pe_bwd_sm103.cu", "pe_bwd_sm103.cuh",
+                                           "pe_bwd_simt.cu"] + _HEADERS,
+                  "tcgen05_bf16_d128_bwd": ["pe_bwd_sm103_d128.cu", "pe_bwd_sm103.cuh",
+                                            "pe_bwd_simt.cu"] + _HEADERS}
 
 
 # --------------------------------------------------------------------------- our arm
