@@ -240,9 +240,11 @@ def run_ours(args, rank, world):
     fwd_flops = real_flops(lengths, h, d, first_token=args.first_token, window=window)
     bwd_flops = 2.5 * fwd_flops if train else 0.0   # 10 sum L^2 H d: five GEMM-shaped products
     flops = fwd_flops + bwd_flops
-    kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token)
+    kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token,
+                                    window=window, max_seq_len=s)
     bwd_kernel = pe.pe_attention_kernel(wl.torch_dtype, d, query_is_first_token=args.first_token,
-                                        backward=True) if train else None
+                                        backward=True, window=window,
+                                        max_seq_len=s) if train else None
 
     # The per-step layout metadata: lengths, or the packed rows' mask.
     meta_host = row_ids if rows_layout else lengths

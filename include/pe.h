@@ -385,6 +385,18 @@ pe_status pe_geglu(pe_dtype dtype, const void* x, int64_t num_tokens, int32_t fe
 const char* pe_attention_kernel(pe_dtype dtype, int32_t head_dim, int query_is_first_token,
                                 int backward);
 
+/* The same for pe_packed_attention_fwd_local / pe_packed_attention_bwd_local
+ * with this window (window_left, window_right, max_seq_len as in those calls;
+ * a window that reaches every key is full attention). Local attention changes
+ * the family only for the forward of full-query calls: bf16 head_dim 64 keeps
+ * its tensor-core family ("tcgen05_bf16_d64", a local instance of the same
+ * kernel), every other forward runs "simt_ffma"; the backward families and
+ * the first-token families are those of pe_attention_kernel. max_seq_len < 1:
+ * "unsupported". A static string; never NULL. */
+const char* pe_attention_kernel_local(pe_dtype dtype, int32_t head_dim, int32_t max_seq_len,
+                                      int32_t window_left, int32_t window_right,
+                                      int query_is_first_token, int backward);
+
 /* ------------------------------------------------------------------------
  * Allocation-free forward. The pages have no counterpart to this call; it
  * exists for callers that cannot give the library a workspace: a host

@@ -29,7 +29,7 @@ EXPORTED = (
     "pe_rows_workspace_size", "pe_pack_document_ids", "pe_flatten_packed_metadata",
     "pe_packed_positions", "pe_rope_packed", "pe_layernorm", "pe_geglu", "pe_upload_packed",
     "pe_download_padded", "pe_packed_attention_fwd_noalloc", "pe_read_noalloc_status",
-    "pe_set_wait_limit_ns",
+    "pe_set_wait_limit_ns", "pe_attention_kernel_local",
 )
 
 _lib = None
@@ -104,6 +104,8 @@ def load_library(path: str = LIB_PATH):
     lib.pe_geglu.restype = c.c_int
     lib.pe_attention_kernel.argtypes = [c.c_int, i32, c.c_int, c.c_int]
     lib.pe_attention_kernel.restype = c.c_char_p
+    lib.pe_attention_kernel_local.argtypes = [c.c_int, i32, i32, i32, i32, c.c_int, c.c_int]
+    lib.pe_attention_kernel_local.restype = c.c_char_p
     lib.pe_read_device_status.argtypes = [vp, vp]
     lib.pe_read_device_status.restype = c.c_int
     lib.pe_read_noalloc_status.argtypes = [vp]
@@ -402,11 +404,19 @@ def _backward(window, dout, q, k, v, out, lse, cu_seqlens, max_seq_len, scale,
 
 
 def pe_attention_kernel(dtype: torch.dtype, head_dim: int, query_is_first_token: bool = False,
-                        backward: bool = False) -> str:
-    """Kernel family the forward (or backward) dispatches to for these arguments."""
-    return load_library().pe_attention_kernel(
-        _dtype_code(dtype), int(head_dim), int(bool(query_is_first_token)),
-        int(bool(backward))).decode()
+                        backward: bool = False, window=None, max_seq_len: int | None = None) -> str:
+    """Kernel family the forward (or backward) dispatches to for these arguments;
+    with window = (left, right) and max_seq_len, that of the local calls."""
+    lib = load_library()
+    if window is None:
+        return lib.pe_attention_kernel(
+            _dtype_code(dtype), int(head_dim), int(bool(query_is_first_token)),
+            int(bool(backward))).decode()
+    if max_seq_len is None:
+        raise ValueError("a window needs max_seq_len")
+    return lib.pe_attention_kernel_local(
+        _dtype_code(dtype), int(head_dim), int(max_seq_len), int(window[0]), int(window[1]),
+        int(bool(query_is_first_token)), int(bool(backward))).decode()
 
 
 def pe_read_device_status(workspace: torch.Tensor) -> int:

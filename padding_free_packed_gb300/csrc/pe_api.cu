@@ -1,5 +1,6 @@
 // C-ABI entry points of libpe: host-side argument checks, workspace layout and
 // dispatch to the kernel families. Every check runs before any launch.
+#include <cstring>
 #include <math.h>
 
 #include <atomic>
@@ -290,6 +291,20 @@ extern "C" const char* pe_attention_kernel(pe_dtype dtype, int32_t D, int query_
   if (dtype == PE_BF16 && D == 128) return "tcgen05_bf16_d128";
   if (dtype == PE_FP32 && D == 64) return "tcgen05_f32_d64";
   return "simt_ffma";
+}
+
+extern "C" const char* pe_attention_kernel_local(pe_dtype dtype, int32_t D, int32_t S,
+                                                int32_t window_left, int32_t window_right,
+                                                int query_is_first_token, int backward) {
+  const char* family = pe_attention_kernel(dtype, D, query_is_first_token, backward);
+  if (S < 1) return "unsupported";
+  // A window that reaches every key is full attention; first-token calls and
+  // the backward families take windows in their own kernels. Of the forward's
+  // tensor-core families only bf16 head_dim 64 has a local instance.
+  if (!make_window(window_left, window_right, S).active() || query_is_first_token || backward)
+    return family;
+  if (dtype == PE_BF16 && D == 64) return family;
+  return std::strcmp(family, "unsupported") == 0 ? family : "simt_ffma";
 }
 
 extern "C" uint64_t pe_set_wait_limit_ns(uint64_t ns) {

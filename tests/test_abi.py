@@ -227,3 +227,24 @@ def test_kernel_families(lib):
     assert fam(1, 128, 1, 1) == "first_token_bwd"
     assert fam(0, 96, 1, 1) == "simt_ffma_bwd"
     assert fam(0, 12, 0, 0) == "unsupported"
+
+
+def test_kernel_families_with_a_window(lib):
+    """Local calls: only the full-query forward changes family, and only off
+    bf16 head_dim 64; a window reaching every key is full attention."""
+    lib.pe_attention_kernel_local.restype = ctypes.c_char_p
+    fam = lambda *a: lib.pe_attention_kernel_local(*a).decode()
+    # (dtype, head_dim, max_seq_len, left, right, first_token, backward)
+    assert fam(0, 64, 8192, 64, 64, 0, 0) == "tcgen05_bf16_d64"
+    assert fam(0, 128, 8192, 64, 64, 0, 0) == "simt_ffma"
+    assert fam(1, 64, 8192, 64, 64, 0, 0) == "simt_ffma"
+    assert fam(1, 64, 8192, -1, -1, 0, 0) == "tcgen05_f32_d64"
+    assert fam(0, 128, 100, 99, 200, 0, 0) == "tcgen05_bf16_d128"   # reaches every key
+    assert fam(0, 128, 100, 98, -1, 0, 0) == "simt_ffma"
+    assert fam(0, 64, 8192, 64, 64, 0, 1) == "tcgen05_bf16_d64_bwd"
+    assert fam(0, 128, 8192, 64, 64, 0, 1) == "tcgen05_bf16_d128_bwd"
+    assert fam(1, 64, 8192, 64, 64, 0, 1) == "simt_ffma_bwd"
+    assert fam(1, 64, 8192, 64, 64, 1, 0) == "first_token_gemv"
+    assert fam(0, 64, 8192, 0, 64, 1, 1) == "first_token_bwd"
+    assert fam(0, 12, 8192, 64, 64, 0, 0) == "unsupported"
+    assert fam(0, 64, 0, 64, 64, 0, 0) == "unsupported"
