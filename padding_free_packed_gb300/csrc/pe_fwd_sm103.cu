@@ -94,13 +94,17 @@ constexpr uint32_t kHalfTileBytes = kTileBytes / 2;  // 64 rows
 // written to HBM by one TMA store.
 constexpr uint32_t kStageWarpBytes = 32 * kD * 2;
 
+// kQSlots sets of the two Q tiles. With two (local attention, whose items
+// are a few key blocks each) the next item's Q loads while this item's last
+// QK products are still to be issued; full attention keeps one set.
+template <int kQSlots>
 struct alignas(1024) Smem {
-  __nv_bfloat16 q[2][kRows * kD];
+  __nv_bfloat16 q[kQSlots][2][kRows * kD];
   __nv_bfloat16 k[kStages][kRows * kD];
   __nv_bfloat16 v[kStages][kRows * kD];
   alignas(1024) uint8_t ostage[8][kStageWarpBytes];   // per softmax warp, on the way to HBM
   uint64_t item_full[2], item_empty[2];
-  uint64_t q_full, q_empty;
+  uint64_t q_full[kQSlots], q_empty[kQSlots];
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_full[2];
   uint64_t drain[kIssueWarps];
@@ -108,6 +112,11 @@ struct alignas(1024) Smem {
   uint32_t tmem_base;
   WaitGuard guard;
 };
+
+// Plus the runtime 1024-byte alignment pad, within the 227 KiB a block may use.
+static_assert(sizeof(Smem<2>) + 1024 <= 227 * 1024, "shared memory per block");
+template <bool kLocal>
+using FwdSmem = Smem<kLocal ? 2 : 1>;
 
 struct FwdParams {
   const int32_t* cu;
@@ -254,7 +263,9 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                  const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
+  constexpr int kQSlots = kLocal ? 2 : 1;
+  FwdSmem<kLocal>& S =
+      *reinterpret_cast<FwdSmem<kLocal>*>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile WaitGuard* abort_flag = &S.guard;
 
@@ -268,8 +279,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mbar_init(smem_u32(&S.p_full[i]), 4);
       mbar_init(smem_u32(&S.o_full[i]), 1);
     }
-    mbar_init(smem_u32(&S.q_full), 1);
-    mbar_init(smem_u32(&S.q_empty), 1);            // the QK issuer, after an item's last QK
+    for (int i = 0; i < kQSlots; ++i) {
+      mbar_init(smem_u32(&S.q_full[i]), 1);
+      mbar_init(smem_u32(&S.q_empty[i]), 1);       // the QK issuer, after an item's last QK
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&S.k_full[s]), 1);
       mbar_init(smem_u32(&S.v_full[s]), 1);
@@ -305,7 +318,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         uint32_t kv_no = 0;
-        int pending_q = -1;                // parity of the last Q load not yet known complete
+        int pending_q[kQSlots];            // per Q slot: parity of the last load not yet known complete
+        for (int i = 0; i < kQSlots; ++i) pending_q[i] = -1;
         int pending_k[kStages], pending_v[kStages];  // parity of the last K / V load per stage
         for (int s = 0; s < kStages; ++s) pending_k[s] = pending_v[s] = -1;
         bool ok = true;
@@ -334,29 +348,32 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const ItemRange ir = item_range<kLocal>(p, len, r0, it.multi, ntiles);
           const int32_t nkv = ir.nkv;
           const int32_t x = it.head * kD;
-          if (!mbar_wait(smem_u32(&S.q_empty), (item_no & 1) ^ 1, abort_flag, p.status,
+          // Q slot qs was last read by the QK products of item item_no - kQSlots.
+          const int qs = item_no % kQSlots;
+          const uint32_t q_par = (item_no / kQSlots) & 1;
+          if (!mbar_wait(smem_u32(&S.q_empty[qs]), q_par ^ 1, abort_flag, p.status,
                          kSiteProducer)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(smem_u32(&S.q_full), ntiles * kTileBytes);
+          const uint32_t q_bar = smem_u32(&S.q_full[qs]);
+          mbar_arrive_expect_tx(q_bar, ntiles * kTileBytes);
           // Multi-head items load every tile (and K/V block) from the
           // sequence's first row: one head's columns per tile, or two heads'
           // in 64-row halves.
           for (int tt = 0; tt < ntiles; ++tt) {
             if (it.multi == kTwoHeadsPerTile) {
               for (int hh = 0; hh < 2; ++hh)
-                tma_load_2d(smem_u32(S.q[tt]) + hh * kHalfTileBytes, &tm_q64, smem_u32(&S.q_full),
+                tma_load_2d(smem_u32(S.q[qs][tt]) + hh * kHalfTileBytes, &tm_q64, q_bar,
                             packed_head(p, it, tt, hh) * kD, start);
             } else if (it.multi == kTailPair) {  // both tiles: rows r0.., heads head + tt
-              tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full), x + tt * kD,
-                          start + r0);
+              tma_load_2d(smem_u32(S.q[qs][tt]), &tm_q, q_bar, x + tt * kD, start + r0);
             } else {
-              tma_load_2d(smem_u32(S.q[tt]), &tm_q, smem_u32(&S.q_full),
-                          it.multi ? x + tt * kD : x, it.multi ? start : start + r0 + tt * kRows);
+              tma_load_2d(smem_u32(S.q[qs][tt]), &tm_q, q_bar, it.multi ? x + tt * kD : x,
+                          it.multi ? start : start + r0 + tt * kRows);
             }
           }
-          pending_q = item_no & 1;
+          pending_q[qs] = static_cast<int>(q_par);
           for (int32_t j = 0; j < nkv; ++j, ++kv_no) {
             const int s = kv_no % kStages;
             const uint32_t ph = (kv_no / kStages) & 1;
@@ -395,7 +412,8 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         if (!ok) {
           // Let every copy this thread started land before the CTA exits.
-          if (pending_q >= 0) mbar_drain_wait(smem_u32(&S.q_full), (uint32_t)pending_q);
+          for (int i = 0; i < kQSlots; ++i)
+            if (pending_q[i] >= 0) mbar_drain_wait(smem_u32(&S.q_full[i]), (uint32_t)pending_q[i]);
           for (int s = 0; s < kStages; ++s) {
             if (pending_k[s] >= 0) mbar_drain_wait(smem_u32(&S.k_full[s]), (uint32_t)pending_k[s]);
             if (pending_v[s] >= 0) mbar_drain_wait(smem_u32(&S.v_full[s]), (uint32_t)pending_v[s]);
@@ -424,7 +442,10 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int ntiles = item_tiles(p, it, len);
         const ItemRange ir = item_range<kLocal>(p, len, r0, it.multi, ntiles);
         const int32_t nkv = ir.nkv;
-        if (!warp_wait(smem_u32(&S.q_full), item_no & 1, abort_flag, p.status, kSiteMma)) break;
+        const int qs = item_no % kQSlots;
+        if (!warp_wait(smem_u32(&S.q_full[qs]), (item_no / kQSlots) & 1, abort_flag, p.status,
+                       kSiteMma))
+          break;
         for (int32_t j = 0; j < nkv && ok; ++j) {
           const uint32_t c = kv_no + j;
           const int s = c % kStages;
@@ -444,7 +465,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               break;
             }
             tc_fence_after();
-            const uint32_t q_addr = smem_u32(S.q[t]);
+            const uint32_t q_addr = smem_u32(S.q[qs][t]);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               mma_ss_warp(tmem + col_s(t), smem_desc_sw128(q_addr + kk * 32, 16, 1024),
@@ -456,7 +477,7 @@ fwd_sm103_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           tc_commit_warp(smem_u32(&S.k_empty[s]));  // K_j no longer needed by either tile
         }
         kv_no += nkv;
-        if (ok) tc_commit_warp(smem_u32(&S.q_empty));
+        if (ok) tc_commit_warp(smem_u32(&S.q_empty[qs]));
       }
       // Every MMA this warp issued must finish before tensor memory is freed.
       tc_commit_warp(smem_u32(&S.drain[0]));
@@ -786,7 +807,7 @@ pe_status fwd_sm103(const void* q, const void* k, const void* v, const int32_t* 
   PE_TRY(make_map(&mq64, q, N, H, 64));
   PE_TRY(make_map(&mk64, k, N, H, 64));
   PE_TRY(make_map(&mv64, v, N, H, 64));
-  const size_t smem = sizeof(Smem) + 1024;
+  const size_t smem = (win.active() ? sizeof(FwdSmem<true>) : sizeof(FwdSmem<false>)) + 1024;
   auto kernel = win.active() ? fwd_sm103_kernel<true> : fwd_sm103_kernel<false>;
   PE_CUDA_TRY(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(smem)));
