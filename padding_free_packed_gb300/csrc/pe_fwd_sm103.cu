@@ -36,11 +36,9 @@
 // share an item instead, each tile against its own head's key blocks (which
 // alternate in the K/V ring). With local attention (a window of key positions
 // around each query position) an item visits only the key blocks its rows can
-// see, and the softmax masks each row to its window; the local instance keeps
-// two sets of Q tiles, one per item slot, so that the next item's Q loads
-// while this item's last QK products are still to be issued. Keys past the
-// sequence end are masked to -inf; query rows past it are computed but never
-// stored. TMA zero-fills rows beyond the packed buffer.
+// see, and the softmax masks each row to its window. Keys past the sequence end are masked to -inf;
+// query rows past it are computed but never stored. TMA zero-fills rows
+// beyond the packed buffer.
 //
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) P0 [256,320)
 // P1 [320,384) O0 [384,448) O1 [448,512).
