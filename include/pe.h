@@ -65,7 +65,8 @@ const char* pe_status_string(int status);
  * pe_packed_positions, pe_rope_packed, pe_layernorm, pe_geglu, pe_upload_packed;
  * later additions within 2: pe_download_padded; 3 added the device-side
  * layout check of the attention calls, pe_set_wait_limit_ns and
- * pe_read_noalloc_status). */
+ * pe_read_noalloc_status; later additions within 3:
+ * pe_attention_kernel_local). */
 int pe_abi_version(void);
 
 /* ------------------------------------------------------------------------

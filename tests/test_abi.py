@@ -248,3 +248,46 @@ def test_kernel_families_with_a_window(lib):
     assert fam(0, 64, 8192, 0, 64, 1, 1) == "first_token_bwd"
     assert fam(0, 12, 8192, 64, 64, 0, 0) == "unsupported"
     assert fam(0, 64, 0, 64, 64, 0, 0) == "unsupported"
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "pe.h"
+
+int main(void) {
+  int code;
+  printf("abi %d\n", pe_abi_version());
+  for (code = 0; code <= 7; ++code) printf("status %d %s\n", code, pe_status_string(code));
+  printf("ws %lu\n", (unsigned long)pe_attention_workspace_size(PE_BF16, 3, 6, 2, 64, 3, 0, 1));
+  printf("family %s\n", pe_attention_kernel(PE_BF16, 64, 0, 0));
+  printf("local %s\n", pe_attention_kernel_local(PE_FP32, 64, 8192, 64, 64, 0, 0));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links_from_c(lib, tmp_path):
+    """A C99 program (gcc, -Wall -Wextra -pedantic -Werror) includes the header,
+    links the library and calls its host-only entry points; what it prints
+    matches the same calls made through ctypes."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    from padding_free_packed_gb300 import binding
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(binding.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lpe", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    lines = out.splitlines()
+    assert lines[0] == f"abi {lib.pe_abi_version()}"
+    lib.pe_status_string.restype = ctypes.c_char_p
+    for code in range(8):
+        assert lines[1 + code] == f"status {code} {lib.pe_status_string(code).decode()}"
+    assert lines[9] == f"ws {lib.pe_attention_workspace_size(0, 3, 6, 2, 64, 3, 0, 1)}"
+    assert lines[10] == "family tcgen05_bf16_d64"
+    assert lines[11] == "local simt_ffma"
